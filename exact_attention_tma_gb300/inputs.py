@@ -1,0 +1,86 @@
+"""Seeded synthetic inputs for the attention workloads.
+
+This module draws random numbers and nothing else: it holds none of the
+attention arithmetic, so both the CUDA path and the fp64 oracle can take
+their inputs from it.  Inputs are drawn in fp32 from one CPU
+``torch.Generator`` seeded per workload, in the order Q, K, V (decode: q, K,
+V), then rounded to bf16 with torch's round-to-nearest-even.  The oracle reads
+those bf16 values (exact in fp64), so parity errors measure the kernels only.
+
+The named workloads are the five shapes the attention path is specified on:
+a tiny non-causal forward, a causal forward, a non-causal forward with peaky
+scores and uniform V, a long-sequence causal forward and a split-KV decode
+against a long cache.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    kind: str            # "fwd" or "decode"
+    B: int
+    H: int
+    N: int               # sequence length (fwd) or cache length L (decode)
+    d: int
+    causal: bool
+    seed: int
+    qk_std: float = 1.0  # Q and K are N(0, qk_std^2)
+    v_dist: str = "normal"   # "normal": N(0,1); "uniform": U(-1, 1)
+    nsplit: int = 0      # decode only: KV splits per head
+    scale: float = field(default=0.0)
+
+    def __post_init__(self):
+        if self.scale == 0.0:
+            object.__setattr__(self, "scale", 1.0 / math.sqrt(self.d))
+
+
+WORKLOADS = {
+    "tiny_fwd": Workload("tiny_fwd", "fwd", 1, 2, 256, 64, False, 0),
+    "causal_fwd": Workload("causal_fwd", "fwd", 4, 16, 2048, 128, True, 1),
+    "noncausal_fwd": Workload("noncausal_fwd", "fwd", 8, 32, 4096, 64, False, 2,
+                              qk_std=1.5, v_dist="uniform"),
+    "long_causal_fwd": Workload("long_causal_fwd", "fwd", 1, 32, 16384, 128, True, 3),
+    "decode": Workload("decode", "decode", 16, 32, 8192, 128, False, 4, nsplit=32),
+}
+
+
+def _draw(gen: torch.Generator, shape, std: float, dist: str) -> torch.Tensor:
+    if dist == "normal":
+        x = torch.randn(shape, generator=gen, dtype=torch.float32)
+        if std != 1.0:
+            x = x * std
+        return x
+    if dist == "uniform":
+        return torch.rand(shape, generator=gen, dtype=torch.float32) * 2.0 - 1.0
+    raise ValueError(f"unknown distribution {dist!r}")
+
+
+def fwd_inputs(B: int, H: int, N: int, d: int, seed: int, qk_std: float = 1.0,
+               v_dist: str = "normal", device="cpu"):
+    """Q, K, V as contiguous bf16 [B, H, N, d] tensors on ``device``."""
+    gen = torch.Generator(device="cpu").manual_seed(seed)
+    q = _draw(gen, (B, H, N, d), qk_std, "normal").to(torch.bfloat16)
+    k = _draw(gen, (B, H, N, d), qk_std, "normal").to(torch.bfloat16)
+    v = _draw(gen, (B, H, N, d), 1.0, v_dist).to(torch.bfloat16)
+    return q.to(device), k.to(device), v.to(device)
+
+
+def decode_inputs(B: int, H: int, L: int, d: int, seed: int, device="cpu"):
+    """q [B, H, d] and Kcache, Vcache [B, H, L, d], all bf16 on ``device``."""
+    gen = torch.Generator(device="cpu").manual_seed(seed)
+    q = _draw(gen, (B, H, d), 1.0, "normal").to(torch.bfloat16)
+    k = _draw(gen, (B, H, L, d), 1.0, "normal").to(torch.bfloat16)
+    v = _draw(gen, (B, H, L, d), 1.0, "normal").to(torch.bfloat16)
+    return q.to(device), k.to(device), v.to(device)
+
+
+def workload_inputs(w: Workload, device="cpu"):
+    if w.kind == "fwd":
+        return fwd_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_std, w.v_dist, device)
+    return decode_inputs(w.B, w.H, w.N, w.d, w.seed, device)

@@ -1,0 +1,214 @@
+"""fp64 CPU oracle for exact attention (ctypes wrapper over attn_oracle.c).
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference leg of ``bench.py`` may import this package.  The
+product library (``exact_attention_tma_gb300``) never imports it, and this
+package imports nothing from the product.
+
+The arithmetic lives in ``attn_oracle.c`` (plain loops, fp64, single-threaded
+per head; S and P materialised).  This wrapper only marshals numpy arrays and,
+for many heads, runs independent per-head calls on a thread pool (ctypes drops
+the GIL during each call, so heads run in parallel on the host cores).
+
+Definition followed: "Why fast GPUs still wait for memory", section
+"Attention from first principles" (S = QK^T, P = softmax(S), O = PV), with the
+readings on scale, causal alignment, LSE and split-KV stated in the C file.
+Every function here is pinned by ``tests/test_oracle.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+_lock = threading.Lock()
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_lp = ctypes.POINTER(ctypes.c_long)
+
+
+def build(force: bool = False) -> str:
+    """Compile attn_oracle.c into liboracle.so with gcc (no fast-math)."""
+    if force or not os.path.exists(_LIB_PATH) or (
+        os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)
+    ):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-o", tmp, _SRC, "-lm"]
+        )
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            lib.oracle_attention.argtypes = [
+                _dp, ctypes.c_long, _dp, _dp, ctypes.c_long, ctypes.c_long,
+                ctypes.c_double, ctypes.c_int, _lp, ctypes.c_long,
+                _dp, _dp, _dp, _dp,
+            ]
+            lib.oracle_decode.argtypes = [
+                _dp, _dp, _dp, ctypes.c_long, ctypes.c_long, ctypes.c_double, _dp, _dp,
+            ]
+            lib.oracle_decode_split.argtypes = [
+                _dp, _dp, _dp, ctypes.c_long, ctypes.c_long, ctypes.c_double,
+                ctypes.c_long, _dp, _dp,
+            ]
+            lib.oracle_lse_combine.argtypes = [
+                _dp, _dp, ctypes.c_long, ctypes.c_long, _dp, _dp,
+            ]
+            for fn in (lib.oracle_attention, lib.oracle_decode,
+                       lib.oracle_decode_split, lib.oracle_lse_combine):
+                fn.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(_dp)
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != 0:
+        raise RuntimeError(f"{what} failed with oracle status {rc}")
+
+
+def attention_head(Q, K, V, scale: float, causal: bool, rows=None,
+                   return_p: bool = False):
+    """One head: Q (nq,d), K/V (nk,d).  Returns (O, LSE[, P, rowsum_err]).
+
+    ``rows`` selects query rows (default: all).  P is (len(rows), nk).
+    """
+    lib = _load()
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    nq, d = Q.shape
+    nk = K.shape[0]
+    if rows is None:
+        rows_arr = None
+        nrows = nq
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        nrows = rows_arr.shape[0]
+    O = np.empty((nrows, d), np.float64)
+    LSE = np.empty((nrows,), np.float64)
+    P = np.empty((nrows, nk), np.float64) if return_p else None
+    err = ctypes.c_double(0.0)
+    rc = lib.oracle_attention(
+        _ptr(Q), nq, _ptr(K), _ptr(V), nk, d, float(scale), int(bool(causal)),
+        rows_arr.ctypes.data_as(_lp) if rows_arr is not None else None, nrows,
+        _ptr(O), _ptr(LSE), _ptr(P) if P is not None else None, ctypes.byref(err),
+    )
+    _check(rc, "oracle_attention")
+    if return_p:
+        return O, LSE, P, err.value
+    return O, LSE
+
+
+def attention(Q, K, V, scale: float, causal: bool, rows=None, heads=None,
+              threads: int | None = None):
+    """Batched heads: Q/K/V (..., N, d).  Returns O (..., R, d), LSE (..., R).
+
+    ``heads`` optionally lists flat head indices (over the leading dims) to
+    compute; the result then has shape (len(heads), R, d).  ``rows`` selects
+    query rows for every head.  Heads run on ``threads`` host threads.
+    """
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    lead = Q.shape[:-2]
+    N, d = Q.shape[-2:]
+    Qf = Q.reshape(-1, N, d)
+    Kf = K.reshape(-1, K.shape[-2], d)
+    Vf = V.reshape(-1, V.shape[-2], d)
+    hs = list(range(Qf.shape[0])) if heads is None else list(heads)
+    R = N if rows is None else len(rows)
+    O = np.empty((len(hs), R, d), np.float64)
+    LSE = np.empty((len(hs), R), np.float64)
+
+    def one(t):
+        h = hs[t]
+        O[t], LSE[t] = attention_head(Qf[h], Kf[h], Vf[h], scale, causal, rows)
+
+    _run(one, len(hs), threads)
+    if heads is None:
+        return O.reshape(*lead, R, d), LSE.reshape(*lead, R)
+    return O, LSE
+
+
+def decode(q, K, V, scale: float, heads=None, threads: int | None = None):
+    """Decode: q (..., d), K/V (..., L, d).  Returns O (..., d), LSE (...)."""
+    lib = _load()
+    q, K, V = _f64(q), _f64(K), _f64(V)
+    lead = q.shape[:-1]
+    d = q.shape[-1]
+    L = K.shape[-2]
+    qf = q.reshape(-1, d)
+    Kf = K.reshape(-1, L, d)
+    Vf = V.reshape(-1, L, d)
+    hs = list(range(qf.shape[0])) if heads is None else list(heads)
+    O = np.empty((len(hs), d), np.float64)
+    LSE = np.empty((len(hs),), np.float64)
+
+    def one(t):
+        h = hs[t]
+        o = np.empty((d,), np.float64)
+        lse = np.empty((1,), np.float64)
+        rc = lib.oracle_decode(_ptr(qf[h]), _ptr(Kf[h]), _ptr(Vf[h]), L, d,
+                               float(scale), _ptr(o), _ptr(lse))
+        _check(rc, "oracle_decode")
+        O[t], LSE[t] = o, lse[0]
+
+    _run(one, len(hs), threads)
+    if heads is None:
+        return O.reshape(*lead, d), LSE.reshape(lead)
+    return O, LSE
+
+
+def decode_split(q, K, V, scale: float, nsplit: int):
+    """One head's split-KV partials: returns O_s (nsplit, d), lse_s (nsplit)."""
+    lib = _load()
+    q, K, V = _f64(q), _f64(K), _f64(V)
+    L, d = K.shape
+    O_s = np.empty((nsplit, d), np.float64)
+    lse_s = np.empty((nsplit,), np.float64)
+    rc = lib.oracle_decode_split(_ptr(q), _ptr(K), _ptr(V), L, d, float(scale),
+                                 nsplit, _ptr(O_s), _ptr(lse_s))
+    _check(rc, "oracle_decode_split")
+    return O_s, lse_s
+
+
+def lse_combine(O_s, lse_s):
+    """Combine normalised partials: returns O (d), LSE (scalar)."""
+    lib = _load()
+    O_s, lse_s = _f64(O_s), _f64(lse_s)
+    nsplit, d = O_s.shape
+    O = np.empty((d,), np.float64)
+    lse = np.empty((1,), np.float64)
+    rc = lib.oracle_lse_combine(_ptr(O_s), _ptr(lse_s), nsplit, d, _ptr(O), _ptr(lse))
+    _check(rc, "oracle_lse_combine")
+    return O, lse[0]
+
+
+def _run(fn, n: int, threads: int | None) -> None:
+    if n == 0:
+        return
+    threads = threads or min(n, os.cpu_count() or 1)
+    if threads <= 1 or n == 1:
+        for t in range(n):
+            fn(t)
+        return
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(fn, range(n)))

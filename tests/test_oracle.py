@@ -1,0 +1,243 @@
+"""Pins for the fp64 CPU oracle (no GPU).
+
+The oracle is checked against things fixed by the definition of attention
+("Why fast GPUs still wait for memory", section 'Attention from first
+principles': S = QK^T, P = softmax(S), O = PV), not against itself:
+hand-worked closed forms (tests/golden/hand_cases.json), invariants that hold
+for any input (rows of P sum to one, masked entries are exactly zero,
+permutation of keys/values, identical keys, constant V, causal row 0), the
+split-KV identity, and brute force in 50-digit arithmetic without the
+max-shift on tiny random inputs.  Each pin is chosen so that a plausible slip
+in the oracle (dropped scale, transposed operand, wrong mask index, natural
+vs base-2 log, missing max add-back, wrong combine weight) fails one of them.
+"""
+import json
+import math
+import os
+
+import mpmath
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_cases.json")
+_NS = {"e": math.e, "ln": math.log, "sqrt": math.sqrt, "inf": math.inf}
+
+
+def _ev(expr):
+    return float(eval(expr, {"__builtins__": {}}, _NS))
+
+
+def _golden():
+    with open(GOLDEN) as f:
+        return json.load(f)
+
+
+@pytest.mark.parametrize("case", _golden()["cases"], ids=lambda c: c["name"])
+def test_hand_cases(case):
+    O, LSE = oracle.attention_head(case["Q"], case["K"], case["V"], case["scale"],
+                                   case["causal"])
+    O_exp = np.array([[_ev(x) for x in row] for row in case["O"]])
+    LSE_exp = np.array([_ev(x) for x in case["LSE"]])
+    np.testing.assert_allclose(O, O_exp, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(LSE, LSE_exp, rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("case", _golden()["decode_cases"], ids=lambda c: c["name"])
+def test_decode_hand_cases(case):
+    O, LSE = oracle.decode(case["q"], case["K"], case["V"], case["scale"])
+    np.testing.assert_allclose(O, [_ev(x) for x in case["O"]], rtol=0, atol=1e-14)
+    assert abs(float(LSE) - _ev(case["LSE"])) < 1e-14
+    O_s, lse_s = oracle.decode_split(case["q"], case["K"], case["V"], case["scale"],
+                                     case["nsplit"])
+    np.testing.assert_allclose(O_s, [[_ev(x) for x in r] for r in case["O_s"]],
+                               rtol=0, atol=1e-14)
+    for got, want in zip(lse_s, case["lse_s"]):
+        w = _ev(want)
+        if w == -math.inf:
+            assert got == -math.inf
+        else:
+            assert abs(got - w) < 1e-14
+    O_c, LSE_c = oracle.lse_combine(O_s, lse_s)
+    np.testing.assert_allclose(O_c, [_ev(x) for x in case["O"]], rtol=0, atol=1e-14)
+    assert abs(LSE_c - _ev(case["LSE"])) < 1e-14
+
+
+def _rand(rng, n, d, std=1.0):
+    return rng.standard_normal((n, d)) * std
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_rows_of_p_sum_to_one_and_mask_is_exact(causal):
+    rng = np.random.default_rng(11)
+    N, d = 37, 8
+    Q, K, V = _rand(rng, N, d, 2.0), _rand(rng, N, d, 2.0), _rand(rng, N, d)
+    O, LSE, P, err = oracle.attention_head(Q, K, V, 0.7, causal, return_p=True)
+    assert err < 1e-14
+    np.testing.assert_allclose(P.sum(axis=1), 1.0, atol=1e-14, rtol=0)
+    assert (P >= 0).all()
+    if causal:
+        assert (P[np.triu_indices(N, 1)] == 0.0).all()
+        assert (P[np.tril_indices(N)] > 0.0).all()
+    else:
+        assert (P > 0).all()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("zero_q", [False, True])
+def test_identical_keys_give_mean_of_v(causal, zero_q):
+    rng = np.random.default_rng(5)
+    N, d, scale = 23, 6, 0.37
+    Q = np.zeros((N, d)) if zero_q else _rand(rng, N, d)
+    k = rng.standard_normal(d)
+    K = np.tile(k, (N, 1))
+    V = _rand(rng, N, d)
+    O, LSE = oracle.attention_head(Q, K, V, scale, causal)
+    for i in range(N):
+        n_vis = i + 1 if causal else N
+        np.testing.assert_allclose(O[i], V[:n_vis].mean(axis=0), atol=1e-13, rtol=0)
+        s = scale * float(Q[i] @ k)
+        assert abs(LSE[i] - (s + math.log(n_vis))) < 1e-13
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_constant_v_gives_constant_output(causal):
+    rng = np.random.default_rng(7)
+    N, d = 19, 5
+    v = rng.standard_normal(d)
+    O, _ = oracle.attention_head(_rand(rng, N, d, 3.0), _rand(rng, N, d, 3.0),
+                                 np.tile(v, (N, 1)), 0.5, causal)
+    np.testing.assert_allclose(O, np.tile(v, (N, 1)), atol=1e-13, rtol=0)
+
+
+def test_causal_row0_is_v0():
+    rng = np.random.default_rng(9)
+    N, d, scale = 16, 4, 0.81
+    Q, K, V = _rand(rng, N, d), _rand(rng, N, d), _rand(rng, N, d)
+    O, LSE = oracle.attention_head(Q, K, V, scale, True)
+    assert (O[0] == V[0]).all()
+    assert abs(LSE[0] - scale * float(Q[0] @ K[0])) < 1e-15
+
+
+def test_permuting_keys_and_values_together_is_invariant():
+    rng = np.random.default_rng(13)
+    N, d = 29, 7
+    Q, K, V = _rand(rng, N, d), _rand(rng, N, d), _rand(rng, N, d)
+    perm = rng.permutation(N)
+    O1, L1 = oracle.attention_head(Q, K, V, 0.4, False)
+    O2, L2 = oracle.attention_head(Q, K[perm], V[perm], 0.4, False)
+    np.testing.assert_allclose(O1, O2, atol=1e-13, rtol=0)
+    np.testing.assert_allclose(L1, L2, atol=1e-13, rtol=0)
+
+
+def test_large_scores_stay_finite():
+    # Identical keys with huge scores: exp without the shift would overflow.
+    N, d = 8, 2
+    Q = np.full((N, d), 30.0)
+    K = np.full((N, d), 30.0)
+    V = np.arange(N * d, dtype=np.float64).reshape(N, d)
+    O, LSE = oracle.attention_head(Q, K, V, 1.0, False)
+    np.testing.assert_allclose(O, np.tile(V.mean(axis=0), (N, 1)), atol=1e-12, rtol=0)
+    np.testing.assert_allclose(LSE, 1800.0 + math.log(N), atol=1e-12, rtol=0)
+
+
+def test_row_subset_matches_full():
+    rng = np.random.default_rng(17)
+    N, d = 41, 9
+    Q, K, V = _rand(rng, N, d), _rand(rng, N, d), _rand(rng, N, d)
+    for causal in (False, True):
+        O, LSE = oracle.attention_head(Q, K, V, 0.3, causal)
+        rows = [40, 0, 17, 3]
+        Os, Ls = oracle.attention_head(Q, K, V, 0.3, causal, rows=rows)
+        np.testing.assert_array_equal(Os, O[rows])
+        np.testing.assert_array_equal(Ls, LSE[rows])
+
+
+@pytest.mark.parametrize("L,nsplit", [(1, 1), (1, 32), (7, 3), (64, 32), (100, 32),
+                                      (257, 32), (8192 // 16, 32)])
+def test_split_then_combine_equals_unsplit(L, nsplit):
+    rng = np.random.default_rng(L * 131 + nsplit)
+    d = 16
+    q, K, V = rng.standard_normal(d) * 2, _rand(rng, L, d, 2.0), _rand(rng, L, d)
+    O, LSE = oracle.decode(q, K, V, 0.25)
+    O_s, lse_s = oracle.decode_split(q, K, V, 0.25, nsplit)
+    O_c, LSE_c = oracle.lse_combine(O_s, lse_s)
+    np.testing.assert_allclose(O_c, O, atol=1e-12, rtol=0)
+    assert abs(LSE_c - float(LSE)) < 1e-12
+    chunk = -(-L // nsplit)
+    for s in range(nsplit):
+        if s * chunk >= L:
+            assert lse_s[s] == -math.inf and (O_s[s] == 0).all()
+
+
+def _brute(Q, K, V, scale, causal):
+    """Softmax in 50-digit arithmetic with no max shift (independent of the C code)."""
+    mpmath.mp.dps = 50
+    nq, d = len(Q), len(Q[0])
+    nk = len(K)
+    O = np.zeros((nq, d))
+    LSE = np.zeros(nq)
+    for i in range(nq):
+        w = []
+        for j in range(nk):
+            if causal and j > i:
+                w.append(mpmath.mpf(0))
+                continue
+            dot = mpmath.fsum(mpmath.mpf(float(Q[i][k])) * mpmath.mpf(float(K[j][k]))
+                              for k in range(d))
+            w.append(mpmath.exp(mpmath.mpf(scale) * dot))
+        z = mpmath.fsum(w)
+        for k in range(d):
+            O[i, k] = float(mpmath.fsum(w[j] * mpmath.mpf(float(V[j][k]))
+                                        for j in range(nk)) / z)
+        LSE[i] = float(mpmath.log(z))
+    return O, LSE
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_bruteforce_tiny_random(seed):
+    rng = np.random.default_rng(1000 + seed)
+    N = int(rng.integers(1, 9))
+    d = int(rng.integers(1, 5))
+    scale = float(rng.uniform(0.1, 2.0))
+    Q, K, V = _rand(rng, N, d, 1.5), _rand(rng, N, d, 1.5), _rand(rng, N, d)
+    for causal in (False, True):
+        O, LSE = oracle.attention_head(Q, K, V, scale, causal)
+        Ob, Lb = _brute(Q, K, V, scale, causal)
+        np.testing.assert_allclose(O, Ob, atol=1e-13, rtol=0)
+        np.testing.assert_allclose(LSE, Lb, atol=1e-13, rtol=0)
+
+
+def test_rectangular_noncausal_bruteforce():
+    # Decode is the one-row, non-causal case against a longer key list.
+    rng = np.random.default_rng(77)
+    L, d = 11, 3
+    q, K, V = rng.standard_normal(d), _rand(rng, L, d), _rand(rng, L, d)
+    O, LSE = oracle.decode(q, K, V, 0.9)
+    Ob, Lb = _brute([q], K, V, 0.9, False)
+    np.testing.assert_allclose(O, Ob[0], atol=1e-13, rtol=0)
+    assert abs(float(LSE) - Lb[0]) < 1e-13
+
+
+def test_batched_wrapper_matches_per_head():
+    rng = np.random.default_rng(3)
+    B, H, N, d = 2, 3, 10, 4
+    Q = rng.standard_normal((B, H, N, d))
+    K = rng.standard_normal((B, H, N, d))
+    V = rng.standard_normal((B, H, N, d))
+    O, LSE = oracle.attention(Q, K, V, 0.5, True, threads=3)
+    for b in range(B):
+        for h in range(H):
+            o, l = oracle.attention_head(Q[b, h], K[b, h], V[b, h], 0.5, True)
+            np.testing.assert_array_equal(O[b, h], o)
+            np.testing.assert_array_equal(LSE[b, h], l)
+
+
+def test_bad_arguments_are_rejected():
+    with pytest.raises(RuntimeError):
+        # causal needs as many queries as keys
+        oracle.attention_head(np.ones((2, 2)), np.ones((3, 2)), np.ones((3, 2)), 1.0, True)
+    with pytest.raises(RuntimeError):
+        oracle.attention_head(np.ones((2, 2)), np.ones((2, 2)), np.ones((2, 2)), 1.0,
+                              False, rows=[5])
