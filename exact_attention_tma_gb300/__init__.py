@@ -1,0 +1,188 @@
+"""GB300-native exact attention: Python binding of the C ABI in include/exact_attn.h.
+
+Every function here only marshals arguments (checks dtypes, shapes and
+contiguity, passes device pointers and the CUDA stream handle) and calls the
+same-named entry point of ``lib/libexact_attn.so``; all arithmetic runs in the
+library's sm_103a kernels.  There is no CPU fallback: if the library is not
+built, the first call raises.  Build it with ``python -m
+exact_attention_tma_gb300.build`` (or ``__graft_entry__.build()``).
+
+PyTorch is used only to hold device memory and to name the stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "AttnError", "attn_fwd", "attn_decode", "attn_decode_ws",
+    "attn_decode_workspace_bytes", "attn_get_device_status", "attn_status_string",
+    "attn_decode_num_splits", "forward", "decode", "library_path", "load",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "lib", "libexact_attn.so")
+_lib = None
+_lock = threading.Lock()
+
+ATTN_OK = 0
+
+
+class AttnError(RuntimeError):
+    """A non-OK attn_status returned by the library."""
+
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {attn_status_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load libexact_attn.so (once).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    f"CUDA library {_LIB_PATH} is missing; build it with "
+                    "`python -m exact_attention_tma_gb300.build`")
+            lib = ctypes.CDLL(_LIB_PATH)
+            vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+            lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+            lib.attn_decode.argtypes = [vp, vp, vp, vp, i, i, i, i, f, vp]
+            lib.attn_decode_ws.argtypes = [vp, vp, vp, vp, i, i, i, i, f, vp, sz, vp]
+            lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i]
+            lib.attn_decode_workspace_bytes.restype = sz
+            lib.attn_get_device_status.argtypes = [vp]
+            lib.attn_status_string.argtypes = [i]
+            lib.attn_status_string.restype = ctypes.c_char_p
+            lib.attn_decode_num_splits.argtypes = []
+            for fn in (lib.attn_fwd, lib.attn_decode, lib.attn_decode_ws,
+                       lib.attn_get_device_status, lib.attn_decode_num_splits):
+                fn.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _stream(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev(t, name, dtype):
+    import torch
+
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _check(status: int, what: str) -> None:
+    if status != ATTN_OK:
+        raise AttnError(status, what)
+
+
+def attn_status_string(status: int) -> str:
+    return load().attn_status_string(int(status)).decode()
+
+
+def attn_decode_num_splits() -> int:
+    return load().attn_decode_num_splits()
+
+
+def attn_fwd(Q, K, V, O, LSE, causal: bool, scale: float, stream=None) -> None:
+    """O, LSE <- attention(Q, K, V); all [B, H, N, d] bf16 (LSE [B, H, N] fp32)."""
+    import torch
+
+    B, H, N, d = Q.shape
+    for name, t in (("K", K), ("V", V), ("O", O)):
+        if tuple(t.shape) != (B, H, N, d):
+            raise ValueError(f"{name} shape {tuple(t.shape)} != Q shape {(B, H, N, d)}")
+    if tuple(LSE.shape) != (B, H, N):
+        raise ValueError(f"LSE shape {tuple(LSE.shape)} != {(B, H, N)}")
+    args = [_dev(Q, "Q", torch.bfloat16), _dev(K, "K", torch.bfloat16),
+            _dev(V, "V", torch.bfloat16), _dev(O, "O", torch.bfloat16),
+            _dev(LSE, "LSE", torch.float32)]
+    _check(load().attn_fwd(*args, B, H, N, d, float(scale), int(bool(causal)),
+                           _stream(stream)), "attn_fwd")
+
+
+def attn_decode(q, Kcache, Vcache, O, scale: float, stream=None) -> None:
+    """O [B, H, d] <- attention of q [B, H, d] over Kcache/Vcache [B, H, L, d]."""
+    import torch
+
+    B, H, L, d = Kcache.shape
+    if tuple(Vcache.shape) != (B, H, L, d):
+        raise ValueError("Vcache shape must match Kcache")
+    for name, t in (("q", q), ("O", O)):
+        if tuple(t.shape) != (B, H, d):
+            raise ValueError(f"{name} shape {tuple(t.shape)} != {(B, H, d)}")
+    args = [_dev(q, "q", torch.bfloat16), _dev(Kcache, "Kcache", torch.bfloat16),
+            _dev(Vcache, "Vcache", torch.bfloat16), _dev(O, "O", torch.bfloat16)]
+    _check(load().attn_decode(*args, B, H, L, d, float(scale), _stream(stream)),
+           "attn_decode")
+
+
+def attn_decode_workspace_bytes(B: int, H: int, L: int, d: int) -> int:
+    return int(load().attn_decode_workspace_bytes(B, H, L, d))
+
+
+def attn_decode_ws(q, Kcache, Vcache, O, scale: float, ws, stream=None) -> None:
+    """attn_decode with a caller-owned workspace tensor ``ws`` (any dtype, CUDA)."""
+    import torch
+
+    B, H, L, d = Kcache.shape
+    if tuple(Vcache.shape) != (B, H, L, d):
+        raise ValueError("Vcache shape must match Kcache")
+    for name, t in (("q", q), ("O", O)):
+        if tuple(t.shape) != (B, H, d):
+            raise ValueError(f"{name} shape {tuple(t.shape)} != {(B, H, d)}")
+    if not (isinstance(ws, torch.Tensor) and ws.is_cuda and ws.is_contiguous()):
+        raise ValueError("ws must be a contiguous CUDA tensor")
+    args = [_dev(q, "q", torch.bfloat16), _dev(Kcache, "Kcache", torch.bfloat16),
+            _dev(Vcache, "Vcache", torch.bfloat16), _dev(O, "O", torch.bfloat16)]
+    nbytes = ws.numel() * ws.element_size()
+    _check(load().attn_decode_ws(*args, B, H, L, d, float(scale),
+                                 ctypes.c_void_p(ws.data_ptr()), nbytes, _stream(stream)),
+           "attn_decode_ws")
+
+
+def attn_get_device_status(stream=None) -> int:
+    """Synchronise ``stream`` and return (and clear) the device status code."""
+    return int(load().attn_get_device_status(_stream(stream)))
+
+
+def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
+    """Allocate O and LSE on q's device and run attn_fwd.  Returns (O, LSE)."""
+    import torch
+
+    B, H, N, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    attn_fwd(q, k, v, o, lse, causal, d ** -0.5 if scale is None else scale, stream)
+    return o, lse
+
+
+def decode(q, Kcache, Vcache, scale: float | None = None, stream=None):
+    """Allocate O on q's device and run attn_decode.  Returns O [B, H, d]."""
+    import torch
+
+    o = torch.empty_like(q)
+    d = q.shape[-1]
+    attn_decode(q, Kcache, Vcache, o, d ** -0.5 if scale is None else scale, stream)
+    return o

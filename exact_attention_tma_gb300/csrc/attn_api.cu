@@ -1,0 +1,163 @@
+// attn_api.cu — the C ABI declared in include/exact_attn.h.
+//
+// Host-side only: argument validation (nothing is launched for an invalid
+// call), the per-device status word that bounded device waits report into,
+// the library-owned decode workspace, and dispatch to the kernel launchers.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "exact_attn.h"
+#include "internal.h"
+
+namespace {
+
+// Device status word: kernels OR in ea::kStatusTimeoutBit when a bounded wait
+// gives up.  One per device (each device gets its own copy of the module).
+__device__ unsigned int g_attn_status;
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxLen = 1 << 24;
+
+std::mutex g_mu;
+unsigned *g_status_ptr[kMaxDevices];
+void *g_ws_ptr[kMaxDevices];
+size_t g_ws_bytes[kMaxDevices];
+
+attn_status current_device(int *dev) {
+  if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+// Device address of this device's status word (looked up once per device).
+attn_status status_ptr(unsigned **out) {
+  int dev;
+  attn_status st = current_device(&dev);
+  if (st != ATTN_OK) return st;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_attn_status) != cudaSuccess || !p) return ATTN_ERR_CUDA;
+    g_status_ptr[dev] = static_cast<unsigned *>(p);
+  }
+  *out = g_status_ptr[dev];
+  return ATTN_OK;
+}
+
+bool misaligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+attn_status check_common(int B, int H, int len, int d, float scale) {
+  if (B < 1 || H < 1 || len < 1 || len > kMaxLen) return ATTN_ERR_SHAPE;
+  if (static_cast<long long>(B) * H > (1LL << 24)) return ATTN_ERR_SHAPE;
+  if (d != 64 && d != 128) return ATTN_ERR_HEADDIM;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_ARG;
+  return ATTN_OK;
+}
+
+attn_status check_decode(const void *q, const void *K, const void *V, const void *O, int B, int H,
+                         int L, int d, float scale) {
+  if (!q || !K || !V || !O) return ATTN_ERR_NULL;
+  attn_status st = check_common(B, H, L, d, scale);
+  if (st != ATTN_OK) return st;
+  if (misaligned(q) || misaligned(K) || misaligned(V) || misaligned(O)) return ATTN_ERR_ALIGN;
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
+                     int H, int N, int d, float scale, int causal, cudaStream_t stream) {
+  if (!Q || !K || !V || !O || !LSE) return ATTN_ERR_NULL;
+  attn_status st = check_common(B, H, N, d, scale);
+  if (st != ATTN_OK) return st;
+  if (causal != 0 && causal != 1) return ATTN_ERR_ARG;
+  // One CTA per (head, 128-row query tile) must fit a 1-D grid.
+  if (static_cast<long long>(B) * H * ((N + 127) / 128) >= (1LL << 31)) return ATTN_ERR_SHAPE;
+  if (misaligned(Q) || misaligned(K) || misaligned(V) || misaligned(O) ||
+      (reinterpret_cast<uintptr_t>(LSE) & 3u) != 0)
+    return ATTN_ERR_ALIGN;
+  unsigned *status = nullptr;
+  st = status_ptr(&status);
+  if (st != ATTN_OK) return st;
+  cudaError_t e = ea::launch_fwd(Q, K, V, O, LSE, B, H, N, d, scale, causal, status, stream);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+size_t attn_decode_workspace_bytes(int B, int H, int L, int d) {
+  if (check_common(B, H, L, d, 1.f) != ATTN_OK) return 0;
+  return ea::decode_ws_bytes(B, H, d);
+}
+
+attn_status attn_decode_ws(const void *q, const void *Kcache, const void *Vcache, void *O, int B,
+                           int H, int L, int d, float scale, void *ws, size_t ws_bytes,
+                           cudaStream_t stream) {
+  attn_status st = check_decode(q, Kcache, Vcache, O, B, H, L, d, scale);
+  if (st != ATTN_OK) return st;
+  if (!ws) return ATTN_ERR_NULL;
+  if (misaligned(ws)) return ATTN_ERR_ALIGN;
+  if (ws_bytes < ea::decode_ws_bytes(B, H, d)) return ATTN_ERR_NOMEM;
+  cudaError_t e = ea::launch_decode(q, Kcache, Vcache, O, B, H, L, d, scale, ws, stream);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status attn_decode(const void *q, const void *Kcache, const void *Vcache, void *O, int B,
+                        int H, int L, int d, float scale, cudaStream_t stream) {
+  attn_status st = check_decode(q, Kcache, Vcache, O, B, H, L, d, scale);
+  if (st != ATTN_OK) return st;
+  int dev;
+  st = current_device(&dev);
+  if (st != ATTN_OK) return st;
+  const size_t need = ea::decode_ws_bytes(B, H, d);
+  void *ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_ws_bytes[dev] < need) {
+      // Grow-only workspace; cudaFree waits for work already using the old one.
+      if (g_ws_ptr[dev]) cudaFree(g_ws_ptr[dev]);
+      g_ws_ptr[dev] = nullptr;
+      g_ws_bytes[dev] = 0;
+      if (cudaMalloc(&g_ws_ptr[dev], need) != cudaSuccess) {
+        g_ws_ptr[dev] = nullptr;
+        return ATTN_ERR_NOMEM;
+      }
+      g_ws_bytes[dev] = need;
+    }
+    ws = g_ws_ptr[dev];
+  }
+  cudaError_t e = ea::launch_decode(q, Kcache, Vcache, O, B, H, L, d, scale, ws, stream);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status attn_get_device_status(cudaStream_t stream) {
+  unsigned *p = nullptr;
+  attn_status st = status_ptr(&p);
+  if (st != ATTN_OK) return st;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  unsigned v = 0;
+  const unsigned zero = 0;
+  if (cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (v != 0 && cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return (v & ea::kStatusTimeoutBit) ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+const char *attn_status_string(attn_status status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_NULL: return "a required pointer is NULL";
+    case ATTN_ERR_SHAPE: return "B, H, N or L out of range";
+    case ATTN_ERR_HEADDIM: return "head dimension must be 64 or 128";
+    case ATTN_ERR_ALIGN: return "a tensor pointer is not 16-byte aligned";
+    case ATTN_ERR_CUDA: return "a CUDA call or kernel launch failed";
+    case ATTN_ERR_NOMEM: return "workspace allocation failed or workspace too small";
+    case ATTN_ERR_TIMEOUT: return "a bounded device-side wait expired";
+    case ATTN_ERR_ARG: return "invalid argument (scale must be finite and > 0, causal 0 or 1)";
+  }
+  return "unknown status";
+}
+
+int attn_decode_num_splits(void) { return ea::kDecodeSplits; }
+
+}  // extern "C"

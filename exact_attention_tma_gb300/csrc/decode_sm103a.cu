@@ -1,0 +1,246 @@
+// decode_sm103a.cu — split-KV single-token decode for GB300 (sm_103a).
+//
+// One query row per (batch, head) against a KV cache of L keys, following
+// "Why fast GPUs still wait for memory", section "Attention III · KV cache,
+// GQA, MLA": W = 4Ld flops against 2*2*L*d bytes of K and V, an intensity of
+// one flop per byte, so the kernel is bound by HBM bandwidth and its job is
+// to stream K and V exactly once with as many bytes in flight as possible.
+// Parallelism moves from the (collapsed) query axis to KV splits, as the
+// prefill/decode example of "M4.2 GPU Execution Model" (operation atlas)
+// describes, with the split's partial outputs reduced afterwards (schedule
+// table of its section 0x08: "split-K ... partial-output reduction,
+// workspace").
+//
+// Kernel 1 (split): one CTA per (head, split), 4 warps.  Keys are cut into 32
+// chunks of ceil(L/32).  Inside a warp, d/8 consecutive lanes own one key row
+// (16-byte coalesced loads, lane -> 8 consecutive head-dim elements, as in
+// the K[B,H,T,d_h] lane mapping of M4.2's coalescing section); a warp-shuffle
+// butterfly finishes each q.k dot product.  Each lane keeps an online-softmax
+// state (running max, sum, 8 accumulators) in base 2; the 4 warps x (32 / (d/8))
+// lane groups are merged through shared memory into the split's normalised
+// partial O_s and its log-sum-exp, written to the fp32 workspace.
+// Kernel 2 (combine): one warp per head merges its 32 partials with weights
+// 2^(lse_s - max lse) and writes bf16 O.
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace ea {
+namespace dec {
+
+constexpr int kWarps = 4;
+constexpr int kUnroll = 8;   // 16-byte loads of K and of V in flight per lane per batch
+
+template <int D>
+__global__ void __launch_bounds__(kWarps * 32)
+    attn_decode_split_kernel(const __nv_bfloat16 *__restrict__ q,
+                             const __nv_bfloat16 *__restrict__ Kc,
+                             const __nv_bfloat16 *__restrict__ Vc, float *__restrict__ ws_o,
+                             float *__restrict__ ws_lse, int L, int chunk, int nsplit,
+                             float scale_log2) {
+  constexpr int LPK = D / 8;          // lanes per key row
+  constexpr int KPI = 32 / LPK;       // keys per warp-wide load
+  constexpr int G = kWarps * KPI;     // lane groups per CTA
+  constexpr int BATCH = kWarps * KPI * kUnroll;
+  // 1-D grid: consecutive CTAs read consecutive chunks of one head.
+  const int split = blockIdx.x % nsplit;
+  const int bh = blockIdx.x / nsplit;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / LPK;         // which key of the warp-wide load
+  const int dl = lane % LPK;          // which 8-element slice of the head dim
+
+  const int lo = split * chunk;
+  const int hi = min(L, lo + chunk);
+
+  // q slice for this lane, in fp32.
+  float qf[8];
+  {
+    const uint4 qv = *reinterpret_cast<const uint4 *>(q + static_cast<size_t>(bh) * D + dl * 8);
+    const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      qf[2 * e] = bf16lo(w[e]);
+      qf[2 * e + 1] = bf16hi(w[e]);
+    }
+  }
+
+  const size_t head_off = static_cast<size_t>(bh) * L * D;
+  const __nv_bfloat16 *Kh = Kc + head_off + dl * 8;
+  const __nv_bfloat16 *Vh = Vc + head_off + dl * 8;
+
+  float m = -INFINITY, lsum = 0.f;
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+
+  for (int base = lo; base < hi; base += BATCH) {
+    uint4 kr[kUnroll], vr[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int key = base + (warp * kUnroll + u) * KPI + sub;
+      if (key < hi) {
+        kr[u] = ld_stream_v4(Kh + static_cast<size_t>(key) * D);
+        vr[u] = ld_stream_v4(Vh + static_cast<size_t>(key) * D);
+      } else {
+        kr[u] = make_uint4(0, 0, 0, 0);
+        vr[u] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    float x[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const uint32_t w[4] = {kr[u].x, kr[u].y, kr[u].z, kr[u].w};
+      float part = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        part = fmaf(qf[2 * e], bf16lo(w[e]), part);
+        part = fmaf(qf[2 * e + 1], bf16hi(w[e]), part);
+      }
+#pragma unroll
+      for (int off = LPK / 2; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+      const int key = base + (warp * kUnroll + u) * KPI + sub;
+      x[u] = (key < hi) ? part * scale_log2 : -INFINITY;
+    }
+    float mb = x[0];
+#pragma unroll
+    for (int u = 1; u < kUnroll; ++u) mb = fmaxf(mb, x[u]);
+    const float m_new = fmaxf(m, mb);
+    if (m_new != -INFINITY) {
+      const float alpha = ex2_approx(m - m_new);
+      lsum *= alpha;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] *= alpha;
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const float p = ex2_approx(x[u] - m_new);
+        lsum += p;
+        const uint32_t w[4] = {vr[u].x, vr[u].y, vr[u].z, vr[u].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          acc[2 * e] = fmaf(p, bf16lo(w[e]), acc[2 * e]);
+          acc[2 * e + 1] = fmaf(p, bf16hi(w[e]), acc[2 * e + 1]);
+        }
+      }
+      m = m_new;
+    }
+  }
+
+  // Merge the G lane-group states of this CTA.
+  __shared__ float sm_m[G], sm_l[G];
+  __shared__ float sm_acc[G][D];
+  const int g = warp * KPI + sub;
+  if (dl == 0) {
+    sm_m[g] = m;
+    sm_l[g] = lsum;
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) sm_acc[g][dl * 8 + e] = acc[e];
+  __syncthreads();
+  const size_t part = static_cast<size_t>(bh) * nsplit + split;
+  for (int t = threadIdx.x; t < D; t += blockDim.x) {
+    float mx = sm_m[0];
+#pragma unroll
+    for (int i = 1; i < G; ++i) mx = fmaxf(mx, sm_m[i]);
+    if (mx == -INFINITY) {   // empty split
+      ws_o[part * D + t] = 0.f;
+      if (t == 0) ws_lse[part] = -INFINITY;
+      continue;
+    }
+    float den = 0.f, num = 0.f;
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+      const float w = ex2_approx(sm_m[i] - mx);
+      den = fmaf(sm_l[i], w, den);
+      num = fmaf(sm_acc[i][t], w, num);
+    }
+    ws_o[part * D + t] = num / den;
+    if (t == 0) {
+      float lg;
+      asm("lg2.approx.f32 %0, %1;" : "=f"(lg) : "f"(den));
+      ws_lse[part] = mx + lg;   // base-2 log-sum-exp of the split
+    }
+  }
+}
+
+// One warp per head: lane s holds split s's log-sum-exp (nsplit <= 32).
+template <int D>
+__global__ void __launch_bounds__(128)
+    attn_decode_combine_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_lse,
+                               __nv_bfloat16 *__restrict__ O, int BH, int nsplit) {
+  const int head = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (head >= BH) return;
+  const float lse = (lane < nsplit) ? ws_lse[static_cast<size_t>(head) * nsplit + lane] : -INFINITY;
+  float mx = lse;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  const float w = (lse == -INFINITY) ? 0.f : ex2_approx(lse - mx);
+  float wsum = w;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+  constexpr int E = D / 32;   // head-dim elements per lane
+  float o[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) o[e] = 0.f;
+  const float *base = ws_o + static_cast<size_t>(head) * nsplit * D + lane * E;
+  for (int s = 0; s < nsplit; ++s) {
+    const float ws = __shfl_sync(0xffffffffu, w, s);
+    if constexpr (E == 4) {
+      const float4 v = *reinterpret_cast<const float4 *>(base + static_cast<size_t>(s) * D);
+      o[0] = fmaf(ws, v.x, o[0]);
+      o[1] = fmaf(ws, v.y, o[1]);
+      o[2] = fmaf(ws, v.z, o[2]);
+      o[3] = fmaf(ws, v.w, o[3]);
+    } else {
+      const float2 v = *reinterpret_cast<const float2 *>(base + static_cast<size_t>(s) * D);
+      o[0] = fmaf(ws, v.x, o[0]);
+      o[1] = fmaf(ws, v.y, o[1]);
+    }
+  }
+  const float inv = 1.f / wsum;
+  __nv_bfloat16 *out = O + static_cast<size_t>(head) * D + lane * E;
+  if constexpr (E == 4) {
+    const uint32_t a = pack_bf16x2(o[0] * inv, o[1] * inv);
+    const uint32_t b = pack_bf16x2(o[2] * inv, o[3] * inv);
+    *reinterpret_cast<uint2 *>(out) = make_uint2(a, b);
+  } else {
+    *reinterpret_cast<uint32_t *>(out) = pack_bf16x2(o[0] * inv, o[1] * inv);
+  }
+}
+
+template <int D>
+static cudaError_t launch_t(const void *q, const void *Kc, const void *Vc, void *O, int BH, int L,
+                            float scale_log2, void *ws, cudaStream_t stream) {
+  const int nsplit = kDecodeSplits;
+  const int chunk = (L + nsplit - 1) / nsplit;
+  float *ws_o = static_cast<float *>(ws);
+  float *ws_lse = ws_o + static_cast<size_t>(BH) * nsplit * D;
+  attn_decode_split_kernel<D><<<static_cast<unsigned>(BH) * nsplit, kWarps * 32, 0, stream>>>(
+      static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(Kc),
+      static_cast<const __nv_bfloat16 *>(Vc), ws_o, ws_lse, L, chunk, nsplit, scale_log2);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  attn_decode_combine_kernel<D><<<(BH + 3) / 4, 128, 0, stream>>>(
+      ws_o, ws_lse, static_cast<__nv_bfloat16 *>(O), BH, nsplit);
+  return cudaGetLastError();
+}
+
+}  // namespace dec
+
+size_t decode_ws_bytes(int B, int H, int d) {
+  const size_t parts = static_cast<size_t>(B) * H * kDecodeSplits;
+  return parts * static_cast<size_t>(d) * 4 + parts * 4;
+}
+
+cudaError_t launch_decode(const void *q, const void *Kc, const void *Vc, void *O, int B, int H,
+                          int L, int d, float scale, void *ws, cudaStream_t stream) {
+  const float scale_log2 = scale * 1.44269504088896340736f;
+  if (d == 128) return dec::launch_t<128>(q, Kc, Vc, O, B * H, L, scale_log2, ws, stream);
+  return dec::launch_t<64>(q, Kc, Vc, O, B * H, L, scale_log2, ws, stream);
+}
+
+}  // namespace ea

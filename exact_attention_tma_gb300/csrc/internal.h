@@ -1,0 +1,23 @@
+// internal.h — launchers shared between the C-ABI layer and the kernel files.
+#pragma once
+#include <cstddef>
+#include <cuda_runtime.h>
+
+namespace ea {
+
+// Bits of the device status word (see attn_get_device_status).
+constexpr unsigned kStatusTimeoutBit = 1u;
+
+// Forward: one launch of the fused tcgen05/TMA kernel.  Arguments are already
+// validated by the caller.  Returns cudaSuccess or the launch/encode error.
+cudaError_t launch_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
+                       int H, int N, int d, float scale, int causal, unsigned *status,
+                       cudaStream_t stream);
+
+// Decode: split kernel + combine kernel on `stream`, partials in `ws`.
+constexpr int kDecodeSplits = 32;
+size_t decode_ws_bytes(int B, int H, int d);
+cudaError_t launch_decode(const void *q, const void *Kc, const void *Vc, void *O, int B, int H,
+                          int L, int d, float scale, void *ws, cudaStream_t stream);
+
+}  // namespace ea

@@ -1,0 +1,131 @@
+/*
+ * exact_attn.h — C ABI of the GB300 (sm_103a) exact-attention library.
+ *
+ * The library computes exact scaled-dot-product attention,
+ *     O = softmax(scale * Q K^T + causal mask) V,
+ * as defined in "Why fast GPUs still wait for memory"
+ * (srini-anirudh.github.io), section "Attention from first principles"
+ * (S = QK^T, P = softmax(S), O = PV), computed the IO-aware way described in
+ * the section "FlashAttention is an IO algorithm" on the same page: K/V blocks
+ * stream through on-chip memory and a running maximum and normaliser rescale
+ * the output block, so the n x n score matrix never reaches HBM.  Causal
+ * masking follows that page's note "causal masking is not an optimisation
+ * here"; single-token decode follows its section "Attention III · KV cache,
+ * GQA, MLA"; split-KV decode with a partial-output reduction follows the
+ * schedule table of "M4.2 GPU Execution Model" (numinens.com), section 0x08
+ * ("split-K ... partial-output reduction, workspace") and its prefill/decode
+ * example in the operation atlas.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     never frees them and keeps no reference after the call returns.
+ *   - bf16 tensors are contiguous, row-major, head dimension innermost
+ *     ([B, H, N, d] for the forward, [B, H, L, d] for the caches), and must be
+ *     16-byte aligned.  d must be 64 or 128.
+ *   - Work is enqueued on `stream` and runs asynchronously: the call returns
+ *     after the launch without synchronising.  A NULL stream is the legacy
+ *     default stream.
+ *   - Arguments are validated on the host before anything is launched; an
+ *     invalid call returns an error code and launches nothing.
+ *   - Launch failures return ATTN_ERR_CUDA.  A device-side wait that exceeds
+ *     its bounded limit records ATTN_ERR_TIMEOUT in a device status word that
+ *     attn_get_device_status() reads and clears; the kernel then skips its
+ *     remaining work and exits cleanly instead of hanging.
+ *   - Every entry point may be called from several host threads.
+ */
+#ifndef EXACT_ATTN_H
+#define EXACT_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_NULL = 1,     /* a required pointer is NULL                        */
+    ATTN_ERR_SHAPE = 2,    /* B, H, N or L out of range (< 1 or too large)      */
+    ATTN_ERR_HEADDIM = 3,  /* d is not 64 or 128                                */
+    ATTN_ERR_ALIGN = 4,    /* a tensor pointer is not 16-byte aligned           */
+    ATTN_ERR_CUDA = 5,     /* a CUDA runtime/driver call or launch failed       */
+    ATTN_ERR_NOMEM = 6,    /* workspace allocation failed / too small           */
+    ATTN_ERR_TIMEOUT = 7,  /* a bounded device-side wait expired                */
+    ATTN_ERR_ARG = 8       /* another argument is invalid (scale, causal flag)  */
+} attn_status;
+
+/*
+ * attn_fwd — fused forward attention for B*H independent heads.
+ *
+ *   Q, K, V : bf16 [B, H, N, d], contiguous.
+ *   O       : bf16 [B, H, N, d] output, contiguous; O = P V / rowsum(P).
+ *   LSE     : fp32 [B, H, N] output; LSE[i] = ln sum_j exp(scale * q_i . k_j)
+ *             over the keys visible to query i (natural log, scale included).
+ *   N       : sequence length, 1 <= N <= 2^24 (queries and keys alike).
+ *   scale   : multiplies Q K^T before masking and softmax (finite, > 0).
+ *   causal  : 0 = every key visible; 1 = key j visible to query i iff j <= i.
+ *
+ * One persistent tcgen05/TMA kernel launch; no workspace; S and P stay on chip.
+ * O and LSE are written exactly once per element.  O must not alias Q, K or V.
+ */
+attn_status attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                     int B, int H, int N, int d, float scale, int causal,
+                     cudaStream_t stream);
+
+/*
+ * attn_decode — one query token per (batch, head) against a KV cache.
+ *
+ *   q       : bf16 [B, H, d].
+ *   Kcache  : bf16 [B, H, L, d];  Vcache : bf16 [B, H, L, d].
+ *   O       : bf16 [B, H, d] output.
+ *   L       : cache length, 1 <= L <= 2^24.  The new token follows the cache,
+ *             so all L keys are visible (no mask).
+ *
+ * Split-KV: each head's keys are cut into 32 chunks of ceil(L/32) keys; one
+ * launch computes every chunk's normalised partial output and log-sum-exp
+ * into a workspace, a second launch combines them with weights
+ * exp(lse_s - max_s lse_s).  The workspace is owned by the library: it is
+ * allocated on first use per device, grows when a larger call needs it and
+ * lives until process exit.  Growing it synchronises the device, so warm it up
+ * with the largest shape before capturing a CUDA graph.  Calls that share a
+ * device share that workspace, so concurrent calls on different streams of
+ * one device race; use attn_decode_ws with separate workspaces for that.
+ */
+attn_status attn_decode(const void *q, const void *Kcache, const void *Vcache, void *O,
+                        int B, int H, int L, int d, float scale, cudaStream_t stream);
+
+/* Bytes of workspace attn_decode_ws needs for this shape (0 if invalid). */
+size_t attn_decode_workspace_bytes(int B, int H, int L, int d);
+
+/*
+ * attn_decode_ws — attn_decode with a caller-owned device workspace of at
+ * least attn_decode_workspace_bytes(B, H, L, d) bytes, 16-byte aligned.
+ * Returns ATTN_ERR_NOMEM if ws_bytes is too small.  The workspace holds fp32
+ * partials only while the call's two launches run; the caller may reuse it
+ * for another call on the same stream afterwards.
+ */
+attn_status attn_decode_ws(const void *q, const void *Kcache, const void *Vcache, void *O,
+                           int B, int H, int L, int d, float scale, void *ws,
+                           size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * attn_get_device_status — synchronises `stream`, then reads and clears the
+ * library's device status word on the current device.  Returns ATTN_OK, or
+ * ATTN_ERR_TIMEOUT if any kernel since the last call gave up on a bounded
+ * wait, or ATTN_ERR_CUDA if synchronisation itself failed.
+ */
+attn_status attn_get_device_status(cudaStream_t stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char *attn_status_string(attn_status status);
+
+/* Number of KV splits attn_decode uses per head (32). */
+int attn_decode_num_splits(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACT_ATTN_H */

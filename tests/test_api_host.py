@@ -1,0 +1,118 @@
+"""Host-side tests of the C ABI (no GPU needed).
+
+The library must load and export every function include/exact_attn.h
+declares, and every invalid call must be rejected by host validation with the
+documented status code before any CUDA call or launch happens (so fake,
+never-dereferenced pointers are enough here).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_attention_tma_gb300 as ea
+from exact_attention_tma_gb300 import build as ea_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+OK, NULL, SHAPE, HEADDIM, ALIGN, CUDA, NOMEM, TIMEOUT, ARG = range(9)
+P = 0x10000  # fake 16-byte-aligned device address (never dereferenced)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ea_build.build()
+    return ea.load()
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(HEADER_DIR):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(HEADER_DIR, fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*[A-Za-z_][\w\s\*]*?\b(attn_\w+)\s*\(", text, re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert {"attn_fwd", "attn_decode", "attn_decode_ws", "attn_get_device_status",
+            "attn_status_string", "attn_decode_workspace_bytes",
+            "attn_decode_num_splits"} <= names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_status_strings(lib):
+    for code in range(9):
+        s = ea.attn_status_string(code)
+        assert isinstance(s, str) and s
+    assert ea.attn_status_string(99) == "unknown status"
+
+
+def test_decode_workspace_bytes(lib):
+    nsplit = ea.attn_decode_num_splits()
+    assert nsplit == 32
+    assert ea.attn_decode_workspace_bytes(16, 32, 8192, 128) == 16 * 32 * nsplit * (128 + 1) * 4
+    assert ea.attn_decode_workspace_bytes(1, 1, 1, 64) == nsplit * 65 * 4
+    assert ea.attn_decode_workspace_bytes(1, 1, 1, 96) == 0
+    assert ea.attn_decode_workspace_bytes(0, 1, 1, 64) == 0
+
+
+def _fwd(lib, Q=P, K=P, V=P, O=P, L=P, B=1, H=1, N=128, d=64, scale=0.125, causal=0):
+    vp = ctypes.c_void_p
+    return lib.attn_fwd(vp(Q), vp(K), vp(V), vp(O), vp(L), B, H, N, d, scale, causal, None)
+
+
+def _dec(lib, q=P, K=P, V=P, O=P, B=1, H=1, L=128, d=64, scale=0.125):
+    vp = ctypes.c_void_p
+    return lib.attn_decode(vp(q), vp(K), vp(V), vp(O), B, H, L, d, scale, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Q=0), NULL), (dict(K=0), NULL), (dict(V=0), NULL), (dict(O=0), NULL),
+    (dict(L=0), NULL),
+    (dict(B=0), SHAPE), (dict(H=-1), SHAPE), (dict(N=0), SHAPE), (dict(N=(1 << 24) + 1), SHAPE),
+    (dict(B=1 << 13, H=1 << 12), SHAPE),
+    (dict(d=96), HEADDIM), (dict(d=256), HEADDIM), (dict(d=0), HEADDIM),
+    (dict(Q=P + 8), ALIGN), (dict(K=P + 2), ALIGN), (dict(V=P + 4), ALIGN),
+    (dict(O=P + 1), ALIGN), (dict(L=P + 2), ALIGN),
+    (dict(scale=0.0), ARG), (dict(scale=-1.0), ARG), (dict(scale=float("nan")), ARG),
+    (dict(scale=float("inf")), ARG), (dict(causal=2), ARG),
+])
+def test_fwd_rejects_bad_arguments_before_launch(lib, kw, code):
+    assert _fwd(lib, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), NULL), (dict(K=0), NULL), (dict(V=0), NULL), (dict(O=0), NULL),
+    (dict(B=0), SHAPE), (dict(L=0), SHAPE), (dict(L=(1 << 24) + 1), SHAPE),
+    (dict(d=32), HEADDIM),
+    (dict(q=P + 8), ALIGN), (dict(K=P + 8), ALIGN), (dict(V=P + 8), ALIGN), (dict(O=P + 2), ALIGN),
+    (dict(scale=0.0), ARG), (dict(scale=float("nan")), ARG),
+])
+def test_decode_rejects_bad_arguments_before_launch(lib, kw, code):
+    assert _dec(lib, **kw) == code
+
+
+def test_decode_ws_checks_workspace(lib):
+    vp = ctypes.c_void_p
+    need = ea.attn_decode_workspace_bytes(2, 3, 100, 128)
+    assert lib.attn_decode_ws(vp(P), vp(P), vp(P), vp(P), 2, 3, 100, 128, 0.1, None, need,
+                              None) == NULL
+    assert lib.attn_decode_ws(vp(P), vp(P), vp(P), vp(P), 2, 3, 100, 128, 0.1, vp(P + 4), need,
+                              None) == ALIGN
+    assert lib.attn_decode_ws(vp(P), vp(P), vp(P), vp(P), 2, 3, 100, 128, 0.1, vp(P), need - 1,
+                              None) == NOMEM
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(ea, "_lib", None)
+    monkeypatch.setattr(ea, "_LIB_PATH", str(tmp_path / "nope.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        ea.load()

@@ -1,0 +1,136 @@
+"""GPU parity of the fused forward kernel against the fp64 oracle.
+
+Small shapes are compared element by element over every output (they span
+several 128-row / 128-key tiles and ragged tails); the full-size workloads
+are compared on sampled heads and rows that the oracle computes one by one,
+in the same launch configuration the bench uses.
+"""
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_tma_gb300 as ea
+from exact_attention_tma_gb300.inputs import WORKLOADS, fwd_inputs, workload_inputs
+from parity import assert_within, compare_fwd, oracle_fwd
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(cuda_ok):
+    from exact_attention_tma_gb300 import build
+
+    build.build()
+    ea.load()
+    yield
+    assert ea.attn_get_device_status() == 0
+
+
+def _run(q, k, v, causal, scale):
+    o, lse = ea.forward(q, k, v, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+def _full_check(B, H, N, d, causal, seed, qk_std=1.0, v_dist="normal"):
+    q, k, v = fwd_inputs(B, H, N, d, seed, qk_std, v_dist, device="cuda")
+    scale = d ** -0.5
+    o, lse = _run(q, k, v, causal, scale)
+    O_ref, L_ref = oracle_fwd(q, k, v, scale, causal)
+    st = compare_fwd(o, lse, O_ref, L_ref, range(B * H), None)
+    assert_within(st)
+    return st
+
+
+def test_tiny_workload_full():
+    w = WORKLOADS["tiny_fwd"]
+    q, k, v = workload_inputs(w, device="cuda")
+    o, lse = _run(q, k, v, w.causal, w.scale)
+    O_ref, L_ref = oracle_fwd(q, k, v, w.scale, w.causal)
+    assert_within(compare_fwd(o, lse, O_ref, L_ref, range(w.B * w.H), None))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 17, 127, 128, 129, 255, 300, 513])
+def test_small_shapes_full(N, d, causal):
+    _full_check(1, 2, N, d, causal, seed=100 + N)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_multi_head_multi_tile_full(d, causal):
+    _full_check(2, 3, 1000, d, causal, seed=7)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_peaky_scores_full(causal):
+    # Large score spread forces frequent running-max updates and O rescaling.
+    _full_check(1, 2, 640, 64, causal, seed=9, qk_std=3.0, v_dist="uniform")
+
+
+def _sampled(name, heads, rows, full_heads=()):
+    w = WORKLOADS[name]
+    q, k, v = workload_inputs(w, device="cuda")
+    o, lse = _run(q, k, v, w.causal, w.scale)
+    O_ref, L_ref = oracle_fwd(q, k, v, w.scale, w.causal, heads=heads, rows=rows)
+    assert_within(compare_fwd(o, lse, O_ref, L_ref, heads, rows))
+    for h in full_heads:
+        O_ref, L_ref = oracle_fwd(q, k, v, w.scale, w.causal, heads=[h])
+        assert_within(compare_fwd(o, lse, O_ref, L_ref, [h], None))
+    return o, lse
+
+
+def _rows(N, n, seed):
+    rng = np.random.default_rng(seed)
+    edge = [0, 1, 126, 127, 128, 129, N // 2, N - 129, N - 128, N - 2, N - 1]
+    return sorted(set(edge) | set(rng.choice(N, n, replace=False).tolist()))
+
+
+def test_causal_workload_sampled():
+    w = WORKLOADS["causal_fwd"]
+    _sampled("causal_fwd", heads=range(w.B * w.H), rows=_rows(w.N, 48, 1),
+             full_heads=[0, w.B * w.H - 1])
+
+
+def test_noncausal_workload_sampled():
+    w = WORKLOADS["noncausal_fwd"]
+    heads = np.random.default_rng(2).choice(w.B * w.H, 24, replace=False).tolist()
+    _sampled("noncausal_fwd", heads=sorted(heads), rows=_rows(w.N, 40, 2), full_heads=[5])
+
+
+def test_long_causal_workload_sampled():
+    w = WORKLOADS["long_causal_fwd"]
+    _sampled("long_causal_fwd", heads=[0, 7, 19, 31], rows=_rows(w.N, 40, 3))
+
+
+def test_deterministic_and_no_out_of_bounds_writes():
+    B, H, N, d = 2, 2, 333, 128
+    q, k, v = fwd_inputs(B, H, N, d, 21, device="cuda")
+    pad = 4096
+    o_buf = torch.full((B * H * N * d + pad,), 7.0, dtype=torch.bfloat16, device="cuda")
+    l_buf = torch.full((B * H * N + pad,), 7.0, dtype=torch.float32, device="cuda")
+    o = o_buf[: B * H * N * d].view(B, H, N, d)
+    lse = l_buf[: B * H * N].view(B, H, N)
+    outs = []
+    for _ in range(2):
+        ea.attn_fwd(q, k, v, o, lse, True, d ** -0.5)
+        torch.cuda.synchronize()
+        outs.append((o.clone(), lse.clone()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    assert (o_buf[B * H * N * d:] == 7.0).all()
+    assert (l_buf[B * H * N:] == 7.0).all()
+
+
+def test_runs_on_a_side_stream():
+    B, H, N, d = 1, 4, 256, 64
+    q, k, v = fwd_inputs(B, H, N, d, 31, device="cuda")
+    s = torch.cuda.Stream()
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        ea.attn_fwd(q, k, v, o, lse, False, 0.125, stream=s)
+    s.synchronize()
+    O_ref, L_ref = oracle_fwd(q, k, v, 0.125, False)
+    assert_within(compare_fwd(o, lse, O_ref, L_ref, range(B * H), None))
