@@ -1,7 +1,7 @@
 // decode_sm103a.cu — split-KV single-token decode for GB300 (sm_103a).
 //
 // One query row per (batch, head) against a KV cache of L keys, following
-// "Why fast GPUs still wait for memory", section "Attention III · KV cache,
+// "Why Fast GPUs Still Wait for Memory", section "Attention III · KV cache,
 // GQA, MLA": W = 4Ld flops against 2*2*L*d bytes of K and V, an intensity of
 // one flop per byte, so the kernel is bound by HBM bandwidth and its job is
 // to stream K and V exactly once with as many bytes in flight as possible.

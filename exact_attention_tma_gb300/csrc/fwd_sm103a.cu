@@ -1,7 +1,7 @@
 // fwd_sm103a.cu — fused exact-attention forward for GB300 (sm_103a).
 //
 // Computes O = softmax(scale * Q K^T + causal mask) V and the row log-sum-exp
-// for every (batch, head), following "Why fast GPUs still wait for memory",
+// for every (batch, head), following "Why Fast GPUs Still Wait for Memory",
 // sections "Attention from first principles" (the definition) and
 // "FlashAttention is an IO algorithm": Q is split into blocks of B_r = 128
 // rows, K/V into blocks of B_c = 128 keys that stream through shared memory,

@@ -1,0 +1,58 @@
+"""Run one attention case a few times through the C ABI, for profilers.
+
+    python -m exact_attention_tma_gb300.profile_cases --case fwd-causal --iters 3
+    python -m exact_attention_tma_gb300.profile_cases --case decode --batch 4 --iters 3
+
+Cases use the same shapes and seeded inputs as the bench workloads; decode
+can be run at a smaller batch so that a multi-pass Nsight Compute capture
+stays small (each head is an independent unit of work, so DRAM traffic
+scales with the batch).  Inputs are generated on the device (torch RNG), since
+only the kernels' behaviour is profiled here, not their values.
+"""
+from __future__ import annotations
+
+import argparse
+
+import torch
+
+import exact_attention_tma_gb300 as ea
+from exact_attention_tma_gb300.inputs import WORKLOADS
+
+CASES = {"fwd-causal": "causal_fwd", "fwd-noncausal": "noncausal_fwd",
+         "fwd-long-causal": "long_causal_fwd", "decode": "decode"}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--case", choices=sorted(CASES), required=True)
+    ap.add_argument("--batch", type=int, default=0, help="override B (0 = workload's)")
+    ap.add_argument("--iters", type=int, default=3)
+    args = ap.parse_args(argv)
+    w = WORKLOADS[CASES[args.case]]
+    B = args.batch or w.B
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev).manual_seed(w.seed)
+    if w.kind == "fwd":
+        shape = (B, w.H, w.N, w.d)
+        q, k, v = (torch.randn(shape, generator=g, device=dev).to(torch.bfloat16)
+                   for _ in range(3))
+        o = torch.empty_like(q)
+        lse = torch.empty(shape[:3], dtype=torch.float32, device=dev)
+        call = lambda: ea.attn_fwd(q, k, v, o, lse, w.causal, w.scale)  # noqa: E731
+    else:
+        q = torch.randn((B, w.H, w.d), generator=g, device=dev).to(torch.bfloat16)
+        kc, vc = (torch.randn((B, w.H, w.N, w.d), generator=g, device=dev).to(torch.bfloat16)
+                  for _ in range(2))
+        o = torch.empty_like(q)
+        call = lambda: ea.attn_decode(q, kc, vc, o, w.scale)  # noqa: E731
+    for _ in range(args.iters):
+        call()
+    torch.cuda.synchronize()
+    status = ea.attn_get_device_status()
+    if status != 0:
+        raise SystemExit(f"device status {status}: {ea.attn_status_string(status)}")
+    print(f"{args.case} B={B}: {args.iters} launches ok")
+
+
+if __name__ == "__main__":
+    main()

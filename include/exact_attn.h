@@ -3,7 +3,7 @@
  *
  * The library computes exact scaled-dot-product attention,
  *     O = softmax(scale * Q K^T + causal mask) V,
- * as defined in "Why fast GPUs still wait for memory"
+ * as defined in "Why Fast GPUs Still Wait for Memory"
  * (srini-anirudh.github.io), section "Attention from first principles"
  * (S = QK^T, P = softmax(S), O = PV), computed the IO-aware way described in
  * the section "FlashAttention is an IO algorithm" on the same page: K/V blocks

@@ -10,7 +10,7 @@ per head; S and P materialised).  This wrapper only marshals numpy arrays and,
 for many heads, runs independent per-head calls on a thread pool (ctypes drops
 the GIL during each call, so heads run in parallel on the host cores).
 
-Definition followed: "Why fast GPUs still wait for memory", section
+Definition followed: "Why Fast GPUs Still Wait for Memory", section
 "Attention from first principles" (S = QK^T, P = softmax(S), O = PV), with the
 readings on scale, causal alignment, LSE and split-KV stated in the C file.
 Every function here is pinned by ``tests/test_oracle.py``.

@@ -7,10 +7,10 @@
  * the CUDA library under exact_attention_tma_gb300/csrc.
  *
  * What it computes is the plain definition of attention given in
- * "Why fast GPUs still wait for memory" (srini-anirudh.github.io), section
+ * "Why Fast GPUs Still Wait for Memory" (srini-anirudh.github.io), section
  * "Attention from first principles" (the "core of attention" display):
  *     S = Q K^T,  P = softmax(S),  O = P V
- * and restated in "Phase 18 warm-up" (ai-engineer-zt0.pages.dev), chapter 7
+ * and restated in "Warmup Guide — C++/CUDA & GPU Performance Engineering" (ai-engineer-zt0.pages.dev), chapter 7, Operator Fusion
  * (FlashAttention paragraph).  Decode is the same definition with a single
  * query row against the whole KV cache ("Attention III · KV cache, GQA, MLA"
  * on the roofline page).

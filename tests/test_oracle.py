@@ -1,7 +1,7 @@
 """Pins for the fp64 CPU oracle (no GPU).
 
 The oracle is checked against things fixed by the definition of attention
-("Why fast GPUs still wait for memory", section 'Attention from first
+("Why Fast GPUs Still Wait for Memory", section 'Attention from first
 principles': S = QK^T, P = softmax(S), O = PV), not against itself:
 hand-worked closed forms (tests/golden/hand_cases.json), invariants that hold
 for any input (rows of P sum to one, masked entries are exactly zero,
