@@ -18,7 +18,8 @@ import threading
 __all__ = [
     "AttnError", "attn_fwd", "attn_decode", "attn_decode_ws",
     "attn_decode_workspace_bytes", "attn_get_device_status", "attn_status_string",
-    "attn_decode_num_splits", "forward", "decode", "library_path", "load",
+    "attn_decode_num_splits", "attn_decode_noalloc", "forward", "decode", "library_path",
+    "load",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -55,6 +56,8 @@ def load():
             lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
             lib.attn_decode.argtypes = [vp, vp, vp, vp, i, i, i, i, f, vp]
             lib.attn_decode_ws.argtypes = [vp, vp, vp, vp, i, i, i, i, f, vp, sz, vp]
+            lib.attn_decode_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, f, vp]
+            lib.attn_decode_noalloc.restype = ctypes.c_int
             lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i]
             lib.attn_decode_workspace_bytes.restype = sz
             lib.attn_get_device_status.argtypes = [vp]
@@ -160,6 +163,27 @@ def attn_decode_ws(q, Kcache, Vcache, O, scale: float, ws, stream=None) -> None:
     _check(load().attn_decode_ws(*args, B, H, L, d, float(scale),
                                  ctypes.c_void_p(ws.data_ptr()), nbytes, _stream(stream)),
            "attn_decode_ws")
+
+
+def attn_decode_noalloc(q, Kcache, Vcache, O, scale: float, stream=None) -> None:
+    """attn_decode without any device allocation, for callers that cannot allocate.
+
+    The partials go to a fixed 16 MiB scratch array inside the library (one per
+    GPU, held until exit) instead of memory the library or the caller allocates;
+    see include/exact_attn.h for the size limit and the sharing rules.
+    """
+    import torch
+
+    B, H, L, d = Kcache.shape
+    if tuple(Vcache.shape) != (B, H, L, d):
+        raise ValueError("Vcache shape must match Kcache")
+    for name, t in (("q", q), ("O", O)):
+        if tuple(t.shape) != (B, H, d):
+            raise ValueError(f"{name} shape {tuple(t.shape)} != {(B, H, d)}")
+    args = [_dev(q, "q", torch.bfloat16), _dev(Kcache, "Kcache", torch.bfloat16),
+            _dev(Vcache, "Vcache", torch.bfloat16), _dev(O, "O", torch.bfloat16)]
+    _check(load().attn_decode_noalloc(*args, B, H, L, d, float(scale), _stream(stream)),
+           "attn_decode_noalloc")
 
 
 def attn_get_device_status(stream=None) -> int:

@@ -111,6 +111,37 @@ attn_status attn_decode_ws(const void *q, const void *Kcache, const void *Vcache
                            size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * attn_decode_noalloc — attn_decode for callers that cannot allocate device
+ * memory.  (The pages describe no such entry point; it has no counterpart
+ * there.)
+ *
+ * Some callers can't let a library call cudaMalloc: a serving process whose
+ * own allocator has already reserved nearly all of the GPU's memory, code that
+ * must not have cudaMalloc/cudaFree block or synchronise the device in the
+ * middle of its work, or a host framework that forbids plug-ins from
+ * allocating device memory themselves.  This call computes the same result as
+ * attn_decode with the same kernels, but its partials live in a fixed scratch
+ * array compiled into the library: 16 MiB of device memory that every GPU
+ * which loads the library holds until the process exits.  It never calls
+ * cudaMalloc, cudaFree or any allocating routine.  The caller still passes
+ * q, the caches and O.
+ *
+ *   Limit: B*H*32*(d+1)*4 bytes of partials must fit in 16 MiB
+ *          (B*H <= 1016 at d = 128, B*H <= 2016 at d = 64); larger shapes
+ *          return ATTN_ERR_NOMEM and launch nothing.
+ *   Set-up: the first call on each device looks up the array's device address
+ *          (cudaGetSymbolAddress, with that device current).  Make that first
+ *          call before any stream capture.
+ *   Sharing: every call on a device uses the same array, which keeps the last
+ *          call's contents (no part of it needs to start at zero).  Calls that
+ *          overlap on the GPU -- on different streams, or from different host
+ *          threads -- race on it and must be serialised by the caller.
+ * Other arguments, validation and errors are those of attn_decode.
+ */
+attn_status attn_decode_noalloc(const void *q, const void *Kcache, const void *Vcache, void *O,
+                                int B, int H, int L, int d, float scale, cudaStream_t stream);
+
+/*
  * attn_get_device_status — synchronises `stream`, then reads and clears the
  * library's device status word on the current device.  Returns ATTN_OK, or
  * ATTN_ERR_TIMEOUT if any kernel since the last call gave up on a bounded
