@@ -6,32 +6,36 @@
 // "FlashAttention is an IO algorithm": Q is split into blocks of B_r = 128
 // rows, K/V into blocks of B_c = 128 keys that stream through shared memory,
 // and a running maximum and normaliser per row rescale the output block as
-// each K/V block arrives, so S and P never reach HBM.  Causal masking follows
-// the note "causal masking is not an optimisation here" on the same page:
-// K/V blocks entirely above the diagonal are never loaded or multiplied.
+// K/V blocks arrive, so S and P never reach HBM.  Causal masking follows the
+// note "causal masking is not an optimisation here" on the same page: K/V
+// blocks entirely above the diagonal are never loaded or multiplied.
 //
-// GB300 mapping (one CTA per 128-row query tile, 6 warps):
-//   warp 4     TMA producer: Q tile once, then K_j / V_j into a ring of
-//              STAGES shared-memory slots (128-byte swizzle), each slot
-//              guarded by full/empty mbarriers.
-//   warp 5     MMA issuer (one thread): tcgen05.mma S_j = Q K_j^T into one of
-//              two TMEM S buffers, then O += P_j V_j into the TMEM O
-//              accumulator; tcgen05.commit signals the other roles.
-//   warps 0-3  softmax: thread r owns query row r (TMEM lane r); reads its S
-//              row from TMEM, masks, updates the running max m and sum l in
-//              the base-2 domain (scale * log2(e) folded into one FMA before
-//              ex2), rescales its O row in TMEM when m moved, and writes P as
-//              bf16 into a swizzled shared-memory tile for the P V MMA.
-//              The epilogue divides by l, rounds to bf16 and writes O and LSE.
-// S is double-buffered in TMEM, so the tensor core computes S_{j+1} while
-// the softmax warps are still working on S_j.
+// GB300 mapping: one CTA owns two 128-row query tiles of one head (256 rows)
+// and streams that head's K/V tiles once for both.  16 warps:
+//   warps 0-3   softmax for query tile 0   (thread = row = TMEM lane)
+//   warps 4-7   softmax for query tile 1
+//   warps 8-11  correction: rescales a tile's O accumulator in TMEM when its
+//               running max moved by more than 2^8 (lazy rescaling: between
+//               rescales the stale max is used for both P and the row sum, so
+//               the final O / l is unchanged and P stays <= 256)
+//   warp 12     MMA issuer (one thread): tcgen05.mma S_i = Q_i K_j^T into TMEM
+//               (both operands from swizzled shared memory), then
+//               O_i += P_i V_j with P_i read straight from TMEM (it overwrites
+//               the first half of S_i as packed bf16)
+//   warp 13     TMA producer: Q tiles once, K_j and V_j into separate rings
+//               guarded by full/empty mbarriers
+//   warps 14-15 idle
+// The two softmax warpgroups work on different query tiles, so while one
+// computes exponentials the tensor core runs the other tile's MMAs.
+// Registers are re-balanced with setmaxnreg: 192 per softmax thread, 80 per
+// correction thread, 48 for warps 12-15 (2*128*192 + 128*80 + 128*48 = 65536,
+// the block's launch allocation of 512 threads x 128).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
 #include <atomic>
 #include <cmath>
-#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -41,83 +45,109 @@ namespace fwd {
 
 constexpr int BM = 128;                  // query rows per tile (B_r)
 constexpr int BN = 128;                  // keys per K/V tile (B_c)
-constexpr int kSoftmaxThreads = 128;     // warps 0-3
-constexpr int kWarpTMA = 4;
-constexpr int kWarpMMA = 5;
-constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 512;      // S0 | S1 | O
-constexpr uint32_t kTmemS0 = 0;
-constexpr uint32_t kTmemS1 = 128;
-constexpr uint32_t kTmemO = 256;
+constexpr int QT = 2;                    // query tiles per CTA
+constexpr int kThreads = 512;
+constexpr int kWarpMMA = 12;
+constexpr int kWarpTMA = 13;
+constexpr uint32_t kTmemCols = 512;      // S0 | S1 | O0 | O1
 constexpr uint32_t kBoxBytes = 64 * 128 * 2;   // one TMA box: 64 columns x 128 rows bf16
 constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kRescaleThreshold = 8.0f;      // log2 units: rescale when max grows > 2^8
 
 template <int D>
 struct Cfg {
   static_assert(D == 64 || D == 128, "head dimension");
   static constexpr int KB = D / 64;                 // 128-byte swizzle column blocks
-  static constexpr int STAGES = (D == 128) ? 2 : 3;
-  static constexpr uint32_t Q_BYTES = BM * D * 2;
-  static constexpr uint32_t KV_BYTES = BN * D * 2;
-  static constexpr uint32_t P_BYTES = BM * BN * 2;
+  static constexpr int SK = (D == 128) ? 2 : 3;     // K ring stages
+  static constexpr int SV = (D == 128) ? 2 : 3;     // V ring stages
+  static constexpr uint32_t Q_BYTES = BM * D * 2;   // one query tile
+  static constexpr uint32_t KV_BYTES = BN * D * 2;  // one K or V tile
   static constexpr uint32_t OFF_Q = 0;
-  static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
-  static constexpr uint32_t OFF_V = OFF_K + STAGES * KV_BYTES;
-  static constexpr uint32_t OFF_P = OFF_V + STAGES * KV_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_P + P_BYTES;
-  // q_full, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full, o_done, drain
-  static constexpr int NBAR = 1 + 3 * STAGES + 2 + 3;
+  static constexpr uint32_t OFF_K = OFF_Q + QT * Q_BYTES;
+  static constexpr uint32_t OFF_V = OFF_K + SK * KV_BYTES;
+  static constexpr uint32_t OFF_ALPHA = OFF_V + SV * KV_BYTES;   // float[QT][BM]
+  static constexpr uint32_t OFF_BAR = OFF_ALPHA + QT * BM * 4;
+  // q, kf[SK], ke[SK], vf[SV], ve[SV], s[2], p[2], a[2], c[2], o[2], drain
+  static constexpr int NBAR = 1 + 2 * SK + 2 * SV + 5 * QT + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;
   static constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;   // 1024-byte alignment slack
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+  static constexpr uint32_t TMEM_S = 0;               // S_i at column 128 * i
+  static constexpr uint32_t TMEM_O = QT * BN;         // O_i at column TMEM_O + D * i
+  static_assert(TMEM_O + QT * D <= kTmemCols, "tensor memory budget");
 };
+
+__device__ __forceinline__ void setmaxnreg_inc192() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
+}
+__device__ __forceinline__ void setmaxnreg_dec80() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
+}
+__device__ __forceinline__ void setmaxnreg_dec48() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 48;" ::: "memory");
+}
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, __nv_bfloat16 *__restrict__ O,
-                    float *__restrict__ LSE, int N, int BH, int n_qt, float scale_log2,
+                    float *__restrict__ LSE, int N, int BH, int n_blk, float scale_log2,
                     unsigned *status) {
   using C = Cfg<D>;
-  constexpr int S = C::STAGES;
+  constexpr int SK = C::SK;
+  constexpr int SV = C::SV;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int wg = warp >> 2;
 
-  // Heads vary fastest and, for causal, the longest query tiles go first.
+  // Heads vary fastest; for causal the longest query blocks go first.
   const int bh = blockIdx.x % BH;
-  const int qt = n_qt - 1 - static_cast<int>(blockIdx.x / BH);
-  const int q0 = qt * BM;
+  const int blk = n_blk - 1 - static_cast<int>(blockIdx.x / BH);
+  const int q0 = blk * (QT * BM);
   const int n_kv_total = (N + BN - 1) / BN;
-  const int n_kv = CAUSAL ? min(qt + 1, n_kv_total) : n_kv_total;
+  // K/V tiles each query tile needs (query tile 0 can stop one tile earlier when causal).
+  const int n0 = CAUSAL ? min(QT * blk + 1, n_kv_total) : n_kv_total;
+  const int n1 = CAUSAL ? min(QT * blk + 2, n_kv_total) : n_kv_total;
 
   const uint32_t bar0 = sb + C::OFF_BAR;
   const uint32_t B_Q = bar0;
-  auto B_K = [&](int st) { return bar0 + 8u * (1 + st); };
-  auto B_V = [&](int st) { return bar0 + 8u * (1 + S + st); };
-  auto B_E = [&](int st) { return bar0 + 8u * (1 + 2 * S + st); };
-  auto B_S = [&](int b) { return bar0 + 8u * (1 + 3 * S + b); };
-  const uint32_t B_P = bar0 + 8u * (3 + 3 * S);
-  const uint32_t B_O = bar0 + 8u * (4 + 3 * S);
-  const uint32_t B_DRAIN = bar0 + 8u * (5 + 3 * S);
+  auto B_KF = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto B_KE = [&](int s) { return bar0 + 8u * (1 + SK + s); };
+  auto B_VF = [&](int s) { return bar0 + 8u * (1 + 2 * SK + s); };
+  auto B_VE = [&](int s) { return bar0 + 8u * (1 + 2 * SK + SV + s); };
+  constexpr int kB5 = 1 + 2 * SK + 2 * SV;
+  auto B_S = [&](int i) { return bar0 + 8u * (kB5 + i); };            // S_i ready (MMA)
+  auto B_P = [&](int i) { return bar0 + 8u * (kB5 + QT + i); };       // P_i written (softmax)
+  auto B_A = [&](int i) { return bar0 + 8u * (kB5 + 2 * QT + i); };   // alpha_i ready (softmax)
+  auto B_C = [&](int i) { return bar0 + 8u * (kB5 + 3 * QT + i); };   // O_i corrected
+  auto B_O = [&](int i) { return bar0 + 8u * (kB5 + 4 * QT + i); };   // P_i V_j done (MMA)
+  const uint32_t B_DRAIN = bar0 + 8u * (kB5 + 5 * QT);
+  float *alpha_s = reinterpret_cast<float *>(smem + C::OFF_ALPHA);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
   if (threadIdx.x == 0) {
     mbar_init(B_Q, 1);
-    for (int st = 0; st < S; ++st) {
-      mbar_init(B_K(st), 1);
-      mbar_init(B_V(st), 1);
-      mbar_init(B_E(st), 1);
+    for (int s = 0; s < SK; ++s) {
+      mbar_init(B_KF(s), 1);
+      mbar_init(B_KE(s), 1);
     }
-    mbar_init(B_S(0), 1);
-    mbar_init(B_S(1), 1);
-    mbar_init(B_P, kSoftmaxThreads);
-    mbar_init(B_O, 1);
+    for (int s = 0; s < SV; ++s) {
+      mbar_init(B_VF(s), 1);
+      mbar_init(B_VE(s), 1);
+    }
+    for (int i = 0; i < QT; ++i) {
+      mbar_init(B_S(i), 1);
+      mbar_init(B_P(i), BM);
+      mbar_init(B_A(i), BM);
+      mbar_init(B_C(i), BM);
+      mbar_init(B_O(i), 1);
+    }
     mbar_init(B_DRAIN, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -136,131 +166,48 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == kWarpTMA) {
-    // ------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      mbar_arrive_expect_tx(B_Q, C::Q_BYTES);
-#pragma unroll
-      for (int kb = 0; kb < C::KB; ++kb)
-        tma_load_3d(sb + C::OFF_Q + kb * kBoxBytes, &tmQ, kb * 64, q0, bh, B_Q);
-      int issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
-        const int st = j % S;
-        const uint32_t ph = (j / S) & 1;
-        if (!mbar_wait(B_E(st), ph ^ 1u, status, abort_flag)) break;
-        mbar_arrive_expect_tx(B_K(st), C::KV_BYTES);
-#pragma unroll
-        for (int kb = 0; kb < C::KB; ++kb)
-          tma_load_3d(sb + C::OFF_K + st * C::KV_BYTES + kb * kBoxBytes, &tmK, kb * 64, j * BN,
-                      bh, B_K(st));
-        mbar_arrive_expect_tx(B_V(st), C::KV_BYTES);
-#pragma unroll
-        for (int kb = 0; kb < C::KB; ++kb)
-          tma_load_3d(sb + C::OFF_V + st * C::KV_BYTES + kb * kBoxBytes, &tmV, kb * 64, j * BN,
-                      bh, B_V(st));
-        issued = j + 1;
-      }
-      if (*abort_flag) {
-        // Let every copy this thread started land before the CTA exits.
-        mbar_wait_drain(B_Q, 0, 100000000ull);
-        for (int st = 0; st < S && st < issued; ++st) {
-          const int last = st + ((issued - 1 - st) / S) * S;
-          mbar_wait_drain(B_K(st), (last / S) & 1, 100000000ull);
-          mbar_wait_drain(B_V(st), (last / S) & 1, 100000000ull);
-        }
-      }
-    }
-    __syncwarp();
-  } else if (warp == kWarpMMA) {
-    // ------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kIdescQK = make_idesc_bf16(BM, BN, 0, 0);
-      constexpr uint32_t kIdescPV = make_idesc_bf16(BM, D, 0, 1);
-      // S_j = Q K_j^T: both operands K-major (head dim contiguous).
-      auto issue_qk = [&](uint32_t d_tmem, int st) {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-          const uint64_t a = make_sdesc_sw128(sb + C::OFF_Q + koff, 16, 1024);
-          const uint64_t b = make_sdesc_sw128(sb + C::OFF_K + st * C::KV_BYTES + koff, 16, 1024);
-          mma_bf16_ss(d_tmem, a, b, kIdescQK, kk > 0 ? 1u : 0u);
-        }
-      };
-      // O += P_j V_j: P is K-major (keys contiguous); V is MN-major (head dim
-      // contiguous), 64-column blocks kBoxBytes apart, 8-key groups 1024 B apart.
-      auto issue_pv = [&](int st, bool acc) {
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t a =
-              make_sdesc_sw128(sb + C::OFF_P + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024);
-          const uint64_t b =
-              make_sdesc_sw128(sb + C::OFF_V + st * C::KV_BYTES + kk * 16 * 128, kBoxBytes, 1024);
-          mma_bf16_ss(tmem + kTmemO, a, b, kIdescPV, (acc || kk > 0) ? 1u : 0u);
-        }
-      };
-      bool ok = mbar_wait(B_Q, 0, status, abort_flag) && mbar_wait(B_K(0), 0, status, abort_flag);
-      if (ok) {
-        tc_fence_after();
-        issue_qk(tmem + kTmemS0, 0);
-        mma_commit(B_S(0));
-      }
-      for (int j = 0; ok && j < n_kv; ++j) {
-        if (j + 1 < n_kv) {
-          // S buffer (j+1)&1 was released when the softmax warps signalled P_{j-1}.
-          const int st1 = (j + 1) % S;
-          if (!mbar_wait(B_K(st1), ((j + 1) / S) & 1, status, abort_flag)) break;
-          tc_fence_after();
-          issue_qk(tmem + (((j + 1) & 1) ? kTmemS1 : kTmemS0), st1);
-          mma_commit(B_S((j + 1) & 1));
-        }
-        const int st = j % S;
-        if (!mbar_wait(B_P, j & 1, status, abort_flag)) break;
-        if (!mbar_wait(B_V(st), (j / S) & 1, status, abort_flag)) break;
-        tc_fence_after();
-        issue_pv(st, j > 0);
-        mma_commit(B_O);
-        if (j + S < n_kv) mma_commit(B_E(st));   // slot refilled only if a later tile needs it
-      }
-      // Every MMA issued so far must finish before TMEM is released.
-      mma_commit(B_DRAIN);
-      mbar_wait_drain(B_DRAIN, 0, 100000000ull);
-    }
-    __syncwarp();
-  } else {
-    // ---------------------------------------------------- softmax warps
-    const int r = threadIdx.x;               // row within the tile == TMEM lane
-    const int qrow = q0 + r;
-    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
-    float m = -INFINITY;                     // running max of scale*log2(e)*s
+  if (wg < QT) {
+    setmaxnreg_inc192();
+    // ------------------------------------------------------------ softmax
+    const int i = wg;                        // query tile
+    const int r = threadIdx.x - i * BM;      // row within the tile == TMEM lane
+    const int qrow = q0 + i * BM + r;
+    const int n_i = (i == 0) ? n0 : n1;
+    const int lim = CAUSAL ? min(qrow, N - 1) : N - 1;   // last visible key
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t s_addr = tmem + lane_addr + C::TMEM_S + i * BN;
+    float m = -INFINITY;                     // max used for the exponentials (base 2)
     float l = 0.f;                           // running sum of exp2(x - m)
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      const int b = j & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(B_S(b), (j >> 1) & 1, status, abort_flag));
+    for (int j = 0; j < n_i; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(B_S(i), j & 1, status, abort_flag));
       if (!ok) break;
       tc_fence_after();
       uint32_t sr[4][32];
-      const uint32_t s_addr = tmem + lane_addr + (b ? kTmemS1 : kTmemS0);
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld_32cols(s_addr + c * 32, sr[c]);
       tmem_ld_wait();
       float s[BN];
 #pragma unroll
       for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
-      if (j == n_kv - 1 && (CAUSAL || (N % BN) != 0)) {
-        const int kv0 = j * BN;
+      const int kv0 = j * BN;
+      if (kv0 + BN - 1 > lim) {
 #pragma unroll
-        for (int c = 0; c < BN; ++c) {
-          const int key = kv0 + c;
-          if (key >= N || (CAUSAL && key > qrow)) s[c] = -INFINITY;
-        }
+        for (int c = 0; c < BN; ++c)
+          if (kv0 + c > lim) s[c] = -INFINITY;
       }
       float mt = s[0];
 #pragma unroll
       for (int c = 1; c < BN; ++c) mt = fmaxf(mt, s[c]);
-      const float m_new = fmaxf(m, mt * scale_log2);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = ex2_approx(m - m_use);
+      const float m_tile = mt * scale_log2;
+      float alpha = 1.f;
+      if (m_tile - m > kRescaleThreshold) {   // true on the first tile (m = -inf)
+        alpha = ex2_approx(m - m_tile);
+        m = m_tile;
+      }
+      alpha_s[i * BM + r] = alpha;
+      mbar_arrive(B_A(i));
+      const float m_use = (m == -INFINITY) ? 0.f : m;
       float rs = 0.f;
       uint32_t pk[BN / 2];
 #pragma unroll
@@ -271,39 +218,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         pk[c] = pack_bf16x2(p0, p1);
       }
       l = l * alpha + rs;
-      m = m_new;
-      if (j > 0) {
-        // P_{j-1} V_{j-1} must be done before O is rescaled and P is overwritten.
-        ok = __all_sync(0xffffffffu, mbar_wait(B_O, (j - 1) & 1, status, abort_flag));
-        if (!ok) break;
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            const uint32_t o_addr = tmem + lane_addr + kTmemO + c * 32;
-            tmem_ld_32cols(o_addr, o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st_32cols(o_addr, o);
-          }
-          tmem_st_wait();
-        }
-      }
-      // P row r -> 128-byte-swizzled K-major tile: 16-byte chunk ch of a row
-      // lands at chunk (ch ^ (row & 7)), as the TMA swizzle would place it.
-#pragma unroll
-      for (int c16 = 0; c16 < BN / 8; ++c16) {
-        const uint32_t addr = sb + C::OFF_P + (c16 >> 3) * kBoxBytes + r * 128 +
-                              ((static_cast<uint32_t>(c16 & 7) ^ (r & 7)) << 4);
-        st_shared_v4(addr, pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
-      }
-      fence_proxy_async_smem();
+      // P_i (bf16, keys packed in pairs) over the first 64 columns of S_i.
+      tmem_st_32cols(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      tmem_st_32cols(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(B_P);
+      mbar_arrive(B_P(i));
     }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(B_O, (n_kv - 1) & 1, status, abort_flag));
+    // Epilogue: O_i / l -> bf16 rows, LSE.
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(B_O(i), (n_i - 1) & 1, status, abort_flag));
     if (ok) {
       tc_fence_after();
       const float inv_l = 1.f / l;
@@ -311,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
-        tmem_ld_32cols(tmem + lane_addr + kTmemO + c * 32, o);
+        tmem_ld_32cols(tmem + lane_addr + C::TMEM_O + i * D + c * 32, o);
         tmem_ld_wait();
         if (qrow < N) {
 #pragma unroll
@@ -332,6 +255,160 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     tc_fence_before();
+  } else if (wg == QT) {
+    setmaxnreg_dec80();
+    // --------------------------------------------------------- correction
+    const int t = threadIdx.x - QT * BM;     // row == TMEM lane
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    bool ok = true;
+    for (int j = 0; ok && j < n1; ++j) {
+#pragma unroll
+      for (int i = 0; i < QT; ++i) {
+        if (j >= (i == 0 ? n0 : n1)) continue;
+        ok = __all_sync(0xffffffffu, mbar_wait(B_A(i), j & 1, status, abort_flag));
+        if (!ok) break;
+        const float a = alpha_s[i * BM + t];
+        if (j > 0 && __any_sync(0xffffffffu, a != 1.f)) {
+          // P_i V_{j-1} must have landed before O_i is scaled.
+          ok = __all_sync(0xffffffffu, mbar_wait(B_O(i), (j - 1) & 1, status, abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            const uint32_t o_addr = tmem + lane_addr + C::TMEM_O + i * D + c * 32;
+            tmem_ld_32cols(o_addr, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
+            tmem_st_32cols(o_addr, o);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        mbar_arrive(B_C(i));
+      }
+    }
+    tc_fence_before();
+  } else {
+    setmaxnreg_dec48();
+    if (warp == kWarpTMA) {
+      // ------------------------------------------------------ TMA producer
+      if (lane == 0) {
+        mbar_arrive_expect_tx(B_Q, QT * C::Q_BYTES);
+#pragma unroll
+        for (int i = 0; i < QT; ++i)
+#pragma unroll
+          for (int kb = 0; kb < C::KB; ++kb)
+            tma_load_3d(sb + C::OFF_Q + i * C::Q_BYTES + kb * kBoxBytes, &tmQ, kb * 64,
+                        q0 + i * BM, bh, B_Q);
+        int issued_k = 0, issued_v = 0;
+        for (int j = 0; j < n1; ++j) {
+          const int sk = j % SK;
+          if (!mbar_wait(B_KE(sk), ((j / SK) & 1) ^ 1u, status, abort_flag)) break;
+          mbar_arrive_expect_tx(B_KF(sk), C::KV_BYTES);
+#pragma unroll
+          for (int kb = 0; kb < C::KB; ++kb)
+            tma_load_3d(sb + C::OFF_K + sk * C::KV_BYTES + kb * kBoxBytes, &tmK, kb * 64, j * BN,
+                        bh, B_KF(sk));
+          issued_k = j + 1;
+          const int sv = j % SV;
+          if (!mbar_wait(B_VE(sv), ((j / SV) & 1) ^ 1u, status, abort_flag)) break;
+          mbar_arrive_expect_tx(B_VF(sv), C::KV_BYTES);
+#pragma unroll
+          for (int kb = 0; kb < C::KB; ++kb)
+            tma_load_3d(sb + C::OFF_V + sv * C::KV_BYTES + kb * kBoxBytes, &tmV, kb * 64, j * BN,
+                        bh, B_VF(sv));
+          issued_v = j + 1;
+        }
+        if (*abort_flag) {
+          // Let every copy this thread started land before the CTA exits.
+          mbar_wait_drain(B_Q, 0, 100000000ull);
+          for (int s = 0; s < SK && s < issued_k; ++s)
+            mbar_wait_drain(B_KF(s), (((issued_k - 1 - s) / SK)) & 1, 100000000ull);
+          for (int s = 0; s < SV && s < issued_v; ++s)
+            mbar_wait_drain(B_VF(s), (((issued_v - 1 - s) / SV)) & 1, 100000000ull);
+        }
+      }
+      __syncwarp();
+    } else if (warp == kWarpMMA) {
+      // ------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t kIdescQK = make_idesc_bf16(BM, BN, 0, 0);
+        constexpr uint32_t kIdescPV = make_idesc_bf16(BM, D, 0, 1);
+        // S_i = Q_i K^T: both operands K-major (head dim contiguous), 128-B swizzle.
+        auto issue_qk = [&](int i, int sk) {
+#pragma unroll 1
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t koff = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+            const uint64_t a =
+                make_sdesc_sw128(sb + C::OFF_Q + i * C::Q_BYTES + koff, 16, 1024);
+            const uint64_t b =
+                make_sdesc_sw128(sb + C::OFF_K + sk * C::KV_BYTES + koff, 16, 1024);
+            mma_bf16_ss(tmem + C::TMEM_S + i * BN, a, b, kIdescQK, kk > 0 ? 1u : 0u);
+          }
+        };
+        // O_i += P_i V: P_i from TMEM (8 columns = 16 keys per step); V is MN-major
+        // (head dim contiguous), 64-column blocks kBoxBytes apart, 8-key groups 1024 B apart.
+        auto issue_pv = [&](int i, int sv, bool acc) {
+#pragma unroll 1
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint64_t b =
+                make_sdesc_sw128(sb + C::OFF_V + sv * C::KV_BYTES + kk * 16 * 128, kBoxBytes, 1024);
+            mma_bf16_ts(tmem + C::TMEM_O + i * D, tmem + C::TMEM_S + i * BN + kk * 8, b, kIdescPV,
+                        (acc || kk > 0) ? 1u : 0u);
+          }
+        };
+        bool ok =
+            mbar_wait(B_Q, 0, status, abort_flag) && mbar_wait(B_KF(0), 0, status, abort_flag);
+        if (ok) {
+          tc_fence_after();
+          issue_qk(0, 0);
+          mma_commit(B_S(0));
+          issue_qk(1, 0);
+          mma_commit(B_S(1));
+          if (SK < n1) mma_commit(B_KE(0));
+        }
+        for (int j = 0; ok && j < n1; ++j) {
+          const int sv = j % SV;
+          if (!(ok = mbar_wait(B_VF(sv), (j / SV) & 1, status, abort_flag))) break;
+          if (j < n0) {
+            ok = mbar_wait(B_P(0), j & 1, status, abort_flag) &&
+                 mbar_wait(B_C(0), j & 1, status, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(0, sv, j > 0);
+            mma_commit(B_O(0));
+          }
+          const bool more = j + 1 < n1;
+          const int sk1 = (j + 1) % SK;
+          if (more) {
+            if (!(ok = mbar_wait(B_KF(sk1), ((j + 1) / SK) & 1, status, abort_flag))) break;
+            tc_fence_after();
+            if (j + 1 < n0) {
+              issue_qk(0, sk1);   // overwrites S_0/P_0 after the P_0 V_j MMA above has read it
+              mma_commit(B_S(0));
+            }
+          }
+          ok = mbar_wait(B_P(1), j & 1, status, abort_flag) &&
+               mbar_wait(B_C(1), j & 1, status, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(1, sv, j > 0);
+          mma_commit(B_O(1));
+          if (j + SV < n1) mma_commit(B_VE(sv));
+          if (more) {
+            issue_qk(1, sk1);
+            mma_commit(B_S(1));
+            if (j + 1 + SK < n1) mma_commit(B_KE(sk1));
+          }
+        }
+        // Every MMA issued so far must finish before TMEM is released.
+        mma_commit(B_DRAIN);
+        mbar_wait_drain(B_DRAIN, 0, 100000000ull);
+      }
+      __syncwarp();
+    }
   }
   __syncthreads();
   if (warp == kWarpMMA) {
@@ -388,10 +465,10 @@ static cudaError_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const 
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
-  const int n_qt = (N + BM - 1) / BM;
-  const long long grid = static_cast<long long>(BH) * n_qt;
+  const int n_blk = (N + QT * BM - 1) / (QT * BM);
+  const long long grid = static_cast<long long>(BH) * n_blk;
   kern<<<static_cast<unsigned>(grid), kThreads, C::SMEM_ALLOC, stream>>>(
-      mq, mk, mv, static_cast<__nv_bfloat16 *>(O), LSE, N, BH, n_qt, scale_log2, status);
+      mq, mk, mv, static_cast<__nv_bfloat16 *>(O), LSE, N, BH, n_blk, scale_log2, status);
   return cudaGetLastError();
 }
 
