@@ -27,9 +27,9 @@
 //   warps 14-15 idle
 // The two softmax warpgroups work on different query tiles, so while one
 // computes exponentials the tensor core runs the other tile's MMAs.
-// Registers are re-balanced with setmaxnreg: 192 per softmax thread, 80 per
-// correction thread, 48 for warps 12-15 (2*128*192 + 128*80 + 128*48 = 65536,
-// the block's launch allocation of 512 threads x 128).
+// Registers are re-balanced with setmaxnreg: 176 per softmax thread, 80 per
+// correction thread and 80 for warps 12-15 (2*128*176 + 2*128*80 = 65536, the
+// block's launch allocation of 512 threads x 128).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -54,12 +54,27 @@ constexpr uint32_t kBoxBytes = 64 * 128 * 2;   // one TMA box: 64 columns x 128 
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleThreshold = 8.0f;      // log2 units: rescale when max grows > 2^8
 
+// K/V ring depths per head dimension (shared memory: 2 query tiles + SK + SV
+// tiles of 128 x d bf16 must fit in 227 KB).
+#ifndef EA_FWD_SK128
+#define EA_FWD_SK128 2
+#endif
+#ifndef EA_FWD_SV128
+#define EA_FWD_SV128 2
+#endif
+#ifndef EA_FWD_SK64
+#define EA_FWD_SK64 3
+#endif
+#ifndef EA_FWD_SV64
+#define EA_FWD_SV64 3
+#endif
+
 template <int D>
 struct Cfg {
   static_assert(D == 64 || D == 128, "head dimension");
   static constexpr int KB = D / 64;                 // 128-byte swizzle column blocks
-  static constexpr int SK = (D == 128) ? 2 : 3;     // K ring stages
-  static constexpr int SV = (D == 128) ? 2 : 3;     // V ring stages
+  static constexpr int SK = (D == 128) ? EA_FWD_SK128 : EA_FWD_SK64;   // K ring stages
+  static constexpr int SV = (D == 128) ? EA_FWD_SV128 : EA_FWD_SV64;   // V ring stages
   static constexpr uint32_t Q_BYTES = BM * D * 2;   // one query tile
   static constexpr uint32_t KV_BYTES = BN * D * 2;  // one K or V tile
   static constexpr uint32_t OFF_Q = 0;
@@ -78,14 +93,42 @@ struct Cfg {
   static_assert(TMEM_O + QT * D <= kTmemCols, "tensor memory budget");
 };
 
-__device__ __forceinline__ void setmaxnreg_inc192() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
+// Pairs (out of every 8 pairs of a row) whose exp2 runs on the FMA pipe
+// through exp2_poly2 instead of the MUFU ex2 unit, to balance the two pipes.
+#ifndef EA_POLY_PAIRS_PER8
+#define EA_POLY_PAIRS_PER8 0
+#endif
+constexpr int kPolyPairsPer8 = EA_POLY_PAIRS_PER8;
+
+// 2^x for two lanes on the FMA pipe.  Cody-Waite range reduction: j = round(x)
+// via the float32 "add 1.5 * 2^23" trick (j ends up in the low mantissa bits
+// of t), f = x - j in [-1/2, 1/2]; 2^f from a degree-3 polynomial whose max
+// relative error on [-1/2, 1/2] is 7.5e-5 (minimax fit by Lawson's algorithm,
+// exact_attention_tma_gb300/exp2_poly.py); j is added to the exponent field.
+// x is clamped at -126 so the exponent stays in range (masked -inf -> ~1e-38).
+__device__ __forceinline__ float2 exp2_poly2(float2 x) {
+  x.x = fmaxf(x.x, -126.f);
+  x.y = fmaxf(x.y, -126.f);
+  const float2 t = fadd2(x, make_float2(12582912.f, 12582912.f));
+  const float2 j = fadd2(t, make_float2(-12582912.f, -12582912.f));
+  const float2 f = ffma2(j, make_float2(-1.f, -1.f), x);
+  float2 p = ffma2(make_float2(0.05517132207751274f, 0.05517132207751274f), f,
+                   make_float2(0.24261054396629333f, 0.24261054396629333f));
+  p = ffma2(p, f, make_float2(0.6932609677314758f, 0.6932609677314758f));
+  p = ffma2(p, f, make_float2(0.9999281167984009f, 0.9999281167984009f));
+  p.x = __uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23));
+  p.y = __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23));
+  return p;
+}
+
+__device__ __forceinline__ void setmaxnreg_inc176() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 176;" ::: "memory");
 }
 __device__ __forceinline__ void setmaxnreg_dec80() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
 }
-__device__ __forceinline__ void setmaxnreg_dec48() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 48;" ::: "memory");
+__device__ __forceinline__ void setmaxnreg_dec80b() {  // warps 12-15
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
 }
 
 template <int D, bool CAUSAL>
@@ -167,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (wg < QT) {
-    setmaxnreg_inc192();
+    setmaxnreg_inc176();
     // ------------------------------------------------------------ softmax
     const int i = wg;                        // query tile
     const int r = threadIdx.x - i * BM;      // row within the tile == TMEM lane
@@ -196,10 +239,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < BN; ++c)
           if (kv0 + c > lim) s[c] = -INFINITY;
       }
-      float mt = s[0];
+      // Row max: four independent chains of 3-input max.
+      float mx[4];
 #pragma unroll
-      for (int c = 1; c < BN; ++c) mt = fmaxf(mt, s[c]);
-      const float m_tile = mt * scale_log2;
+      for (int q = 0; q < 4; ++q) {
+        mx[q] = s[32 * q];
+#pragma unroll
+        for (int c = 1; c + 1 < 32; c += 2) mx[q] = fmax3(mx[q], s[32 * q + c], s[32 * q + c + 1]);
+        mx[q] = fmaxf(mx[q], s[32 * q + 31]);
+      }
+      const float m_tile = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]) * scale_log2;
       float alpha = 1.f;
       if (m_tile - m > kRescaleThreshold) {   // true on the first tile (m = -inf)
         alpha = ex2_approx(m - m_tile);
@@ -208,15 +257,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       alpha_s[i * BM + r] = alpha;
       mbar_arrive(B_A(i));
       const float m_use = (m == -INFINITY) ? 0.f : m;
-      float rs = 0.f;
+      const float2 sc2 = make_float2(scale_log2, scale_log2);
+      const float2 nm2 = make_float2(-m_use, -m_use);
+      float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       uint32_t pk[BN / 2];
 #pragma unroll
       for (int c = 0; c < BN / 2; ++c) {
-        const float p0 = ex2_approx(fmaf(s[2 * c], scale_log2, -m_use));
-        const float p1 = ex2_approx(fmaf(s[2 * c + 1], scale_log2, -m_use));
-        rs += p0 + p1;
-        pk[c] = pack_bf16x2(p0, p1);
+        const float2 x = ffma2(make_float2(s[2 * c], s[2 * c + 1]), sc2, nm2);
+        float2 p;
+        if ((c & 7) < kPolyPairsPer8) {
+          p = exp2_poly2(x);
+        } else {
+          p.x = ex2_approx(x.x);
+          p.y = ex2_approx(x.y);
+        }
+        rs2[c & 1] = fadd2(rs2[c & 1], p);
+        pk[c] = pack_bf16x2(p.x, p.y);
       }
+      const float rs = (rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y);
       l = l * alpha + rs;
       // P_i (bf16, keys packed in pairs) over the first 64 columns of S_i.
       tmem_st_32cols(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
@@ -291,10 +349,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
   } else {
-    setmaxnreg_dec48();
+    setmaxnreg_dec80b();
+    // Warps 12 and 13 run their schedules warp-uniformly (every lane waits on the
+    // barriers) and one elected lane issues the TMA copies / MMAs, so addresses
+    // and descriptors stay in the warp-uniform datapath.
     if (warp == kWarpTMA) {
       // ------------------------------------------------------ TMA producer
-      if (lane == 0) {
+      const bool leader = elect_one();
+      if (leader) {
         mbar_arrive_expect_tx(B_Q, QT * C::Q_BYTES);
 #pragma unroll
         for (int i = 0; i < QT; ++i)
@@ -302,98 +364,112 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kb = 0; kb < C::KB; ++kb)
             tma_load_3d(sb + C::OFF_Q + i * C::Q_BYTES + kb * kBoxBytes, &tmQ, kb * 64,
                         q0 + i * BM, bh, B_Q);
-        int issued_k = 0, issued_v = 0;
-        for (int j = 0; j < n1; ++j) {
-          const int sk = j % SK;
-          if (!mbar_wait(B_KE(sk), ((j / SK) & 1) ^ 1u, status, abort_flag)) break;
+      }
+      int issued_k = 0, issued_v = 0;
+      for (int j = 0; j < n1; ++j) {
+        const int sk = j % SK;
+        if (!__all_sync(0xffffffffu, mbar_wait(B_KE(sk), ((j / SK) & 1) ^ 1u, status, abort_flag)))
+          break;
+        if (leader) {
           mbar_arrive_expect_tx(B_KF(sk), C::KV_BYTES);
 #pragma unroll
           for (int kb = 0; kb < C::KB; ++kb)
             tma_load_3d(sb + C::OFF_K + sk * C::KV_BYTES + kb * kBoxBytes, &tmK, kb * 64, j * BN,
                         bh, B_KF(sk));
-          issued_k = j + 1;
-          const int sv = j % SV;
-          if (!mbar_wait(B_VE(sv), ((j / SV) & 1) ^ 1u, status, abort_flag)) break;
+        }
+        issued_k = j + 1;
+        const int sv = j % SV;
+        if (!__all_sync(0xffffffffu, mbar_wait(B_VE(sv), ((j / SV) & 1) ^ 1u, status, abort_flag)))
+          break;
+        if (leader) {
           mbar_arrive_expect_tx(B_VF(sv), C::KV_BYTES);
 #pragma unroll
           for (int kb = 0; kb < C::KB; ++kb)
             tma_load_3d(sb + C::OFF_V + sv * C::KV_BYTES + kb * kBoxBytes, &tmV, kb * 64, j * BN,
                         bh, B_VF(sv));
-          issued_v = j + 1;
         }
-        if (*abort_flag) {
-          // Let every copy this thread started land before the CTA exits.
-          mbar_wait_drain(B_Q, 0, 100000000ull);
-          for (int s = 0; s < SK && s < issued_k; ++s)
-            mbar_wait_drain(B_KF(s), (((issued_k - 1 - s) / SK)) & 1, 100000000ull);
-          for (int s = 0; s < SV && s < issued_v; ++s)
-            mbar_wait_drain(B_VF(s), (((issued_v - 1 - s) / SV)) & 1, 100000000ull);
-        }
+        issued_v = j + 1;
+      }
+      if (leader && *abort_flag) {
+        // Let every copy this warp started land before the CTA exits.
+        mbar_wait_drain(B_Q, 0, 100000000ull);
+        for (int s = 0; s < SK && s < issued_k; ++s)
+          mbar_wait_drain(B_KF(s), (((issued_k - 1 - s) / SK)) & 1, 100000000ull);
+        for (int s = 0; s < SV && s < issued_v; ++s)
+          mbar_wait_drain(B_VF(s), (((issued_v - 1 - s) / SV)) & 1, 100000000ull);
       }
       __syncwarp();
     } else if (warp == kWarpMMA) {
       // ------------------------------------------------------- MMA issuer
-      if (lane == 0) {
-        constexpr uint32_t kIdescQK = make_idesc_bf16(BM, BN, 0, 0);
-        constexpr uint32_t kIdescPV = make_idesc_bf16(BM, D, 0, 1);
-        // S_i = Q_i K^T: both operands K-major (head dim contiguous), 128-B swizzle.
-        auto issue_qk = [&](int i, int sk) {
+      const bool leader = elect_one();
+      constexpr uint32_t kIdescQK = make_idesc_bf16(BM, BN, 0, 0);
+      constexpr uint32_t kIdescPV = make_idesc_bf16(BM, D, 0, 1);
+      // Base descriptors; a k-step or stage moves only the start-address field
+      // (byte offset / 16 added to the low bits).
+      const uint64_t dQ = make_sdesc_sw128(sb + C::OFF_Q, 16, 1024);
+      const uint64_t dK = make_sdesc_sw128(sb + C::OFF_K, 16, 1024);
+      const uint64_t dV = make_sdesc_sw128(sb + C::OFF_V, kBoxBytes, 1024);
+      // S_i = Q_i K^T: both operands K-major (head dim contiguous), 128-B swizzle.
+      auto issue_qk = [&](int i, int sk) {
 #pragma unroll 1
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t koff = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-            const uint64_t a =
-                make_sdesc_sw128(sb + C::OFF_Q + i * C::Q_BYTES + koff, 16, 1024);
-            const uint64_t b =
-                make_sdesc_sw128(sb + C::OFF_K + sk * C::KV_BYTES + koff, 16, 1024);
-            mma_bf16_ss(tmem + C::TMEM_S + i * BN, a, b, kIdescQK, kk > 0 ? 1u : 0u);
-          }
-        };
-        // O_i += P_i V: P_i from TMEM (8 columns = 16 keys per step); V is MN-major
-        // (head dim contiguous), 64-column blocks kBoxBytes apart, 8-key groups 1024 B apart.
-        auto issue_pv = [&](int i, int sv, bool acc) {
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+          mma_bf16_ss(tmem + C::TMEM_S + i * BN, dQ + ((i * C::Q_BYTES) >> 4) + koff,
+                      dK + ((sk * C::KV_BYTES) >> 4) + koff, kIdescQK, kk > 0 ? 1u : 0u);
+        }
+      };
+      // O_i += P_i V: P_i from TMEM (8 columns = 16 keys per step); V is MN-major
+      // (head dim contiguous), 64-column blocks kBoxBytes apart, 8-key groups 1024 B apart.
+      auto issue_pv = [&](int i, int sv, bool acc) {
 #pragma unroll 1
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint64_t b =
-                make_sdesc_sw128(sb + C::OFF_V + sv * C::KV_BYTES + kk * 16 * 128, kBoxBytes, 1024);
-            mma_bf16_ts(tmem + C::TMEM_O + i * D, tmem + C::TMEM_S + i * BN + kk * 8, b, kIdescPV,
-                        (acc || kk > 0) ? 1u : 0u);
-          }
-        };
-        bool ok =
-            mbar_wait(B_Q, 0, status, abort_flag) && mbar_wait(B_KF(0), 0, status, abort_flag);
-        if (ok) {
-          tc_fence_after();
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_bf16_ts(tmem + C::TMEM_O + i * D, tmem + C::TMEM_S + i * BN + kk * 8,
+                      dV + ((sv * C::KV_BYTES + kk * 16 * 128) >> 4), kIdescPV,
+                      (acc || kk > 0) ? 1u : 0u);
+      };
+      auto wait_all = [&](uint32_t bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, abort_flag));
+      };
+      bool ok = wait_all(B_Q, 0) && wait_all(B_KF(0), 0);
+      if (ok) {
+        tc_fence_after();
+        if (leader) {
           issue_qk(0, 0);
           mma_commit(B_S(0));
           issue_qk(1, 0);
           mma_commit(B_S(1));
           if (SK < n1) mma_commit(B_KE(0));
         }
-        for (int j = 0; ok && j < n1; ++j) {
-          const int sv = j % SV;
-          if (!(ok = mbar_wait(B_VF(sv), (j / SV) & 1, status, abort_flag))) break;
-          if (j < n0) {
-            ok = mbar_wait(B_P(0), j & 1, status, abort_flag) &&
-                 mbar_wait(B_C(0), j & 1, status, abort_flag);
-            if (!ok) break;
-            tc_fence_after();
+        __syncwarp();
+      }
+      for (int j = 0; ok && j < n1; ++j) {
+        const int sv = j % SV;
+        if (!(ok = wait_all(B_VF(sv), (j / SV) & 1))) break;
+        if (j < n0) {
+          if (!(ok = wait_all(B_P(0), j & 1) && wait_all(B_C(0), j & 1))) break;
+          tc_fence_after();
+          if (leader) {
             issue_pv(0, sv, j > 0);
             mma_commit(B_O(0));
           }
-          const bool more = j + 1 < n1;
-          const int sk1 = (j + 1) % SK;
-          if (more) {
-            if (!(ok = mbar_wait(B_KF(sk1), ((j + 1) / SK) & 1, status, abort_flag))) break;
-            tc_fence_after();
-            if (j + 1 < n0) {
+          __syncwarp();
+        }
+        const bool more = j + 1 < n1;
+        const int sk1 = (j + 1) % SK;
+        if (more) {
+          if (!(ok = wait_all(B_KF(sk1), ((j + 1) / SK) & 1))) break;
+          tc_fence_after();
+          if (j + 1 < n0) {
+            if (leader) {
               issue_qk(0, sk1);   // overwrites S_0/P_0 after the P_0 V_j MMA above has read it
               mma_commit(B_S(0));
             }
+            __syncwarp();
           }
-          ok = mbar_wait(B_P(1), j & 1, status, abort_flag) &&
-               mbar_wait(B_C(1), j & 1, status, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
+        }
+        if (!(ok = wait_all(B_P(1), j & 1) && wait_all(B_C(1), j & 1))) break;
+        tc_fence_after();
+        if (leader) {
           issue_pv(1, sv, j > 0);
           mma_commit(B_O(1));
           if (j + SV < n1) mma_commit(B_VE(sv));
@@ -403,7 +479,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (j + 1 + SK < n1) mma_commit(B_KE(sk1));
           }
         }
-        // Every MMA issued so far must finish before TMEM is released.
+        __syncwarp();
+      }
+      // Every MMA issued so far must finish before TMEM is released.
+      if (leader) {
         mma_commit(B_DRAIN);
         mbar_wait_drain(B_DRAIN, 0, 100000000ull);
       }
