@@ -65,6 +65,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of a phase.  Several tests issued back to back overlap
+// their shared-memory round trips (~140 clk each when done one after another).
+__device__ __forceinline__ uint32_t mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok;
+}
+
 // Wait for the phase with the given parity to complete, for at most
 // kWaitLimitNs.  Returns false (and raises the timeout bit and the CTA's
 // abort flag) if it gives up, or false at once if another role of the CTA has
