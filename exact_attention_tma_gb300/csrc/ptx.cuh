@@ -79,6 +79,22 @@ __device__ __forceinline__ uint32_t mbar_test(uint32_t bar, uint32_t parity) {
   return ok;
 }
 
+// Warp vote "all lanes non-zero", as volatile inline asm so that it stays
+// after the preceding volatile asm (MMA issue, TMEM stores): a test issued
+// earlier is then consumed late, after its round trip has completed.
+__device__ __forceinline__ bool vote_all_ordered(uint32_t v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "vote.sync.all.pred q, p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(v)
+      : "memory");
+  return r != 0;
+}
+
 // Wait for the phase with the given parity to complete, for at most
 // kWaitLimitNs.  Returns false (and raises the timeout bit and the CTA's
 // abort flag) if it gives up, or false at once if another role of the CTA has
