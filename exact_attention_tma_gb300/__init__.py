@@ -18,8 +18,8 @@ import threading
 __all__ = [
     "AttnError", "attn_fwd", "attn_decode", "attn_decode_ws",
     "attn_decode_workspace_bytes", "attn_get_device_status", "attn_status_string",
-    "attn_decode_num_splits", "attn_decode_noalloc", "forward", "decode", "library_path",
-    "load",
+    "attn_decode_num_splits", "attn_decode_noalloc", "attn_selftest_bounded_wait", "forward",
+    "decode", "library_path", "load",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -56,6 +56,8 @@ def load():
             lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
             lib.attn_decode.argtypes = [vp, vp, vp, vp, i, i, i, i, f, vp]
             lib.attn_decode_ws.argtypes = [vp, vp, vp, vp, i, i, i, i, f, vp, sz, vp]
+            lib.attn_selftest_bounded_wait.argtypes = [i, vp]
+            lib.attn_selftest_bounded_wait.restype = ctypes.c_int
             lib.attn_decode_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, f, vp]
             lib.attn_decode_noalloc.restype = ctypes.c_int
             lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i]
@@ -184,6 +186,12 @@ def attn_decode_noalloc(q, Kcache, Vcache, O, scale: float, stream=None) -> None
             _dev(Vcache, "Vcache", torch.bfloat16), _dev(O, "O", torch.bfloat16)]
     _check(load().attn_decode_noalloc(*args, B, H, L, d, float(scale), _stream(stream)),
            "attn_decode_noalloc")
+
+
+def attn_selftest_bounded_wait(limit_ms: int, stream=None) -> None:
+    """Launch the bounded-wait self-test (see include/exact_attn_selftest.h)."""
+    _check(load().attn_selftest_bounded_wait(int(limit_ms), _stream(stream)),
+           "attn_selftest_bounded_wait")
 
 
 def attn_get_device_status(stream=None) -> int:

@@ -65,6 +65,10 @@ attn_status check_decode(const void *q, const void *K, const void *V, const void
 
 }  // namespace
 
+cudaError_t ea::device_status_word(unsigned **out) {
+  return status_ptr(out) == ATTN_OK ? cudaSuccess : cudaErrorUnknown;
+}
+
 extern "C" {
 
 attn_status attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,

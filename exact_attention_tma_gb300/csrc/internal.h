@@ -14,6 +14,9 @@ cudaError_t launch_fwd(const void *Q, const void *K, const void *V, void *O, flo
                        int H, int N, int d, float scale, int causal, unsigned *status,
                        cudaStream_t stream);
 
+// Device address of the current device's status word (looked up once per device).
+cudaError_t device_status_word(unsigned **out);
+
 // Decode: split kernel + combine kernel on `stream`, partials in `ws`.
 constexpr int kDecodeSplits = 32;
 size_t decode_ws_bytes(int B, int H, int d);

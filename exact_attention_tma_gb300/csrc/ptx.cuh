@@ -96,24 +96,30 @@ __device__ __forceinline__ bool vote_all_ordered(uint32_t v) {
 }
 
 // Wait for the phase with the given parity to complete, for at most
-// kWaitLimitNs.  Returns false (and raises the timeout bit and the CTA's
+// limit_ns (kWaitLimitNs in the kernels).  Returns false (and raises the timeout bit and the CTA's
 // abort flag) if it gives up, or false at once if another role of the CTA has
 // already raised the abort flag.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned *status,
-                                          volatile int *abort_flag) {
+__device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, unsigned *status,
+                                                volatile int *abort_flag,
+                                                unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         atomicOr(status, kStatusTimeoutBit);
         *abort_flag = 1;
         return false;
       }
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned *status,
+                                          volatile int *abort_flag) {
+  return mbar_wait_limit(bar, parity, status, abort_flag, kWaitLimitNs);
 }
 
 // Same as mbar_wait but without the abort flag (used while draining).

@@ -111,6 +111,11 @@ def test_decode_ws_checks_workspace(lib):
                               None) == NOMEM
 
 
+@pytest.mark.parametrize("limit_ms", [0, -5, 10001])
+def test_selftest_rejects_bad_limit_before_launch(lib, limit_ms):
+    assert lib.attn_selftest_bounded_wait(limit_ms, None) == ARG
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(ea, "_lib", None)
     monkeypatch.setattr(ea, "_LIB_PATH", str(tmp_path / "nope.so"))
