@@ -14,22 +14,29 @@
 // and streams that head's K/V tiles once for both.  16 warps:
 //   warps 0-3   softmax for query tile 0   (thread = row = TMEM lane)
 //   warps 4-7   softmax for query tile 1
-//   warps 8-11  correction: rescales a tile's O accumulator in TMEM when its
-//               running max moved by more than 2^8 (lazy rescaling: between
-//               rescales the stale max is used for both P and the row sum, so
-//               the final O / l is unchanged and P stays <= 256)
-//   warp 12     MMA issuer (one thread): tcgen05.mma S_i = Q_i K_j^T into TMEM
-//               (both operands from swizzled shared memory), then
+//   warp 8      MMA issuer (one elected lane): tcgen05.mma S_i = Q_i K_j^T into
+//               TMEM (both operands from swizzled shared memory), then
 //               O_i += P_i V_j with P_i read straight from TMEM (it overwrites
 //               the first half of S_i as packed bf16)
-//   warp 13     TMA producer: Q tiles once, K_j and V_j into separate rings
+//   warp 9      TMA producer: Q tiles once, K_j and V_j into separate rings
 //               guarded by full/empty mbarriers
-//   warps 14-15 idle
+//   warps 10-15 idle
 // The two softmax warpgroups work on different query tiles, so while one
 // computes exponentials the tensor core runs the other tile's MMAs.
-// Registers are re-balanced with setmaxnreg: 176 per softmax thread, 80 per
-// correction thread and 80 for warps 12-15 (2*128*176 + 2*128*80 = 65536, the
-// block's launch allocation of 512 threads x 128).
+//
+// Softmax per K/V tile, in the exp2 domain (x = s * scale * log2 e):
+// the exponentials are computed against the running maximum m straight away
+// while the tile's own maximum is tracked alongside (no separate max pass).
+// Only if some row's maximum exceeds m by more than 2^8 (lazy rescaling) is
+// the tile redone with the new maximum and that row's O accumulator scaled by
+// 2^(m_old - m_new) in TMEM; otherwise the stale m is kept for both P and the
+// row sum, so O / l is unchanged and P stays below 2^8.  The first tile
+// computes its maximum first.  O_i is quiescent while the softmax of tile i
+// runs: the MMA that wrote it last was committed before S_i was.
+//
+// Registers are re-balanced with setmaxnreg: 192 per softmax thread, 96 for
+// warps 8-11 and 32 for the idle warps 12-15 (256*192 + 128*96 + 128*32 =
+// 65536, the block's launch allocation of 512 threads x 128).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -47,8 +54,8 @@ constexpr int BM = 128;                  // query rows per tile (B_r)
 constexpr int BN = 128;                  // keys per K/V tile (B_c)
 constexpr int QT = 2;                    // query tiles per CTA
 constexpr int kThreads = 512;
-constexpr int kWarpMMA = 12;
-constexpr int kWarpTMA = 13;
+constexpr int kWarpMMA = 8;
+constexpr int kWarpTMA = 9;
 constexpr uint32_t kTmemCols = 512;      // S0 | S1 | O0 | O1
 constexpr uint32_t kBoxBytes = 64 * 128 * 2;   // one TMA box: 64 columns x 128 rows bf16
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -80,10 +87,9 @@ struct Cfg {
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = OFF_Q + QT * Q_BYTES;
   static constexpr uint32_t OFF_V = OFF_K + SK * KV_BYTES;
-  static constexpr uint32_t OFF_ALPHA = OFF_V + SV * KV_BYTES;   // float[QT][BM]
-  static constexpr uint32_t OFF_BAR = OFF_ALPHA + QT * BM * 4;
-  // q, kf[SK], ke[SK], vf[SV], ve[SV], s[2], p[2], a[2], c[2], o[2], drain
-  static constexpr int NBAR = 1 + 2 * SK + 2 * SV + 5 * QT + 1;
+  static constexpr uint32_t OFF_BAR = OFF_V + SV * KV_BYTES;
+  // q, kf[SK], ke[SK], vf[SV], ve[SV], s[QT], p[QT], o[QT], drain
+  static constexpr int NBAR = 1 + 2 * SK + 2 * SV + 3 * QT + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;
   static constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;   // 1024-byte alignment slack
@@ -93,42 +99,41 @@ struct Cfg {
   static_assert(TMEM_O + QT * D <= kTmemCols, "tensor memory budget");
 };
 
-// Pairs (out of every 8 pairs of a row) whose exp2 runs on the FMA pipe
-// through exp2_poly2 instead of the MUFU ex2 unit, to balance the two pipes.
-#ifndef EA_POLY_PAIRS_PER8
-#define EA_POLY_PAIRS_PER8 0
-#endif
-constexpr int kPolyPairsPer8 = EA_POLY_PAIRS_PER8;
-
-// 2^x for two lanes on the FMA pipe.  Cody-Waite range reduction: j = round(x)
-// via the float32 "add 1.5 * 2^23" trick (j ends up in the low mantissa bits
-// of t), f = x - j in [-1/2, 1/2]; 2^f from a degree-3 polynomial whose max
-// relative error on [-1/2, 1/2] is 7.5e-5 (minimax fit by Lawson's algorithm,
-// exact_attention_tma_gb300/exp2_poly.py); j is added to the exponent field.
-// x is clamped at -126 so the exponent stays in range (masked -inf -> ~1e-38).
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-  x.x = fmaxf(x.x, -126.f);
-  x.y = fmaxf(x.y, -126.f);
-  const float2 t = fadd2(x, make_float2(12582912.f, 12582912.f));
-  const float2 j = fadd2(t, make_float2(-12582912.f, -12582912.f));
-  const float2 f = ffma2(j, make_float2(-1.f, -1.f), x);
-  float2 p = ffma2(make_float2(0.05517132207751274f, 0.05517132207751274f), f,
-                   make_float2(0.24261054396629333f, 0.24261054396629333f));
-  p = ffma2(p, f, make_float2(0.6932609677314758f, 0.6932609677314758f));
-  p = ffma2(p, f, make_float2(0.9999281167984009f, 0.9999281167984009f));
-  p.x = __uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23));
-  p.y = __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23));
-  return p;
+__device__ __forceinline__ void setmaxnreg_inc192() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
+}
+__device__ __forceinline__ void setmaxnreg_dec96() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 96;" ::: "memory");
+}
+__device__ __forceinline__ void setmaxnreg_dec32() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 32;" ::: "memory");
 }
 
-__device__ __forceinline__ void setmaxnreg_inc176() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 176;" ::: "memory");
+// exp2 of 32 consecutive scores of one row against the maximum m (-nm = m):
+// p = 2^(s * scale_log2 - m), packed as bf16 pairs into pk; adds the p to the
+// two fp32x2 partial sums rs2 and folds s * scale_log2 - m into the running
+// maxima mx (two independent 3-input max chains).
+__device__ __forceinline__ void exp_chunk(const uint32_t (&sr)[32], float2 sc2, float2 nm2,
+                                          uint32_t *pk, float2 (&rs2)[2], float (&mx)[2]) {
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    const float2 x = ffma2(make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])),
+                           sc2, nm2);
+    mx[c & 1] = fmax3(mx[c & 1], x.x, x.y);
+    const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+    rs2[c & 1] = fadd2(rs2[c & 1], p);
+    pk[c] = pack_bf16x2(p.x, p.y);
+  }
 }
-__device__ __forceinline__ void setmaxnreg_dec80() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
-}
-__device__ __forceinline__ void setmaxnreg_dec80b() {  // warps 12-15
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
+
+// Scores of keys kv0 + col0 .. kv0 + col0 + 31 that lie past the last visible
+// key lim become -inf (so p = 0).
+__device__ __forceinline__ void mask_chunk(uint32_t (&sr)[32], int first_key, int lim) {
+  if (first_key + 31 > lim) {
+#pragma unroll
+    for (int c = 0; c < 32; ++c)
+      if (first_key + c > lim) sr[c] = __float_as_uint(-INFINITY);
+  }
 }
 
 template <int D, bool CAUSAL>
@@ -148,9 +153,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int wg = warp >> 2;
 
-  // Heads vary fastest; for causal the longest query blocks go first.
-  const int bh = blockIdx.x % BH;
-  const int blk = n_blk - 1 - static_cast<int>(blockIdx.x / BH);
+  // Causal: heads vary fastest and the longest query blocks go first, so the
+  // hardware scheduler balances the unequal blocks.  Non-causal: all blocks
+  // cost the same, so query blocks vary fastest and the co-resident CTAs share
+  // a few heads' K/V through L2 instead of each streaming its own head.
+  const int bh = CAUSAL ? static_cast<int>(blockIdx.x % BH) : static_cast<int>(blockIdx.x / n_blk);
+  const int blk = CAUSAL ? n_blk - 1 - static_cast<int>(blockIdx.x / BH)
+                         : static_cast<int>(blockIdx.x % n_blk);
   const int q0 = blk * (QT * BM);
   const int n_kv_total = (N + BN - 1) / BN;
   // K/V tiles each query tile needs (query tile 0 can stop one tile earlier when causal).
@@ -166,11 +175,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kB5 = 1 + 2 * SK + 2 * SV;
   auto B_S = [&](int i) { return bar0 + 8u * (kB5 + i); };            // S_i ready (MMA)
   auto B_P = [&](int i) { return bar0 + 8u * (kB5 + QT + i); };       // P_i written (softmax)
-  auto B_A = [&](int i) { return bar0 + 8u * (kB5 + 2 * QT + i); };   // alpha_i ready (softmax)
-  auto B_C = [&](int i) { return bar0 + 8u * (kB5 + 3 * QT + i); };   // O_i corrected
-  auto B_O = [&](int i) { return bar0 + 8u * (kB5 + 4 * QT + i); };   // P_i V_j done (MMA)
-  const uint32_t B_DRAIN = bar0 + 8u * (kB5 + 5 * QT);
-  float *alpha_s = reinterpret_cast<float *>(smem + C::OFF_ALPHA);
+  auto B_O = [&](int i) { return bar0 + 8u * (kB5 + 2 * QT + i); };   // last P_i V_j done (MMA)
+  const uint32_t B_DRAIN = bar0 + 8u * (kB5 + 3 * QT);
+  static_assert(kB5 + 3 * QT + 1 == C::NBAR, "barrier count");
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
@@ -187,8 +194,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < QT; ++i) {
       mbar_init(B_S(i), 1);
       mbar_init(B_P(i), BM);
-      mbar_init(B_A(i), BM);
-      mbar_init(B_C(i), BM);
       mbar_init(B_O(i), 1);
     }
     mbar_init(B_DRAIN, 1);
@@ -210,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (wg < QT) {
-    setmaxnreg_inc176();
+    setmaxnreg_inc192();
     // ------------------------------------------------------------ softmax
     const int i = wg;                        // query tile
     const int r = threadIdx.x - i * BM;      // row within the tile == TMEM lane
@@ -219,62 +224,89 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lim = CAUSAL ? min(qrow, N - 1) : N - 1;   // last visible key
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t s_addr = tmem + lane_addr + C::TMEM_S + i * BN;
-    float m = -INFINITY;                     // max used for the exponentials (base 2)
+    const uint32_t o_addr = tmem + lane_addr + C::TMEM_O + i * D;
+    const float2 sc2 = make_float2(scale_log2, scale_log2);
+    // One pass over S_i: P = 2^(x - m_use) into pk, its row sum, and the row's
+    // maximum of x - m_use.  Keys 64-127 are read from TMEM while keys 0-63
+    // are exponentiated.
+    auto pass = [&](int kv0, float m_use, uint32_t (&pk)[BN / 2], float &rs, float &mx_out) {
+      const float2 nm2 = make_float2(-m_use, -m_use);
+      float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      float mx[2] = {-INFINITY, -INFINITY};
+      uint32_t a[32], b[32], c[32], d[32];
+      tmem_ld_32cols(s_addr, a);
+      tmem_ld_32cols(s_addr + 32, b);
+      tmem_ld_wait_regs(a);
+      reg_fence32(b);
+      tmem_ld_32cols(s_addr + 64, c);
+      tmem_ld_32cols(s_addr + 96, d);
+      mask_chunk(a, kv0, lim);
+      mask_chunk(b, kv0 + 32, lim);
+      exp_chunk(a, sc2, nm2, &pk[0], rs2, mx);
+      exp_chunk(b, sc2, nm2, &pk[16], rs2, mx);
+      __syncwarp();
+      tmem_ld_wait_regs(c);
+      reg_fence32(d);
+      mask_chunk(c, kv0 + 64, lim);
+      mask_chunk(d, kv0 + 96, lim);
+      exp_chunk(c, sc2, nm2, &pk[32], rs2, mx);
+      exp_chunk(d, sc2, nm2, &pk[48], rs2, mx);
+      rs = (rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y);
+      mx_out = fmaxf(mx[0], mx[1]);
+    };
+    float m = 0.f;                           // max used for the exponentials (base 2)
     float l = 0.f;                           // running sum of exp2(x - m)
     bool ok = true;
     for (int j = 0; j < n_i; ++j) {
       ok = __all_sync(0xffffffffu, mbar_wait(B_S(i), j & 1, status, abort_flag));
       if (!ok) break;
       tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld_32cols(s_addr + c * 32, sr[c]);
-      tmem_ld_wait();
-      float s[BN];
-#pragma unroll
-      for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
       const int kv0 = j * BN;
-      if (kv0 + BN - 1 > lim) {
+      if (j == 0) {
+        // First tile: its row maximum first (every row sees at least key 0).
+        uint32_t sr[4][32];
 #pragma unroll
-        for (int c = 0; c < BN; ++c)
-          if (kv0 + c > lim) s[c] = -INFINITY;
-      }
-      // Row max: four independent chains of 3-input max.
-      float mx[4];
+        for (int c = 0; c < 4; ++c) tmem_ld_32cols(s_addr + c * 32, sr[c]);
+        tmem_ld_wait_regs(sr[0]);
+        reg_fence32(sr[1]);
+        reg_fence32(sr[2]);
+        reg_fence32(sr[3]);
+        float mq[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        mx[q] = s[32 * q];
+        for (int q = 0; q < 4; ++q) {
+          mask_chunk(sr[q], kv0 + 32 * q, lim);
+          mq[q] = __uint_as_float(sr[q][0]);
 #pragma unroll
-        for (int c = 1; c + 1 < 32; c += 2) mx[q] = fmax3(mx[q], s[32 * q + c], s[32 * q + c + 1]);
-        mx[q] = fmaxf(mx[q], s[32 * q + 31]);
-      }
-      const float m_tile = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]) * scale_log2;
-      float alpha = 1.f;
-      if (m_tile - m > kRescaleThreshold) {   // true on the first tile (m = -inf)
-        alpha = ex2_approx(m - m_tile);
-        m = m_tile;
-      }
-      alpha_s[i * BM + r] = alpha;
-      mbar_arrive(B_A(i));
-      const float m_use = (m == -INFINITY) ? 0.f : m;
-      const float2 sc2 = make_float2(scale_log2, scale_log2);
-      const float2 nm2 = make_float2(-m_use, -m_use);
-      float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      uint32_t pk[BN / 2];
-#pragma unroll
-      for (int c = 0; c < BN / 2; ++c) {
-        const float2 x = ffma2(make_float2(s[2 * c], s[2 * c + 1]), sc2, nm2);
-        float2 p;
-        if ((c & 7) < kPolyPairsPer8) {
-          p = exp2_poly2(x);
-        } else {
-          p.x = ex2_approx(x.x);
-          p.y = ex2_approx(x.y);
+          for (int c = 1; c + 1 < 32; c += 2)
+            mq[q] = fmax3(mq[q], __uint_as_float(sr[q][c]), __uint_as_float(sr[q][c + 1]));
+          mq[q] = fmaxf(mq[q], __uint_as_float(sr[q][31]));
         }
-        rs2[c & 1] = fadd2(rs2[c & 1], p);
-        pk[c] = pack_bf16x2(p.x, p.y);
+        __syncwarp();
+        m = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * scale_log2;
       }
-      const float rs = (rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y);
+      uint32_t pk[BN / 2];
+      float rs, mx;
+      pass(kv0, m, pk, rs, mx);
+      float alpha = 1.f;
+      if (__any_sync(0xffffffffu, mx > kRescaleThreshold)) {
+        // Some row's maximum grew by more than 2^8: redo the tile with the new
+        // maximum and scale those rows' O_i by 2^(m_old - m_new).
+        const float m_new = (mx > kRescaleThreshold) ? m + mx : m;
+        alpha = ex2_approx(m - m_new);
+        m = m_new;
+        pass(kv0, m, pk, rs, mx);
+        if (j > 0) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld_32cols(o_addr + c * 32, o);
+            tmem_ld_wait_regs(o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st_32cols(o_addr + c * 32, o);
+          }
+        }
+      }
       l = l * alpha + rs;
       // P_i (bf16, keys packed in pairs) over the first 64 columns of S_i.
       tmem_st_32cols(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
@@ -284,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(B_P(i));
     }
     // Epilogue: O_i / l -> bf16 rows, LSE.
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(B_O(i), (n_i - 1) & 1, status, abort_flag));
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(B_O(i), 0, status, abort_flag));
     if (ok) {
       tc_fence_after();
       const float inv_l = 1.f / l;
@@ -292,8 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
-        tmem_ld_32cols(tmem + lane_addr + C::TMEM_O + i * D + c * 32, o);
-        tmem_ld_wait();
+        tmem_ld_32cols(o_addr + c * 32, o);
+        tmem_ld_wait_regs(o);
         if (qrow < N) {
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
@@ -305,6 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             st_global_v4(orow + c * 32 + v * 8, w[0], w[1], w[2], w[3]);
           }
         }
+        __syncwarp();
       }
       if (qrow < N) {
         float lg;
@@ -314,43 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
   } else if (wg == QT) {
-    setmaxnreg_dec80();
-    // --------------------------------------------------------- correction
-    const int t = threadIdx.x - QT * BM;     // row == TMEM lane
-    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    bool ok = true;
-    for (int j = 0; ok && j < n1; ++j) {
-#pragma unroll
-      for (int i = 0; i < QT; ++i) {
-        if (j >= (i == 0 ? n0 : n1)) continue;
-        ok = __all_sync(0xffffffffu, mbar_wait(B_A(i), j & 1, status, abort_flag));
-        if (!ok) break;
-        const float a = alpha_s[i * BM + t];
-        if (j > 0 && __any_sync(0xffffffffu, a != 1.f)) {
-          // P_i V_{j-1} must have landed before O_i is scaled.
-          ok = __all_sync(0xffffffffu, mbar_wait(B_O(i), (j - 1) & 1, status, abort_flag));
-          if (!ok) break;
-          tc_fence_after();
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            const uint32_t o_addr = tmem + lane_addr + C::TMEM_O + i * D + c * 32;
-            tmem_ld_32cols(o_addr, o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
-            tmem_st_32cols(o_addr, o);
-          }
-          tmem_st_wait();
-        }
-        tc_fence_before();
-        mbar_arrive(B_C(i));
-      }
-    }
-    tc_fence_before();
-  } else {
-    setmaxnreg_dec80b();
-    // Warps 12 and 13 run their schedules warp-uniformly (every lane waits on the
+    setmaxnreg_dec96();
+    // Warps 8 and 9 run their schedules warp-uniformly (every lane waits on the
     // barriers) and one elected lane issues the TMA copies / MMAs, so addresses
     // and descriptors stay in the warp-uniform datapath.
     if (warp == kWarpTMA) {
@@ -404,28 +402,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool leader = elect_one();
       constexpr uint32_t kIdescQK = make_idesc_bf16(BM, BN, 0, 0);
       constexpr uint32_t kIdescPV = make_idesc_bf16(BM, D, 0, 1);
-      // Base descriptors; a k-step or stage moves only the start-address field
-      // (byte offset / 16 added to the low bits).
+      // Shared-memory descriptors as low words over one common high word; a
+      // k-step or stage moves only the start-address field (byte offset / 16
+      // added to the low word).  The issue loops are unrolled so that each MMA
+      // costs two integer adds besides the tcgen05.mma itself.
       const uint64_t dQ = make_sdesc_sw128(sb + C::OFF_Q, 16, 1024);
       const uint64_t dK = make_sdesc_sw128(sb + C::OFF_K, 16, 1024);
       const uint64_t dV = make_sdesc_sw128(sb + C::OFF_V, kBoxBytes, 1024);
+      const uint32_t hi = static_cast<uint32_t>(dQ >> 32);   // identical for dK and dV
+      const uint32_t q_lo = static_cast<uint32_t>(dQ);
+      const uint32_t k_lo = static_cast<uint32_t>(dK);
+      const uint32_t v_lo = static_cast<uint32_t>(dV);
       // S_i = Q_i K^T: both operands K-major (head dim contiguous), 128-B swizzle.
       auto issue_qk = [&](int i, int sk) {
-#pragma unroll 1
+        const uint32_t a0 = q_lo + ((i * C::Q_BYTES) >> 4);
+        const uint32_t b0 = k_lo + ((sk * C::KV_BYTES) >> 4);
+#pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-          mma_bf16_ss(tmem + C::TMEM_S + i * BN, dQ + ((i * C::Q_BYTES) >> 4) + koff,
-                      dK + ((sk * C::KV_BYTES) >> 4) + koff, kIdescQK, kk > 0 ? 1u : 0u);
+          mma_bf16_ss_lo(tmem + C::TMEM_S + i * BN, a0 + koff, b0 + koff, hi, kIdescQK,
+                         kk > 0 ? 1u : 0u);
         }
       };
       // O_i += P_i V: P_i from TMEM (8 columns = 16 keys per step); V is MN-major
       // (head dim contiguous), 64-column blocks kBoxBytes apart, 8-key groups 1024 B apart.
       auto issue_pv = [&](int i, int sv, bool acc) {
-#pragma unroll 1
+        const uint32_t b0 = v_lo + ((sv * C::KV_BYTES) >> 4);
+#pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_bf16_ts(tmem + C::TMEM_O + i * D, tmem + C::TMEM_S + i * BN + kk * 8,
-                      dV + ((sv * C::KV_BYTES + kk * 16 * 128) >> 4), kIdescPV,
-                      (acc || kk > 0) ? 1u : 0u);
+          mma_bf16_ts_lo(tmem + C::TMEM_O + i * D, tmem + C::TMEM_S + i * BN + kk * 8,
+                         b0 + ((kk * 16 * 128) >> 4), hi, kIdescPV, (acc || kk > 0) ? 1u : 0u);
       };
       auto wait_all = [&](uint32_t bar, uint32_t parity) {
         return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, abort_flag));
@@ -442,36 +448,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       }
+      // Per K/V tile j: the V_j and K_{j+1} stages are checked first (they are
+      // normally resident long before), so that each softmax hand-off is
+      // followed by one wait and an uninterrupted run of MMAs:
+      // P_0 V_j, Q_0 K_{j+1}^T, then P_1 V_j, Q_1 K_{j+1}^T.
       for (int j = 0; ok && j < n1; ++j) {
         const int sv = j % SV;
+        const bool more = j + 1 < n1;
+        const int sk1 = (j + 1) % SK;
         if (!(ok = wait_all(B_VF(sv), (j / SV) & 1))) break;
+        if (more && !(ok = wait_all(B_KF(sk1), ((j + 1) / SK) & 1))) break;
         if (j < n0) {
-          if (!(ok = wait_all(B_P(0), j & 1) && wait_all(B_C(0), j & 1))) break;
+          if (!(ok = wait_all(B_P(0), j & 1))) break;
           tc_fence_after();
           if (leader) {
             issue_pv(0, sv, j > 0);
-            mma_commit(B_O(0));
+            if (j + 1 == n0) mma_commit(B_O(0));
+            if (j + 1 < n0) {
+              issue_qk(0, sk1);   // overwrites S_0/P_0 after the P_0 V_j MMAs above read it
+              mma_commit(B_S(0));
+            }
           }
           __syncwarp();
         }
-        const bool more = j + 1 < n1;
-        const int sk1 = (j + 1) % SK;
-        if (more) {
-          if (!(ok = wait_all(B_KF(sk1), ((j + 1) / SK) & 1))) break;
-          tc_fence_after();
-          if (j + 1 < n0) {
-            if (leader) {
-              issue_qk(0, sk1);   // overwrites S_0/P_0 after the P_0 V_j MMA above has read it
-              mma_commit(B_S(0));
-            }
-            __syncwarp();
-          }
-        }
-        if (!(ok = wait_all(B_P(1), j & 1) && wait_all(B_C(1), j & 1))) break;
+        if (!(ok = wait_all(B_P(1), j & 1))) break;
         tc_fence_after();
         if (leader) {
           issue_pv(1, sv, j > 0);
-          mma_commit(B_O(1));
+          if (j + 1 == n1) mma_commit(B_O(1));
           if (j + SV < n1) mma_commit(B_VE(sv));
           if (more) {
             issue_qk(1, sk1);
@@ -488,6 +492,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     }
+  } else {
+    setmaxnreg_dec32();   // warps 12-15: nothing to do
   }
   __syncthreads();
   if (warp == kWarpMMA) {

@@ -67,7 +67,8 @@ typedef enum {
  *   scale   : multiplies Q K^T before masking and softmax (finite, > 0).
  *   causal  : 0 = every key visible; 1 = key j visible to query i iff j <= i.
  *
- * One persistent tcgen05/TMA kernel launch; no workspace; S and P stay on chip.
+ * One tcgen05/TMA kernel launch (one CTA per 256 query rows of one head); no
+ * workspace; S and P stay on chip.
  * O and LSE are written exactly once per element.  O must not alias Q, K or V.
  */
 attn_status attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
