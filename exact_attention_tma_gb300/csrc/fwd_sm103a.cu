@@ -12,31 +12,36 @@
 //
 // GB300 mapping: one CTA owns two 128-row query tiles of one head (256 rows)
 // and streams that head's K/V tiles once for both.  16 warps:
-//   warps 0-3   softmax for query tile 0   (thread = row = TMEM lane)
-//   warps 4-7   softmax for query tile 1
+//   warps 0-7   softmax: warps q and q+4 share TMEM lanes 32q..32q+31, i.e.
+//               rows 32q..32q+31 of both query tiles; warp q takes keys 0-63
+//               of every K/V tile, warp q+4 keys 64-127 (thread = row)
 //   warp 8      MMA issuer (one elected lane): tcgen05.mma S_i = Q_i K_j^T into
 //               TMEM (both operands from swizzled shared memory), then
-//               O_i += P_i V_j with P_i read straight from TMEM (it overwrites
-//               the first half of S_i as packed bf16)
+//               O += P_i V_j with P_i read straight from TMEM (each key half
+//               overwrites the first 32 of its own 64 S columns as packed bf16)
 //   warp 9      TMA producer: Q tiles once, K_j and V_j into separate rings
 //               guarded by full/empty mbarriers
 //   warps 10-15 idle
-// The two softmax warpgroups work on different query tiles, so while one
-// computes exponentials the tensor core runs the other tile's MMAs.
+// The softmax warps work through S_0(j), S_1(j), S_0(j+1), ... while the tensor
+// core runs the other query tile's MMAs, and a tile's P is ready after half a
+// row's exponentials.
 //
-// Softmax per K/V tile, in the exp2 domain (x = s * scale * log2 e):
-// the exponentials are computed against the running maximum m straight away
-// while the tile's own maximum is tracked alongside (no separate max pass).
-// Only if some row's maximum exceeds m by more than 2^8 (lazy rescaling) is
-// the tile redone with the new maximum and that row's O accumulator scaled by
-// 2^(m_old - m_new) in TMEM; otherwise the stale m is kept for both P and the
-// row sum, so O / l is unchanged and P stays below 2^8.  The first tile
-// computes its maximum first.  O_i is quiescent while the softmax of tile i
-// runs: the MMA that wrote it last was committed before S_i was.
+// Softmax per K/V tile, in the exp2 domain (x = s * scale * log2 e): the
+// exponentials are computed against the running maximum m straight away (no
+// separate max pass).  Only if a key half's P sum exceeds 2^15 (so some P
+// exceeds 2^9: lazy rescaling) is the tile redone with the new maximum and the
+// O accumulator scaled by 2^(m_old - m_new) in TMEM; otherwise the stale m is
+// kept for both P and the row sum, so O / l is unchanged and P stays below
+// 2^15.  The first tile computes its maximum first.  O is quiescent while the
+// softmax of tile i runs: the MMA that wrote it last was committed before S_i
+// was.  At d = 128 both key halves accumulate into one O_i, so they agree on
+// every rescale through a named barrier; at d = 64 TMEM holds one accumulator
+// per key half, each half keeps its own maximum and sum, and the two are
+// merged once in the epilogue.
 //
-// Registers are re-balanced with setmaxnreg: 192 per softmax thread, 96 for
-// warps 8-11 and 32 for the idle warps 12-15 (256*192 + 128*96 + 128*32 =
-// 65536, the block's launch allocation of 512 threads x 128).
+// Registers are re-balanced with setmaxnreg: 160 per softmax thread, 128 for
+// warps 8-11 and 32 for the idle warps 12-15 (256*160 + 128*128 + 128*32 =
+// 61440 of the block's launch allocation of 512 threads x 128).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -59,7 +64,13 @@ constexpr int kWarpTMA = 9;
 constexpr uint32_t kTmemCols = 512;      // S0 | S1 | O0 | O1
 constexpr uint32_t kBoxBytes = 64 * 128 * 2;   // one TMA box: 64 columns x 128 rows bf16
 constexpr float kLn2 = 0.69314718055994530942f;
-constexpr float kRescaleThreshold = 8.0f;      // log2 units: rescale when max grows > 2^8
+// A half row (64 keys) whose P sum exceeds 2^15 has some P above 2^9: its
+// maximum has grown and the tile is redone against the new maximum.  Below
+// that P <= 2^15, harmless for bf16 P and the fp32 accumulators.
+constexpr float kRescaleSum = 32768.0f;
+// Running maximum of a key half that has seen no visible key yet: any visible
+// score then overflows the half's P sum to +inf, which takes the rescale path.
+constexpr float kMInit = -1.0e30f;
 
 // K/V ring depths per head dimension (shared memory: 2 query tiles + SK + SV
 // tiles of 128 x d bf16 must fit in 227 KB).
@@ -87,23 +98,28 @@ struct Cfg {
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = OFF_Q + QT * Q_BYTES;
   static constexpr uint32_t OFF_V = OFF_K + SK * KV_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_V + SV * KV_BYTES;
-  // q, kf[SK], ke[SK], vf[SV], ve[SV], s[QT], p[QT], o[QT], drain
-  static constexpr int NBAR = 1 + 2 * SK + 2 * SV + 3 * QT + 1;
+  // d = 64: the two key halves of a row keep separate maxima, sums and O
+  // accumulators (merged once at the end); d = 128 (no room in TMEM for that):
+  // the halves agree on every rescale and share one O accumulator.
+  static constexpr bool kIndep = (D == 64);
+  static constexpr int NPB = kIndep ? 2 : 1;        // P hand-off barriers per query tile
+  static constexpr uint32_t OFF_XCH = OFF_V + SV * KV_BYTES;   // float[2][QT][2][BM]
+  static constexpr uint32_t OFF_BAR = OFF_XCH + 2 * QT * 2 * BM * 4;
+  // q, kf[SK], ke[SK], vf[SV], ve[SV], s[QT], p[QT][NPB], o[QT], drain
+  static constexpr int NBAR = 1 + 2 * SK + 2 * SV + QT + QT * NPB + QT + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 32;   // tmem slot, abort flag, pair_abort[4]
   static constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;   // 1024-byte alignment slack
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
   static constexpr uint32_t TMEM_S = 0;               // S_i at column 128 * i
-  static constexpr uint32_t TMEM_O = QT * BN;         // O_i at column TMEM_O + D * i
-  static_assert(TMEM_O + QT * D <= kTmemCols, "tensor memory budget");
+  // O accumulators at TMEM_O + D * b: b = i (shared by both halves) or
+  // b = 2 i + h (one per key half h).
+  static constexpr uint32_t TMEM_O = QT * BN;
+  static_assert(TMEM_O + QT * NPB * D <= kTmemCols, "tensor memory budget");
 };
 
-__device__ __forceinline__ void setmaxnreg_inc192() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
-}
-__device__ __forceinline__ void setmaxnreg_dec96() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 96;" ::: "memory");
+__device__ __forceinline__ void setmaxnreg_inc160() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 160;" ::: "memory");
 }
 __device__ __forceinline__ void setmaxnreg_dec32() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 32;" ::: "memory");
@@ -111,15 +127,13 @@ __device__ __forceinline__ void setmaxnreg_dec32() {
 
 // exp2 of 32 consecutive scores of one row against the maximum m (-nm = m):
 // p = 2^(s * scale_log2 - m), packed as bf16 pairs into pk; adds the p to the
-// two fp32x2 partial sums rs2 and folds s * scale_log2 - m into the running
-// maxima mx (two independent 3-input max chains).
+// two fp32x2 partial sums rs2.
 __device__ __forceinline__ void exp_chunk(const uint32_t (&sr)[32], float2 sc2, float2 nm2,
-                                          uint32_t *pk, float2 (&rs2)[2], float (&mx)[2]) {
+                                          uint32_t *pk, float2 (&rs2)[2]) {
 #pragma unroll
   for (int c = 0; c < 16; ++c) {
     const float2 x = ffma2(make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])),
                            sc2, nm2);
-    mx[c & 1] = fmax3(mx[c & 1], x.x, x.y);
     const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
     rs2[c & 1] = fadd2(rs2[c & 1], p);
     pk[c] = pack_bf16x2(p.x, p.y);
@@ -174,12 +188,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto B_VE = [&](int s) { return bar0 + 8u * (1 + 2 * SK + SV + s); };
   constexpr int kB5 = 1 + 2 * SK + 2 * SV;
   auto B_S = [&](int i) { return bar0 + 8u * (kB5 + i); };            // S_i ready (MMA)
-  auto B_P = [&](int i) { return bar0 + 8u * (kB5 + QT + i); };       // P_i written (softmax)
-  auto B_O = [&](int i) { return bar0 + 8u * (kB5 + 2 * QT + i); };   // last P_i V_j done (MMA)
-  const uint32_t B_DRAIN = bar0 + 8u * (kB5 + 3 * QT);
-  static_assert(kB5 + 3 * QT + 1 == C::NBAR, "barrier count");
+  constexpr int NPB = C::NPB;
+  // P_i written by the softmax (per key half when the halves are independent)
+  auto B_P = [&](int i, int hh) { return bar0 + 8u * (kB5 + QT + i * NPB + (NPB > 1 ? hh : 0)); };
+  auto B_O = [&](int i) { return bar0 + 8u * (kB5 + QT + QT * NPB + i); };   // last P_i V_j done
+  const uint32_t B_DRAIN = bar0 + 8u * (kB5 + 2 * QT + QT * NPB);
+  static_assert(kB5 + 2 * QT + QT * NPB + 1 == C::NBAR, "barrier count");
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+  // Set by a softmax warp whose wait gave up, read by it and its partner warp
+  // after their shared barrier (so both take the same exit).
+  volatile int *pair_abort = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 16);
 
   if (threadIdx.x == 0) {
     mbar_init(B_Q, 1);
@@ -193,11 +212,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < QT; ++i) {
       mbar_init(B_S(i), 1);
-      mbar_init(B_P(i), BM);
+      for (int hh = 0; hh < NPB; ++hh) mbar_init(B_P(i, hh), 2 * BM / NPB);   // 256 threads, 2 per row
       mbar_init(B_O(i), 1);
     }
     mbar_init(B_DRAIN, 1);
     *abort_flag = 0;
+    for (int p = 0; p < 4; ++p) pair_abort[p] = 0;
     fence_mbar_init();
   }
   if (warp == kWarpMMA) {
@@ -215,139 +235,214 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (wg < QT) {
-    setmaxnreg_inc192();
+    setmaxnreg_inc160();
     // ------------------------------------------------------------ softmax
-    const int i = wg;                        // query tile
-    const int r = threadIdx.x - i * BM;      // row within the tile == TMEM lane
-    const int qrow = q0 + i * BM + r;
-    const int n_i = (i == 0) ? n0 : n1;
-    const int lim = CAUSAL ? min(qrow, N - 1) : N - 1;   // last visible key
-    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t s_addr = tmem + lane_addr + C::TMEM_S + i * BN;
-    const uint32_t o_addr = tmem + lane_addr + C::TMEM_O + i * D;
+    // Warps q and q + 4 share TMEM lanes 32q..32q+31 (rows 32q..32q+31 of
+    // both query tiles): warp q takes keys 0-63 of every K/V tile, warp q + 4
+    // keys 64-127, and both run through S_0, S_1, S_0, ... in the MMA's order.
+    // With one O accumulator per row (d = 128) the pair agrees through its own
+    // named barrier on each rescale (and on an abort); with one per key half
+    // (d = 64) the halves run independently.  Either way the pair combines its
+    // partial sums (and maxima) once at the end.
+    constexpr bool kIndep = C::kIndep;
+    const int h = wg;                        // key half
+    const int q = warp & 3;
+    const int r = q * 32 + lane;             // row within a tile == TMEM lane
+    const uint32_t pair_bar = 1 + q;
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    float *xch = reinterpret_cast<float *>(smem + C::OFF_XCH);   // [2][QT][2][BM]
     const float2 sc2 = make_float2(scale_log2, scale_log2);
-    // One pass over S_i: P = 2^(x - m_use) into pk, its row sum, and the row's
-    // maximum of x - m_use.  Keys 64-127 are read from TMEM while keys 0-63
-    // are exponentiated.
-    auto pass = [&](int kv0, float m_use, uint32_t (&pk)[BN / 2], float &rs, float &mx_out) {
+    int lim[QT];                             // last visible key of the row in tile i
+#pragma unroll
+    for (int i = 0; i < QT; ++i) lim[i] = CAUSAL ? min(q0 + i * BM + r, N - 1) : N - 1;
+    // O accumulator columns this thread rescales and, at the end, reads.
+    auto o_block = [&](int i) {
+      return tmem + lane_addr + C::TMEM_O + (kIndep ? (2 * i + h) * D : i * D + h * (D / 2));
+    };
+    // This thread's 64 scores of S_i: P = 2^(x - m_use) packed into pk and
+    // their sum.  Keys 32-63 are read from TMEM while keys 0-31 are
+    // exponentiated.
+    auto pass = [&](uint32_t s_addr, int k0, int lm, float m_use, uint32_t (&pk)[32], float &rs) {
       const float2 nm2 = make_float2(-m_use, -m_use);
       float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      float mx[2] = {-INFINITY, -INFINITY};
-      uint32_t a[32], b[32], c[32], d[32];
+      uint32_t a[32], b[32];
+      tmem_ld_32cols(s_addr, a);
+      tmem_ld_wait_regs(a);
+      tmem_ld_32cols(s_addr + 32, b);
+      mask_chunk(a, k0, lm);
+      exp_chunk(a, sc2, nm2, &pk[0], rs2);
+      __syncwarp();
+      tmem_ld_wait_regs(b);
+      mask_chunk(b, k0 + 32, lm);
+      exp_chunk(b, sc2, nm2, &pk[16], rs2);
+      rs = (rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y);
+    };
+    // Maximum of this thread's 64 (masked) raw scores of S_i.
+    auto half_max = [&](uint32_t s_addr, int k0, int lm) {
+      uint32_t a[32], b[32];
       tmem_ld_32cols(s_addr, a);
       tmem_ld_32cols(s_addr + 32, b);
       tmem_ld_wait_regs(a);
       reg_fence32(b);
-      tmem_ld_32cols(s_addr + 64, c);
-      tmem_ld_32cols(s_addr + 96, d);
-      mask_chunk(a, kv0, lim);
-      mask_chunk(b, kv0 + 32, lim);
-      exp_chunk(a, sc2, nm2, &pk[0], rs2, mx);
-      exp_chunk(b, sc2, nm2, &pk[16], rs2, mx);
-      __syncwarp();
-      tmem_ld_wait_regs(c);
-      reg_fence32(d);
-      mask_chunk(c, kv0 + 64, lim);
-      mask_chunk(d, kv0 + 96, lim);
-      exp_chunk(c, sc2, nm2, &pk[32], rs2, mx);
-      exp_chunk(d, sc2, nm2, &pk[48], rs2, mx);
-      rs = (rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y);
-      mx_out = fmaxf(mx[0], mx[1]);
-    };
-    float m = 0.f;                           // max used for the exponentials (base 2)
-    float l = 0.f;                           // running sum of exp2(x - m)
-    bool ok = true;
-    for (int j = 0; j < n_i; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(B_S(i), j & 1, status, abort_flag));
-      if (!ok) break;
-      tc_fence_after();
-      const int kv0 = j * BN;
-      if (j == 0) {
-        // First tile: its row maximum first (every row sees at least key 0).
-        uint32_t sr[4][32];
+      mask_chunk(a, k0, lm);
+      mask_chunk(b, k0 + 32, lm);
+      float ma = __uint_as_float(a[0]), mb = __uint_as_float(b[0]);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld_32cols(s_addr + c * 32, sr[c]);
-        tmem_ld_wait_regs(sr[0]);
-        reg_fence32(sr[1]);
-        reg_fence32(sr[2]);
-        reg_fence32(sr[3]);
-        float mq[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          mask_chunk(sr[q], kv0 + 32 * q, lim);
-          mq[q] = __uint_as_float(sr[q][0]);
-#pragma unroll
-          for (int c = 1; c + 1 < 32; c += 2)
-            mq[q] = fmax3(mq[q], __uint_as_float(sr[q][c]), __uint_as_float(sr[q][c + 1]));
-          mq[q] = fmaxf(mq[q], __uint_as_float(sr[q][31]));
-        }
-        __syncwarp();
-        m = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * scale_log2;
+      for (int c = 1; c + 1 < 32; c += 2) {
+        ma = fmax3(ma, __uint_as_float(a[c]), __uint_as_float(a[c + 1]));
+        mb = fmax3(mb, __uint_as_float(b[c]), __uint_as_float(b[c + 1]));
       }
-      uint32_t pk[BN / 2];
-      float rs, mx;
-      pass(kv0, m, pk, rs, mx);
-      float alpha = 1.f;
-      if (__any_sync(0xffffffffu, mx > kRescaleThreshold)) {
-        // Some row's maximum grew by more than 2^8: redo the tile with the new
-        // maximum and scale those rows' O_i by 2^(m_old - m_new).
-        const float m_new = (mx > kRescaleThreshold) ? m + mx : m;
-        alpha = ex2_approx(m - m_new);
-        m = m_new;
-        pass(kv0, m, pk, rs, mx);
-        if (j > 0) {
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld_32cols(o_addr + c * 32, o);
-            tmem_ld_wait_regs(o);
+      __syncwarp();
+      return fmaxf(fmaxf(ma, __uint_as_float(a[31])), fmaxf(mb, __uint_as_float(b[31])));
+    };
+    float m[QT], l[QT];                      // per tile: max used for P (base 2), partial row sum
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st_32cols(o_addr + c * 32, o);
+    for (int i = 0; i < QT; ++i) {
+      m[i] = kIndep ? kMInit : 0.f;
+      l[i] = 0.f;
+    }
+    bool ok = true;
+    for (int j = 0; ok && j < n1; ++j) {
+#pragma unroll
+      for (int i = 0; i < QT; ++i) {
+        if (j >= (i == 0 ? n0 : n1)) continue;
+        // With a shared accumulator, a warp whose wait gave up still takes
+        // part in the pair's barriers below; the vote after the pass then
+        // ends the loop for both.
+        const bool okw = __all_sync(0xffffffffu, mbar_wait(B_S(i), j & 1, status, abort_flag));
+        if (kIndep && !okw) {
+          ok = false;
+          break;
+        }
+        if (okw) tc_fence_after();
+        const uint32_t s_addr = tmem + lane_addr + C::TMEM_S + i * BN + h * 64;
+        const int k0 = j * BN + h * 64;
+        float *xi = xch + i * 2 * BM;
+        if (j == 0) {
+          // First tile: the maximum first (of the half, or of the whole row,
+          // which always contains key 0).
+          if (kIndep) {
+            const float hm = half_max(s_addr, k0, lim[i]);
+            m[i] = (hm == -INFINITY) ? kMInit : hm * scale_log2;
+          } else {
+            xi[h * BM + r] = okw ? half_max(s_addr, k0, lim[i]) : 0.f;
+            named_bar_sync(pair_bar, 64);
+            m[i] = fmaxf(xi[r], xi[BM + r]) * scale_log2;
           }
         }
-      }
-      l = l * alpha + rs;
-      // P_i (bf16, keys packed in pairs) over the first 64 columns of S_i.
-      tmem_st_32cols(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      tmem_st_32cols(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(B_P(i));
-    }
-    // Epilogue: O_i / l -> bf16 rows, LSE.
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(B_O(i), 0, status, abort_flag));
-    if (ok) {
-      tc_fence_after();
-      const float inv_l = 1.f / l;
-      __nv_bfloat16 *orow = O + (static_cast<size_t>(bh) * N + qrow) * D;
+        uint32_t pk[32];
+        float rs = 0.f;
+        if (okw) pass(s_addr, k0, lim[i], m[i], pk, rs);
+        else pair_abort[q] = 1;
+        // rs > 2^15 (or not finite) means some P exceeded 2^9: the maximum
+        // grew, and the tile is redone with the new one (by both halves when
+        // they share the accumulator).
+        bool redo;
+        if (kIndep) {
+          redo = __any_sync(0xffffffffu, !(rs <= kRescaleSum));
+        } else {
+          redo = named_bar_any(pair_bar, 64, !okw || !(rs <= kRescaleSum));
+          if (redo && pair_abort[q]) {
+            ok = false;
+            break;
+          }
+        }
+        float alpha = 1.f;
+        if (redo) {
+          float tmax;
+          if (kIndep) {
+            tmax = half_max(s_addr, k0, lim[i]);
+          } else {
+            xi[h * BM + r] = half_max(s_addr, k0, lim[i]);
+            named_bar_sync(pair_bar, 64);
+            tmax = fmaxf(xi[r], xi[BM + r]);
+          }
+          const float m_new = fmaxf(m[i], tmax * scale_log2);
+          alpha = ex2_approx(m[i] - m_new);
+          m[i] = m_new;
+          pass(s_addr, k0, lim[i], m[i], pk, rs);
+          if (j > 0) {
+            // This thread's accumulator columns scaled by 2^(m_old - m_new).
+            const uint32_t o_addr = o_block(i);
+#pragma unroll 1
+            for (int c = 0; c < (kIndep ? D / 32 : D / 64); ++c) {
+              uint32_t o[32];
+              tmem_ld_32cols(o_addr + c * 32, o);
+              tmem_ld_wait_regs(o);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              tmem_st_32cols(o_addr + c * 32, o);
+            }
+          }
+        }
+        l[i] = l[i] * alpha + rs;
+        // P for keys 64h .. 64h+63 (bf16 pairs) over the first 32 of this
+        // thread's own S columns, which it has already read.
+        tmem_st_32cols(s_addr, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(B_P(i, h));
+      }
+    }
+    // Epilogue per tile: each warp writes its half of the columns of O_i and
+    // the warp of the low half the LSE.  Independent halves are merged with
+    // weights 2^(m_h - max(m_0, m_1)).
+#pragma unroll
+    for (int i = 0; i < QT; ++i) {
+      const bool okw = ok && __all_sync(0xffffffffu, mbar_wait(B_O(i), 0, status, abort_flag));
+      float *xm = xch + i * 2 * BM;                 // maxima (independent halves)
+      float *xl = xch + (QT + i) * 2 * BM;          // partial sums
+      if (kIndep) xm[h * BM + r] = m[i];   // (the shared-max exchange above uses xm otherwise)
+      xl[h * BM + r] = l[i];
+      if (named_bar_any(pair_bar, 64, !okw)) continue;
+      tc_fence_after();
+      float mrow = m[i], w0 = 1.f, w1 = 1.f;
+      if (kIndep) {
+        mrow = fmaxf(xm[r], xm[BM + r]);
+        w0 = ex2_approx(xm[r] - mrow);
+        w1 = ex2_approx(xm[BM + r] - mrow);
+      }
+      const float lt = w0 * xl[r] + w1 * xl[BM + r];
+      const float inv_l = 1.f / lt;
+      const float a0 = w0 * inv_l, a1 = w1 * inv_l;
+      const int qrow = q0 + i * BM + r;
+      __nv_bfloat16 *orow = O + (static_cast<size_t>(bh) * N + qrow) * D + h * (D / 2);
+      const uint32_t o_addr = tmem + lane_addr + C::TMEM_O + (kIndep ? 2 * i * D : i * D) + h * (D / 2);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t o[32], o1[32];
         tmem_ld_32cols(o_addr + c * 32, o);
+        if (kIndep) tmem_ld_32cols(o_addr + D + c * 32, o1);
         tmem_ld_wait_regs(o);
+        if (kIndep) {
+          reg_fence32(o1);
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            o[e] = __float_as_uint(__uint_as_float(o[e]) * a0 + __uint_as_float(o1[e]) * a1);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * inv_l);
+        }
         if (qrow < N) {
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              w[e] = pack_bf16x2(__uint_as_float(o[8 * v + 2 * e]) * inv_l,
-                                 __uint_as_float(o[8 * v + 2 * e + 1]) * inv_l);
+              w[e] = pack_bf16x2(__uint_as_float(o[8 * v + 2 * e]), __uint_as_float(o[8 * v + 2 * e + 1]));
             st_global_v4(orow + c * 32 + v * 8, w[0], w[1], w[2], w[3]);
           }
         }
         __syncwarp();
       }
-      if (qrow < N) {
+      if (h == 0 && qrow < N) {
         float lg;
-        asm("lg2.approx.f32 %0, %1;" : "=f"(lg) : "f"(l));
-        LSE[static_cast<size_t>(bh) * N + qrow] = (m + lg) * kLn2;
+        asm("lg2.approx.f32 %0, %1;" : "=f"(lg) : "f"(lt));
+        LSE[static_cast<size_t>(bh) * N + qrow] = (mrow + lg) * kLn2;
       }
     }
     tc_fence_before();
   } else if (wg == QT) {
-    setmaxnreg_dec96();
     // Warps 8 and 9 run their schedules warp-uniformly (every lane waits on the
     // barriers) and one elected lane issues the TMA copies / MMAs, so addresses
     // and descriptors stay in the warp-uniform datapath.
@@ -413,6 +508,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q_lo = static_cast<uint32_t>(dQ);
       const uint32_t k_lo = static_cast<uint32_t>(dK);
       const uint32_t v_lo = static_cast<uint32_t>(dV);
+      auto wait_all = [&](uint32_t bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, abort_flag));
+      };
       // S_i = Q_i K^T: both operands K-major (head dim contiguous), 128-B swizzle.
       auto issue_qk = [&](int i, int sk) {
         const uint32_t a0 = q_lo + ((i * C::Q_BYTES) >> 4);
@@ -424,17 +522,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                          kk > 0 ? 1u : 0u);
         }
       };
-      // O_i += P_i V: P_i from TMEM (8 columns = 16 keys per step); V is MN-major
+      // O += P_i V: P_i from TMEM (8 columns = 16 keys per step; keys 0-63 in
+      // columns 0-31 of S_i, keys 64-127 in columns 64-95); V is MN-major
       // (head dim contiguous), 64-column blocks kBoxBytes apart, 8-key groups 1024 B apart.
-      auto issue_pv = [&](int i, int sv, bool acc) {
+      // Key steps kb..ke-1 into the accumulator at column o_col.
+      auto issue_pv = [&](int i, int sv, bool acc, int kb, int ke, uint32_t o_col) {
         const uint32_t b0 = v_lo + ((sv * C::KV_BYTES) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_bf16_ts_lo(tmem + C::TMEM_O + i * D, tmem + C::TMEM_S + i * BN + kk * 8,
-                         b0 + ((kk * 16 * 128) >> 4), hi, kIdescPV, (acc || kk > 0) ? 1u : 0u);
+        for (int kk = kb; kk < ke; ++kk)
+          mma_bf16_ts_lo(tmem + o_col, tmem + C::TMEM_S + i * BN + (kk >> 2) * 64 + (kk & 3) * 8,
+                         b0 + ((kk * 16 * 128) >> 4), hi, kIdescPV, (acc || kk > kb) ? 1u : 0u);
       };
-      auto wait_all = [&](uint32_t bar, uint32_t parity) {
-        return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, abort_flag));
+      // P_i V_j: one run over all 128 keys into O_i, or (independent halves)
+      // keys 0-63 into O_i^0 as soon as that half's P is in, then keys 64-127
+      // into O_i^1.
+      auto pv = [&](int i, int sv, int j) {
+        if constexpr (C::kIndep) {
+          if (!wait_all(B_P(i, 0), j & 1)) return false;
+          tc_fence_after();
+          if (leader) issue_pv(i, sv, j > 0, 0, BN / 32, C::TMEM_O + 2 * i * D);
+          __syncwarp();
+          if (!wait_all(B_P(i, 1), j & 1)) return false;
+          tc_fence_after();
+          if (leader) issue_pv(i, sv, j > 0, BN / 32, BN / 16, C::TMEM_O + (2 * i + 1) * D);
+          __syncwarp();
+        } else {
+          if (!wait_all(B_P(i, 0), j & 1)) return false;
+          tc_fence_after();
+          if (leader) issue_pv(i, sv, j > 0, 0, BN / 16, C::TMEM_O + i * D);
+          __syncwarp();
+        }
+        return true;
       };
       bool ok = wait_all(B_Q, 0) && wait_all(B_KF(0), 0);
       if (ok) {
@@ -459,10 +577,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = wait_all(B_VF(sv), (j / SV) & 1))) break;
         if (more && !(ok = wait_all(B_KF(sk1), ((j + 1) / SK) & 1))) break;
         if (j < n0) {
-          if (!(ok = wait_all(B_P(0), j & 1))) break;
-          tc_fence_after();
+          if (!(ok = pv(0, sv, j))) break;
           if (leader) {
-            issue_pv(0, sv, j > 0);
             if (j + 1 == n0) mma_commit(B_O(0));
             if (j + 1 < n0) {
               issue_qk(0, sk1);   // overwrites S_0/P_0 after the P_0 V_j MMAs above read it
@@ -471,10 +587,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           __syncwarp();
         }
-        if (!(ok = wait_all(B_P(1), j & 1))) break;
-        tc_fence_after();
+        if (!(ok = pv(1, sv, j))) break;
         if (leader) {
-          issue_pv(1, sv, j > 0);
           if (j + 1 == n1) mma_commit(B_O(1));
           if (j + SV < n1) mma_commit(B_VE(sv));
           if (more) {
