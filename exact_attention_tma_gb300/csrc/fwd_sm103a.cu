@@ -153,7 +153,8 @@ __device__ __forceinline__ void mask_chunk(uint32_t (&sr)[32], int first_key, in
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, __nv_bfloat16 *__restrict__ O,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    __nv_bfloat16 *__restrict__ O,
                     float *__restrict__ LSE, int N, int BH, int n_blk, float scale_log2,
                     unsigned *status) {
   using C = Cfg<D>;
@@ -228,6 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmO);
   }
   tc_fence_before();
   __syncthreads();
@@ -384,9 +386,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(B_P(i, h));
       }
     }
-    // Epilogue per tile: each warp writes its half of the columns of O_i and
-    // the warp of the low half the LSE.  Independent halves are merged with
-    // weights 2^(m_h - max(m_0, m_1)).
+    // Epilogue per tile: each warp stages its half of the columns of O_i as
+    // bf16 in the (no longer needed) Q_i buffer, in the 128-byte-swizzled box
+    // layout of the O tensor map, and one thread stores the tile with TMA
+    // (rows past N are dropped by the tensor map); the warp of the low half
+    // writes the LSE.  Independent halves are merged with weights
+    // 2^(m_h - max(m_0, m_1)).  Every MMA reading Q_i finished before the last
+    // P_i V_j, whose completion the epilogue waits for.
+    constexpr uint32_t kEpiBar = 5;          // named barrier of all 256 softmax threads
 #pragma unroll
     for (int i = 0; i < QT; ++i) {
       const bool okw = ok && __all_sync(0xffffffffu, mbar_wait(B_O(i), 0, status, abort_flag));
@@ -394,7 +401,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       float *xl = xch + (QT + i) * 2 * BM;          // partial sums
       if (kIndep) xm[h * BM + r] = m[i];   // (the shared-max exchange above uses xm otherwise)
       xl[h * BM + r] = l[i];
-      if (named_bar_any(pair_bar, 64, !okw)) continue;
+      if (named_bar_any(kEpiBar, 2 * BM, !okw)) {
+        ok = false;
+        continue;
+      }
       tc_fence_after();
       float mrow = m[i], w0 = 1.f, w1 = 1.f;
       if (kIndep) {
@@ -406,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv_l = 1.f / lt;
       const float a0 = w0 * inv_l, a1 = w1 * inv_l;
       const int qrow = q0 + i * BM + r;
-      __nv_bfloat16 *orow = O + (static_cast<size_t>(bh) * N + qrow) * D + h * (D / 2);
+      const uint32_t stage = sb + C::OFF_Q + i * C::Q_BYTES + static_cast<uint32_t>(r) * 128;
       const uint32_t o_addr = tmem + lane_addr + C::TMEM_O + (kIndep ? 2 * i * D : i * D) + h * (D / 2);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
@@ -423,17 +433,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * inv_l);
         }
-        if (qrow < N) {
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint32_t w[4];
+        for (int v = 0; v < 4; ++v) {
+          uint32_t w[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              w[e] = pack_bf16x2(__uint_as_float(o[8 * v + 2 * e]), __uint_as_float(o[8 * v + 2 * e + 1]));
-            st_global_v4(orow + c * 32 + v * 8, w[0], w[1], w[2], w[3]);
-          }
+          for (int e = 0; e < 4; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(o[8 * v + 2 * e]), __uint_as_float(o[8 * v + 2 * e + 1]));
+          const int col = h * (D / 2) + c * 32 + v * 8;   // first of these 8 columns
+          const uint32_t chunk = static_cast<uint32_t>((col & 63) >> 3) ^ static_cast<uint32_t>(r & 7);
+          st_shared_v4(stage + (col >> 6) * kBoxBytes + (chunk << 4), w[0], w[1], w[2], w[3]);
         }
         __syncwarp();
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(kEpiBar, 2 * BM);
+      if (threadIdx.x == 0) {
+#pragma unroll
+        for (int kb = 0; kb < C::KB; ++kb)
+          tma_store_3d(&tmO, kb * 64, q0 + i * BM, bh, sb + C::OFF_Q + i * C::Q_BYTES + kb * kBoxBytes);
+        bulk_commit_group();
       }
       if (h == 0 && qrow < N) {
         float lg;
@@ -441,6 +459,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         LSE[static_cast<size_t>(bh) * N + qrow] = (mrow + lg) * kLn2;
       }
     }
+    // The staged tiles must have been read before the CTA's shared memory goes.
+    if (threadIdx.x == 0) bulk_wait_group_read0();
     tc_fence_before();
   } else if (wg == QT) {
     // Warps 8 and 9 run their schedules warp-uniformly (every lane waits on the
@@ -649,7 +669,7 @@ static bool make_map(CUtensorMap *m, const void *base, int BH, int N, int d) {
 
 template <int D, bool CAUSAL>
 static cudaError_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                            void *O, float *LSE, int BH, int N, float scale_log2,
+                            const CUtensorMap &mo, void *O, float *LSE, int BH, int N, float scale_log2,
                             unsigned *status, cudaStream_t stream) {
   using C = Cfg<D>;
   auto kern = attn_fwd_kernel<D, CAUSAL>;
@@ -667,7 +687,7 @@ static cudaError_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const 
   const int n_blk = (N + QT * BM - 1) / (QT * BM);
   const long long grid = static_cast<long long>(BH) * n_blk;
   kern<<<static_cast<unsigned>(grid), kThreads, C::SMEM_ALLOC, stream>>>(
-      mq, mk, mv, static_cast<__nv_bfloat16 *>(O), LSE, N, BH, n_blk, scale_log2, status);
+      mq, mk, mv, mo, static_cast<__nv_bfloat16 *>(O), LSE, N, BH, n_blk, scale_log2, status);
   return cudaGetLastError();
 }
 
@@ -678,15 +698,16 @@ cudaError_t launch_fwd(const void *Q, const void *K, const void *V, void *O, flo
                        cudaStream_t stream) {
   using namespace fwd;
   const int BH = B * H;
-  CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, Q, BH, N, d) || !make_map(&mk, K, BH, N, d) || !make_map(&mv, V, BH, N, d))
+  CUtensorMap mq, mk, mv, mo;
+  if (!make_map(&mq, Q, BH, N, d) || !make_map(&mk, K, BH, N, d) || !make_map(&mv, V, BH, N, d) ||
+      !make_map(&mo, O, BH, N, d))
     return cudaErrorInvalidValue;
   const float scale_log2 = scale * 1.44269504088896340736f;
   if (d == 128)
-    return causal ? launch_t<128, true>(mq, mk, mv, O, LSE, BH, N, scale_log2, status, stream)
-                  : launch_t<128, false>(mq, mk, mv, O, LSE, BH, N, scale_log2, status, stream);
-  return causal ? launch_t<64, true>(mq, mk, mv, O, LSE, BH, N, scale_log2, status, stream)
-                : launch_t<64, false>(mq, mk, mv, O, LSE, BH, N, scale_log2, status, stream);
+    return causal ? launch_t<128, true>(mq, mk, mv, mo, O, LSE, BH, N, scale_log2, status, stream)
+                  : launch_t<128, false>(mq, mk, mv, mo, O, LSE, BH, N, scale_log2, status, stream);
+  return causal ? launch_t<64, true>(mq, mk, mv, mo, O, LSE, BH, N, scale_log2, status, stream)
+                : launch_t<64, false>(mq, mk, mv, mo, O, LSE, BH, N, scale_log2, status, stream);
 }
 
 }  // namespace ea
