@@ -105,8 +105,8 @@ struct Cfg {
   static constexpr int NPB = kIndep ? 2 : 1;        // P hand-off barriers per query tile
   static constexpr uint32_t OFF_XCH = OFF_V + SV * KV_BYTES;   // float[2][QT][2][BM]
   static constexpr uint32_t OFF_BAR = OFF_XCH + 2 * QT * 2 * BM * 4;
-  // q, kf[SK], ke[SK], vf[SV], ve[SV], s[QT], p[QT][NPB], o[QT], drain
-  static constexpr int NBAR = 1 + 2 * SK + 2 * SV + QT + QT * NPB + QT + 1;
+  // q[QT], kf[SK], ke[SK], vf[SV], ve[SV], s[QT], p[QT][NPB], o[QT], drain
+  static constexpr int NBAR = QT + 2 * SK + 2 * SV + QT + QT * NPB + QT + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 32;   // tmem slot, abort flag, pair_abort[4]
   static constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;   // 1024-byte alignment slack
@@ -182,12 +182,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n1 = CAUSAL ? min(QT * blk + 2, n_kv_total) : n_kv_total;
 
   const uint32_t bar0 = sb + C::OFF_BAR;
-  const uint32_t B_Q = bar0;
-  auto B_KF = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto B_KE = [&](int s) { return bar0 + 8u * (1 + SK + s); };
-  auto B_VF = [&](int s) { return bar0 + 8u * (1 + 2 * SK + s); };
-  auto B_VE = [&](int s) { return bar0 + 8u * (1 + 2 * SK + SV + s); };
-  constexpr int kB5 = 1 + 2 * SK + 2 * SV;
+  auto B_Q = [&](int i) { return bar0 + 8u * i; };                    // Q_i loaded
+  auto B_KF = [&](int s) { return bar0 + 8u * (QT + s); };
+  auto B_KE = [&](int s) { return bar0 + 8u * (QT + SK + s); };
+  auto B_VF = [&](int s) { return bar0 + 8u * (QT + 2 * SK + s); };
+  auto B_VE = [&](int s) { return bar0 + 8u * (QT + 2 * SK + SV + s); };
+  constexpr int kB5 = QT + 2 * SK + 2 * SV;
   auto B_S = [&](int i) { return bar0 + 8u * (kB5 + i); };            // S_i ready (MMA)
   constexpr int NPB = C::NPB;
   // P_i written by the softmax (per key half when the halves are independent)
@@ -201,8 +201,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // after their shared barrier (so both take the same exit).
   volatile int *pair_abort = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 16);
 
-  if (threadIdx.x == 0) {
-    mbar_init(B_Q, 1);
+  // One thread of the TMA warp sets up the barriers and at once starts the
+  // first loads, in the order the first MMAs need them (Q_0 and K_0, then Q_1
+  // and V_0), while the MMA warp allocates TMEM.
+  if (threadIdx.x == kWarpTMA * 32) {
+    for (int i = 0; i < QT; ++i) mbar_init(B_Q(i), 1);
     for (int s = 0; s < SK; ++s) {
       mbar_init(B_KF(s), 1);
       mbar_init(B_KE(s), 1);
@@ -220,16 +223,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     for (int p = 0; p < 4; ++p) pair_abort[p] = 0;
     fence_mbar_init();
-  }
-  if (warp == kWarpMMA) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish();
-  }
-  if (warp == kWarpTMA && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmO);
+    auto load_q = [&](int i) {
+      mbar_arrive_expect_tx(B_Q(i), C::Q_BYTES);
+      for (int kb = 0; kb < C::KB; ++kb)
+        tma_load_3d(sb + C::OFF_Q + i * C::Q_BYTES + kb * kBoxBytes, &tmQ, kb * 64, q0 + i * BM,
+                    bh, B_Q(i));
+    };
+    load_q(0);
+    mbar_arrive_expect_tx(B_KF(0), C::KV_BYTES);
+    for (int kb = 0; kb < C::KB; ++kb)
+      tma_load_3d(sb + C::OFF_K + kb * kBoxBytes, &tmK, kb * 64, 0, bh, B_KF(0));
+    for (int i = 1; i < QT; ++i) load_q(i);
+    mbar_arrive_expect_tx(B_VF(0), C::KV_BYTES);
+    for (int kb = 0; kb < C::KB; ++kb)
+      tma_load_3d(sb + C::OFF_V + kb * kBoxBytes, &tmV, kb * 64, 0, bh, B_VF(0));
+  }
+  if (warp == kWarpMMA) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
@@ -468,18 +483,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // and descriptors stay in the warp-uniform datapath.
     if (warp == kWarpTMA) {
       // ------------------------------------------------------ TMA producer
+      // (Q and the first K/V tile were issued before the CTA-wide barrier.)
       const bool leader = elect_one();
-      if (leader) {
-        mbar_arrive_expect_tx(B_Q, QT * C::Q_BYTES);
-#pragma unroll
-        for (int i = 0; i < QT; ++i)
-#pragma unroll
-          for (int kb = 0; kb < C::KB; ++kb)
-            tma_load_3d(sb + C::OFF_Q + i * C::Q_BYTES + kb * kBoxBytes, &tmQ, kb * 64,
-                        q0 + i * BM, bh, B_Q);
-      }
-      int issued_k = 0, issued_v = 0;
-      for (int j = 0; j < n1; ++j) {
+      int issued_k = 1, issued_v = 1;
+      for (int j = 1; j < n1; ++j) {
         const int sk = j % SK;
         if (!__all_sync(0xffffffffu, mbar_wait(B_KE(sk), ((j / SK) & 1) ^ 1u, status, abort_flag)))
           break;
@@ -505,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (leader && *abort_flag) {
         // Let every copy this warp started land before the CTA exits.
-        mbar_wait_drain(B_Q, 0, 100000000ull);
+        for (int i = 0; i < QT; ++i) mbar_wait_drain(B_Q(i), 0, 100000000ull);
         for (int s = 0; s < SK && s < issued_k; ++s)
           mbar_wait_drain(B_KF(s), (((issued_k - 1 - s) / SK)) & 1, 100000000ull);
         for (int s = 0; s < SV && s < issued_v; ++s)
@@ -574,12 +581,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return true;
       };
-      bool ok = wait_all(B_Q, 0) && wait_all(B_KF(0), 0);
+      bool ok = wait_all(B_Q(0), 0) && wait_all(B_KF(0), 0);
       if (ok) {
         tc_fence_after();
         if (leader) {
           issue_qk(0, 0);
           mma_commit(B_S(0));
+        }
+        __syncwarp();
+      }
+      ok = ok && wait_all(B_Q(1), 0);
+      if (ok) {
+        tc_fence_after();
+        if (leader) {
           issue_qk(1, 0);
           mma_commit(B_S(1));
           if (SK < n1) mma_commit(B_KE(0));
