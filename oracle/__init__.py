@@ -202,6 +202,77 @@ def lse_combine(O_s, lse_s):
     return O, lse[0]
 
 
+def kv_head_of(h: int, H: int, H_kv: int) -> int:
+    """K/V head that query head h reads under grouped-query attention.
+
+    "Why Fast GPUs Still Wait for Memory", section "Attention III · KV cache,
+    GQA, MLA": h query heads share h_kv key/value heads with group size
+    g = h / h_kv (MQA is g = h).  Reading: the groups are contiguous, so query
+    head h uses K/V head floor(h / g).
+    """
+    if H_kv < 1 or H % H_kv != 0 or not 0 <= h < H:
+        raise ValueError("need 1 <= H_kv, H % H_kv == 0 and 0 <= h < H")
+    return h // (H // H_kv)
+
+
+def attention_gqa(Q, K, V, scale: float, causal: bool, rows=None, heads=None,
+                  threads: int | None = None):
+    """Grouped-query forward: Q (B, H, N, d), K/V (B, H_kv, N, d).
+
+    Every (b, h) is one call of the per-head definition with K/V head
+    ``kv_head_of(h)``.  ``heads`` optionally lists flat (b * H + h) indices.
+    Returns O (B, H, R, d), LSE (B, H, R), or (len(heads), R, d) / (len(heads), R).
+    """
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    B, H, N, d = Q.shape
+    H_kv = K.shape[1]
+    hs = list(range(B * H)) if heads is None else list(heads)
+    R = N if rows is None else len(rows)
+    O = np.empty((len(hs), R, d), np.float64)
+    LSE = np.empty((len(hs), R), np.float64)
+
+    def one(t):
+        b, h = divmod(hs[t], H)
+        kh = kv_head_of(h, H, H_kv)
+        O[t], LSE[t] = attention_head(Q[b, h], K[b, kh], V[b, kh], scale, causal, rows)
+
+    _run(one, len(hs), threads)
+    if heads is None:
+        return O.reshape(B, H, R, d), LSE.reshape(B, H, R)
+    return O, LSE
+
+
+def decode_gqa(q, K, V, scale: float, heads=None, threads: int | None = None):
+    """Grouped-query decode: q (B, H, d), K/V (B, H_kv, L, d).
+
+    Returns O (B, H, d), LSE (B, H), or per listed flat head.
+    """
+    lib = _load()
+    q, K, V = _f64(q), _f64(K), _f64(V)
+    B, H, d = q.shape
+    H_kv, L = K.shape[1], K.shape[2]
+    hs = list(range(B * H)) if heads is None else list(heads)
+    O = np.empty((len(hs), d), np.float64)
+    LSE = np.empty((len(hs),), np.float64)
+
+    def one(t):
+        b, h = divmod(hs[t], H)
+        kh = kv_head_of(h, H, H_kv)
+        Kh, Vh = np.ascontiguousarray(K[b, kh]), np.ascontiguousarray(V[b, kh])
+        qh = np.ascontiguousarray(q[b, h])
+        o = np.empty((d,), np.float64)
+        lse = np.empty((1,), np.float64)
+        rc = lib.oracle_decode(_ptr(qh), _ptr(Kh), _ptr(Vh), L, d, float(scale), _ptr(o),
+                               _ptr(lse))
+        _check(rc, "oracle_decode")
+        O[t], LSE[t] = o, lse[0]
+
+    _run(one, len(hs), threads)
+    if heads is None:
+        return O.reshape(B, H, d), LSE.reshape(B, H)
+    return O, LSE
+
+
 def _run(fn, n: int, threads: int | None) -> None:
     if n == 0:
         return

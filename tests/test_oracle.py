@@ -241,3 +241,56 @@ def test_bad_arguments_are_rejected():
     with pytest.raises(RuntimeError):
         oracle.attention_head(np.ones((2, 2)), np.ones((2, 2)), np.ones((2, 2)), 1.0,
                               False, rows=[5])
+
+
+# ---------------------------------------------------------------- grouped heads
+# "Why Fast GPUs Still Wait for Memory", section "Attention III · KV cache, GQA,
+# MLA": h query heads share h_kv K/V heads, group size g = h / h_kv.  Reading:
+# contiguous groups, query head h -> K/V head floor(h / g).
+
+def test_kv_head_mapping_contiguous_groups():
+    assert [oracle.kv_head_of(h, 8, 2) for h in range(8)] == [0, 0, 0, 0, 1, 1, 1, 1]
+    assert [oracle.kv_head_of(h, 4, 4) for h in range(4)] == [0, 1, 2, 3]
+    assert [oracle.kv_head_of(h, 6, 1) for h in range(6)] == [0] * 6   # MQA
+    with pytest.raises(ValueError):
+        oracle.kv_head_of(0, 6, 4)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_constant_values_per_kv_head(causal):
+    # Each K/V head holds one constant value row, so every query head must
+    # return exactly its group's value: a mapping mistake (h % h_kv, say)
+    # would hand heads 1 and 2 the wrong constant.
+    rng = np.random.default_rng(11)
+    B, H, H_kv, N, d = 2, 4, 2, 6, 3
+    Q = rng.standard_normal((B, H, N, d))
+    K = rng.standard_normal((B, H_kv, N, d))
+    vals = np.array([[1.0, -2.0, 0.5], [3.0, 0.25, -1.0]])
+    V = np.empty((B, H_kv, N, d))
+    for b in range(B):
+        for kh in range(H_kv):
+            V[b, kh] = vals[kh] + 10.0 * b
+    O, LSE = oracle.attention_gqa(Q, K, V, 0.7, causal)
+    for b in range(B):
+        for h in range(H):
+            np.testing.assert_allclose(O[b, h], np.tile(vals[h // 2] + 10.0 * b, (N, 1)),
+                                       rtol=0, atol=1e-12)
+    q = rng.standard_normal((B, H, d))
+    Od, _ = oracle.decode_gqa(q, K, V, 0.7)
+    for b in range(B):
+        for h in range(H):
+            np.testing.assert_allclose(Od[b, h], vals[h // 2] + 10.0 * b, rtol=0, atol=1e-12)
+
+
+def test_gqa_with_one_group_per_head_is_mha():
+    rng = np.random.default_rng(12)
+    Q, K, V = (rng.standard_normal((2, 3, 5, 4)) for _ in range(3))
+    O, LSE = oracle.attention_gqa(Q, K, V, 0.5, True)
+    O2, LSE2 = oracle.attention(Q, K, V, 0.5, True)
+    np.testing.assert_array_equal(O, O2)
+    np.testing.assert_array_equal(LSE, LSE2)
+    q = rng.standard_normal((2, 3, 4))
+    Od, Ld = oracle.decode_gqa(q, K, V, 0.5)
+    Od2, Ld2 = oracle.decode(q, K, V, 0.5)
+    np.testing.assert_array_equal(Od, Od2)
+    np.testing.assert_array_equal(Ld, Ld2)
