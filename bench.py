@@ -46,17 +46,19 @@ WORKLOAD = ("causal fwd B4 H16 N2048 d128 + decode B16 H32 L8192 d128 (32 KV spl
 
 # ------------------------------------------------------------------ model
 def fwd_work(w):
-    """Algorithmic flops and compulsory HBM bytes of one forward call."""
+    """Algorithmic flops and compulsory HBM bytes of one forward call (K and V
+    have H_kv heads: grouped-query attention reads each K/V head once)."""
     flops = 4.0 * w.B * w.H * w.N * w.N * w.d * (0.5 if w.causal else 1.0)
-    elems = w.B * w.H * w.N * w.d
-    nbytes = 3 * elems * 2 + elems * 2 + w.B * w.H * w.N * 4   # read Q,K,V; write O, LSE
+    q_elems = w.B * w.H * w.N * w.d
+    kv_elems = w.B * w.H_kv * w.N * w.d
+    nbytes = 2 * q_elems * 2 + 2 * kv_elems * 2 + w.B * w.H * w.N * 4   # Q, O; K, V; LSE
     return flops, float(nbytes)
 
 
 def dec_work(w):
     """Algorithmic flops and compulsory HBM bytes of one decode call."""
     flops = 4.0 * w.B * w.H * w.N * w.d
-    nbytes = 2 * w.B * w.H * w.N * w.d * 2 + 2 * w.B * w.H * w.d * 2   # K, V; q, O
+    nbytes = 2 * w.B * w.H_kv * w.N * w.d * 2 + 2 * w.B * w.H * w.d * 2   # K, V; q, O
     return flops, float(nbytes)
 
 
@@ -456,17 +458,21 @@ def per_config(ea, peaks, dev, stream, reps=10):
 
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     out = {}
-    for name in ("causal_fwd", "noncausal_fwd", "long_causal_fwd", "decode"):
+    for name in ("causal_fwd", "noncausal_fwd", "long_causal_fwd", "decode", "gqa_fwd",
+                 "gqa_decode"):
         w = WORKLOADS[name]
         ins = workload_inputs(w, dev)
+        gqa = w.H_kv != w.H
         if w.kind == "fwd":
             o = torch.empty_like(ins[0])
             lse = torch.empty(ins[0].shape[:3], dtype=torch.float32, device=dev)
-            call = lambda: ea.attn_fwd(*ins, o, lse, w.causal, w.scale, stream)  # noqa: E731
+            fn = ea.attn_fwd_gqa if gqa else ea.attn_fwd
+            call = lambda: fn(*ins, o, lse, w.causal, w.scale, stream)  # noqa: E731
             flops, nbytes = fwd_work(w)
         else:
             o = torch.empty_like(ins[0])
-            call = lambda: ea.attn_decode(*ins, o, w.scale, stream)  # noqa: E731
+            fn = ea.attn_decode_gqa if gqa else ea.attn_decode
+            call = lambda: fn(*ins, o, w.scale, stream)  # noqa: E731
             flops, nbytes = dec_work(w)
         for _ in range(3):
             call()

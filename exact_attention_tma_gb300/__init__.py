@@ -56,6 +56,9 @@ def load():
             lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
             lib.attn_decode.argtypes = [vp, vp, vp, vp, i, i, i, i, f, vp]
             lib.attn_decode_ws.argtypes = [vp, vp, vp, vp, i, i, i, i, f, vp, sz, vp]
+            lib.attn_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+            lib.attn_decode_gqa.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp]
+            lib.attn_decode_gqa_ws.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
             lib.attn_selftest_bounded_wait.argtypes = [i, vp]
             lib.attn_selftest_bounded_wait.restype = ctypes.c_int
             lib.attn_decode_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, f, vp]
@@ -66,7 +69,8 @@ def load():
             lib.attn_status_string.argtypes = [i]
             lib.attn_status_string.restype = ctypes.c_char_p
             lib.attn_decode_num_splits.argtypes = []
-            for fn in (lib.attn_fwd, lib.attn_decode, lib.attn_decode_ws,
+            for fn in (lib.attn_fwd, lib.attn_decode, lib.attn_decode_ws, lib.attn_fwd_gqa,
+                       lib.attn_decode_gqa, lib.attn_decode_gqa_ws,
                        lib.attn_get_device_status, lib.attn_decode_num_splits):
                 fn.restype = ctypes.c_int
             _lib = lib
@@ -125,6 +129,61 @@ def attn_fwd(Q, K, V, O, LSE, causal: bool, scale: float, stream=None) -> None:
             _dev(LSE, "LSE", torch.float32)]
     _check(load().attn_fwd(*args, B, H, N, d, float(scale), int(bool(causal)),
                            _stream(stream)), "attn_fwd")
+
+
+def attn_fwd_gqa(Q, K, V, O, LSE, causal: bool, scale: float, stream=None) -> None:
+    """Grouped-query forward: Q, O [B, H, N, d], K, V [B, H_kv, N, d] bf16, LSE [B, H, N]."""
+    import torch
+
+    B, H, N, d = Q.shape
+    H_kv = K.shape[1]
+    if tuple(K.shape) != (B, H_kv, N, d) or tuple(V.shape) != (B, H_kv, N, d):
+        raise ValueError(f"K/V shape must be {(B, H_kv, N, d)}")
+    if tuple(O.shape) != (B, H, N, d):
+        raise ValueError(f"O shape {tuple(O.shape)} != Q shape {(B, H, N, d)}")
+    if tuple(LSE.shape) != (B, H, N):
+        raise ValueError(f"LSE shape {tuple(LSE.shape)} != {(B, H, N)}")
+    args = [_dev(Q, "Q", torch.bfloat16), _dev(K, "K", torch.bfloat16),
+            _dev(V, "V", torch.bfloat16), _dev(O, "O", torch.bfloat16),
+            _dev(LSE, "LSE", torch.float32)]
+    _check(load().attn_fwd_gqa(*args, B, H, H_kv, N, d, float(scale), int(bool(causal)),
+                               _stream(stream)), "attn_fwd_gqa")
+
+
+def _gqa_decode_args(q, Kcache, Vcache, O):
+    import torch
+
+    B, H_kv, L, d = Kcache.shape
+    if tuple(Vcache.shape) != (B, H_kv, L, d):
+        raise ValueError("Vcache shape must match Kcache")
+    if q.dim() != 3 or q.shape[0] != B or q.shape[2] != d:
+        raise ValueError(f"q shape {tuple(q.shape)} must be (B, H, d) = ({B}, H, {d})")
+    H = q.shape[1]
+    if tuple(O.shape) != (B, H, d):
+        raise ValueError(f"O shape {tuple(O.shape)} != {(B, H, d)}")
+    args = [_dev(q, "q", torch.bfloat16), _dev(Kcache, "Kcache", torch.bfloat16),
+            _dev(Vcache, "Vcache", torch.bfloat16), _dev(O, "O", torch.bfloat16)]
+    return args, B, H, H_kv, L, d
+
+
+def attn_decode_gqa(q, Kcache, Vcache, O, scale: float, stream=None) -> None:
+    """Grouped-query decode: q, O [B, H, d], Kcache/Vcache [B, H_kv, L, d] bf16."""
+    args, B, H, H_kv, L, d = _gqa_decode_args(q, Kcache, Vcache, O)
+    _check(load().attn_decode_gqa(*args, B, H, H_kv, L, d, float(scale), _stream(stream)),
+           "attn_decode_gqa")
+
+
+def attn_decode_gqa_ws(q, Kcache, Vcache, O, scale: float, ws, stream=None) -> None:
+    """attn_decode_gqa with a caller-owned workspace tensor ``ws`` (any dtype, CUDA)."""
+    import torch
+
+    args, B, H, H_kv, L, d = _gqa_decode_args(q, Kcache, Vcache, O)
+    if not (isinstance(ws, torch.Tensor) and ws.is_cuda and ws.is_contiguous()):
+        raise ValueError("ws must be a contiguous CUDA tensor")
+    nbytes = ws.numel() * ws.element_size()
+    _check(load().attn_decode_gqa_ws(*args, B, H, H_kv, L, d, float(scale),
+                                     ctypes.c_void_p(ws.data_ptr()), nbytes, _stream(stream)),
+           "attn_decode_gqa_ws")
 
 
 def attn_decode(q, Kcache, Vcache, O, scale: float, stream=None) -> None:

@@ -71,11 +71,13 @@ cudaError_t ea::device_status_word(unsigned **out) {
 
 extern "C" {
 
-attn_status attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
-                     int H, int N, int d, float scale, int causal, cudaStream_t stream) {
+attn_status attn_fwd_gqa(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
+                         int H, int H_kv, int N, int d, float scale, int causal,
+                         cudaStream_t stream) {
   if (!Q || !K || !V || !O || !LSE) return ATTN_ERR_NULL;
   attn_status st = check_common(B, H, N, d, scale);
   if (st != ATTN_OK) return st;
+  if (H_kv < 1 || H % H_kv != 0) return ATTN_ERR_SHAPE;
   if (causal != 0 && causal != 1) return ATTN_ERR_ARG;
   // One CTA per (head, 128-row query tile) must fit a 1-D grid.
   if (static_cast<long long>(B) * H * ((N + 127) / 128) >= (1LL << 31)) return ATTN_ERR_SHAPE;
@@ -85,8 +87,13 @@ attn_status attn_fwd(const void *Q, const void *K, const void *V, void *O, float
   unsigned *status = nullptr;
   st = status_ptr(&status);
   if (st != ATTN_OK) return st;
-  cudaError_t e = ea::launch_fwd(Q, K, V, O, LSE, B, H, N, d, scale, causal, status, stream);
+  cudaError_t e = ea::launch_fwd(Q, K, V, O, LSE, B, H, H_kv, N, d, scale, causal, status, stream);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
+                     int H, int N, int d, float scale, int causal, cudaStream_t stream) {
+  return attn_fwd_gqa(Q, K, V, O, LSE, B, H, H, N, d, scale, causal, stream);
 }
 
 size_t attn_decode_workspace_bytes(int B, int H, int L, int d) {
@@ -94,22 +101,31 @@ size_t attn_decode_workspace_bytes(int B, int H, int L, int d) {
   return ea::decode_ws_bytes(B, H, d);
 }
 
-attn_status attn_decode_ws(const void *q, const void *Kcache, const void *Vcache, void *O, int B,
-                           int H, int L, int d, float scale, void *ws, size_t ws_bytes,
-                           cudaStream_t stream) {
+attn_status attn_decode_gqa_ws(const void *q, const void *Kcache, const void *Vcache, void *O,
+                               int B, int H, int H_kv, int L, int d, float scale, void *ws,
+                               size_t ws_bytes, cudaStream_t stream) {
   attn_status st = check_decode(q, Kcache, Vcache, O, B, H, L, d, scale);
   if (st != ATTN_OK) return st;
+  if (H_kv < 1 || H % H_kv != 0) return ATTN_ERR_SHAPE;
   if (!ws) return ATTN_ERR_NULL;
   if (misaligned(ws)) return ATTN_ERR_ALIGN;
   if (ws_bytes < ea::decode_ws_bytes(B, H, d)) return ATTN_ERR_NOMEM;
-  cudaError_t e = ea::launch_decode(q, Kcache, Vcache, O, B, H, L, d, scale, ws, stream);
+  cudaError_t e =
+      ea::launch_decode_gqa(q, Kcache, Vcache, O, B, H, H_kv, L, d, scale, ws, stream);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-attn_status attn_decode(const void *q, const void *Kcache, const void *Vcache, void *O, int B,
-                        int H, int L, int d, float scale, cudaStream_t stream) {
+attn_status attn_decode_ws(const void *q, const void *Kcache, const void *Vcache, void *O, int B,
+                           int H, int L, int d, float scale, void *ws, size_t ws_bytes,
+                           cudaStream_t stream) {
+  return attn_decode_gqa_ws(q, Kcache, Vcache, O, B, H, H, L, d, scale, ws, ws_bytes, stream);
+}
+
+attn_status attn_decode_gqa(const void *q, const void *Kcache, const void *Vcache, void *O, int B,
+                            int H, int H_kv, int L, int d, float scale, cudaStream_t stream) {
   attn_status st = check_decode(q, Kcache, Vcache, O, B, H, L, d, scale);
   if (st != ATTN_OK) return st;
+  if (H_kv < 1 || H % H_kv != 0) return ATTN_ERR_SHAPE;
   int dev;
   st = current_device(&dev);
   if (st != ATTN_OK) return st;
@@ -130,8 +146,14 @@ attn_status attn_decode(const void *q, const void *Kcache, const void *Vcache, v
     }
     ws = g_ws_ptr[dev];
   }
-  cudaError_t e = ea::launch_decode(q, Kcache, Vcache, O, B, H, L, d, scale, ws, stream);
+  cudaError_t e =
+      ea::launch_decode_gqa(q, Kcache, Vcache, O, B, H, H_kv, L, d, scale, ws, stream);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status attn_decode(const void *q, const void *Kcache, const void *Vcache, void *O, int B,
+                        int H, int L, int d, float scale, cudaStream_t stream) {
+  return attn_decode_gqa(q, Kcache, Vcache, O, B, H, H, L, d, scale, stream);
 }
 
 attn_status attn_get_device_status(cudaStream_t stream) {

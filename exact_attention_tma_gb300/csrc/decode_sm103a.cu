@@ -212,6 +212,176 @@ __global__ void __launch_bounds__(128)
   }
 }
 
+// Grouped-query split kernel ("Why Fast GPUs Still Wait for Memory", Attention
+// III: g = h / h_kv query heads share one K/V head, so the same K/V bytes feed
+// g times the arithmetic; "M4.2 GPU Execution Model", example "logical GQA
+// savings require a physical grouped path": map the group's query heads to one
+// shared K/V load instead of expanding the cache).  One CTA per (batch, K/V
+// head, chunk of GQ query heads of its group, split): every K/V row is loaded
+// once and combined in registers with the GQ query vectors (query head
+// h0 + i of the CTA's chunk).  Lane mapping, online softmax and the merge are
+// those of attn_decode_split_kernel, per query head; the partials go to the
+// same per-query-head workspace slots, so the combine kernel is shared.
+template <int D, int GQ>
+__global__ void __launch_bounds__(kWarps * 32)
+    attn_decode_gqa_split_kernel(const __nv_bfloat16 *__restrict__ q,
+                                 const __nv_bfloat16 *__restrict__ Kc,
+                                 const __nv_bfloat16 *__restrict__ Vc, float *__restrict__ ws_o,
+                                 float *__restrict__ ws_lse, int H, int H_kv, int L, int chunk,
+                                 int nsplit, float scale_log2) {
+  constexpr int U = (GQ >= 8) ? 4 : 8;   // keys per lane group per batch (register budget)
+  constexpr int LPK = D / 8;             // lanes per key row
+  constexpr int KPI = 32 / LPK;          // keys per warp-wide load
+  constexpr int NG = kWarps * KPI;       // lane groups per CTA
+  constexpr int BATCH = NG * U;
+  const int group = H / H_kv;
+  const int n_hc = group / GQ;           // query-head chunks per K/V head
+  const int split = blockIdx.x % nsplit;
+  int rest = blockIdx.x / nsplit;
+  const int hc = rest % n_hc;
+  rest /= n_hc;
+  const int hk = rest % H_kv;
+  const int b = rest / H_kv;
+  const int h0 = hk * group + hc * GQ;   // first query head of this CTA
+  const size_t qh0 = static_cast<size_t>(b) * H + h0;   // flat index of that query head
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / LPK;
+  const int dl = lane % LPK;
+  const int lo = split * chunk;
+  const int hi = min(L, lo + chunk);
+
+  // q slices (pairs of fp32) of the GQ query heads.
+  float2 qf[GQ][4];
+#pragma unroll
+  for (int i = 0; i < GQ; ++i) {
+    const uint4 qv = *reinterpret_cast<const uint4 *>(q + (qh0 + i) * D + dl * 8);
+    const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) qf[i][e] = make_float2(bf16lo(w[e]), bf16hi(w[e]));
+  }
+  const size_t kv_off = (static_cast<size_t>(b) * H_kv + hk) * L * D;
+  const __nv_bfloat16 *Kh = Kc + kv_off + dl * 8;
+  const __nv_bfloat16 *Vh = Vc + kv_off + dl * 8;
+
+  float m[GQ], lsum[GQ];
+  float2 acc[GQ][4];
+#pragma unroll
+  for (int i = 0; i < GQ; ++i) {
+    m[i] = -INFINITY;
+    lsum[i] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[i][e] = make_float2(0.f, 0.f);
+  }
+
+  for (int base = lo; base < hi; base += BATCH) {
+    uint4 kr[U], vr[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int key = base + (warp * U + u) * KPI + sub;
+      if (key < hi) {
+        kr[u] = ld_stream_v4(Kh + static_cast<size_t>(key) * D);
+        vr[u] = ld_stream_v4(Vh + static_cast<size_t>(key) * D);
+      } else {
+        kr[u] = make_uint4(0, 0, 0, 0);
+        vr[u] = make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < GQ; ++i) {
+      float x[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint32_t w[4] = {kr[u].x, kr[u].y, kr[u].z, kr[u].w};
+        float2 part = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) part = ffma2(qf[i][e], make_float2(bf16lo(w[e]), bf16hi(w[e])), part);
+        float s = part.x + part.y;
+#pragma unroll
+        for (int off = LPK / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        const int key = base + (warp * U + u) * KPI + sub;
+        x[u] = (key < hi) ? s * scale_log2 : -INFINITY;
+      }
+      float mb = x[0];
+#pragma unroll
+      for (int u = 1; u < U; ++u) mb = fmaxf(mb, x[u]);
+      const float m_new = fmaxf(m[i], mb);
+      if (m_new != -INFINITY) {
+        const float alpha = ex2_approx(m[i] - m_new);
+        lsum[i] *= alpha;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[i][e] = fmul2(acc[i][e], make_float2(alpha, alpha));
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const float p = ex2_approx(x[u] - m_new);
+          lsum[i] += p;
+          const uint32_t w[4] = {vr[u].x, vr[u].y, vr[u].z, vr[u].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            acc[i][e] = ffma2(make_float2(p, p), make_float2(bf16lo(w[e]), bf16hi(w[e])), acc[i][e]);
+        }
+        m[i] = m_new;
+      }
+    }
+  }
+
+  // Merge the NG lane-group states of each query head.
+  __shared__ float sm_m[GQ][NG], sm_l[GQ][NG];
+  __shared__ float sm_acc[GQ][NG][D];
+  const int gi = warp * KPI + sub;
+#pragma unroll
+  for (int i = 0; i < GQ; ++i) {
+    if (dl == 0) {
+      sm_m[i][gi] = m[i];
+      sm_l[i][gi] = lsum[i];
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      sm_acc[i][gi][dl * 8 + 2 * e] = acc[i][e].x;
+      sm_acc[i][gi][dl * 8 + 2 * e + 1] = acc[i][e].y;
+    }
+  }
+  __syncthreads();
+  for (int t = threadIdx.x; t < GQ * D; t += blockDim.x) {
+    const int i = t / D, c = t % D;
+    const size_t part = (qh0 + i) * nsplit + split;
+    float mx = sm_m[i][0];
+#pragma unroll
+    for (int k = 1; k < NG; ++k) mx = fmaxf(mx, sm_m[i][k]);
+    if (mx == -INFINITY) {   // empty split
+      ws_o[part * D + c] = 0.f;
+      if (c == 0) ws_lse[part] = -INFINITY;
+      continue;
+    }
+    float den = 0.f, num = 0.f;
+#pragma unroll
+    for (int k = 0; k < NG; ++k) {
+      const float w = ex2_approx(sm_m[i][k] - mx);
+      den = fmaf(sm_l[i][k], w, den);
+      num = fmaf(sm_acc[i][k][c], w, num);
+    }
+    ws_o[part * D + c] = num / den;
+    if (c == 0) {
+      float lg;
+      asm("lg2.approx.f32 %0, %1;" : "=f"(lg) : "f"(den));
+      ws_lse[part] = mx + lg;   // base-2 log-sum-exp of the split
+    }
+  }
+}
+
+template <int D, int GQ>
+static cudaError_t launch_gqa_t(const void *q, const void *Kc, const void *Vc, int B, int H, int H_kv,
+                                int L, float scale_log2, float *ws_o, float *ws_lse,
+                                cudaStream_t stream) {
+  const int nsplit = kDecodeSplits;
+  const int chunk = (L + nsplit - 1) / nsplit;
+  const long long grid = static_cast<long long>(B) * H_kv * (H / H_kv / GQ) * nsplit;
+  attn_decode_gqa_split_kernel<D, GQ><<<static_cast<unsigned>(grid), kWarps * 32, 0, stream>>>(
+      static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(Kc),
+      static_cast<const __nv_bfloat16 *>(Vc), ws_o, ws_lse, H, H_kv, L, chunk, nsplit, scale_log2);
+  return cudaGetLastError();
+}
+
 template <int D>
 static cudaError_t launch_t(const void *q, const void *Kc, const void *Vc, void *O, int BH, int L,
                             float scale_log2, void *ws, cudaStream_t stream) {
@@ -241,6 +411,40 @@ cudaError_t launch_decode(const void *q, const void *Kc, const void *Vc, void *O
   const float scale_log2 = scale * 1.44269504088896340736f;
   if (d == 128) return dec::launch_t<128>(q, Kc, Vc, O, B * H, L, scale_log2, ws, stream);
   return dec::launch_t<64>(q, Kc, Vc, O, B * H, L, scale_log2, ws, stream);
+}
+
+namespace dec {
+template <int D>
+static cudaError_t launch_gqa_d(const void *q, const void *Kc, const void *Vc, void *O, int B, int H,
+                                int H_kv, int L, float scale_log2, void *ws, cudaStream_t stream) {
+  const int BH = B * H;
+  const int nsplit = kDecodeSplits;
+  float *ws_o = static_cast<float *>(ws);
+  float *ws_lse = ws_o + static_cast<size_t>(BH) * nsplit * D;
+  const int group = H / H_kv;
+  // Query heads per CTA: the largest of 8, 4, 2 dividing the group size.
+  cudaError_t e;
+  if (group % 8 == 0)
+    e = launch_gqa_t<D, 8>(q, Kc, Vc, B, H, H_kv, L, scale_log2, ws_o, ws_lse, stream);
+  else if (group % 4 == 0)
+    e = launch_gqa_t<D, 4>(q, Kc, Vc, B, H, H_kv, L, scale_log2, ws_o, ws_lse, stream);
+  else if (group % 2 == 0)
+    e = launch_gqa_t<D, 2>(q, Kc, Vc, B, H, H_kv, L, scale_log2, ws_o, ws_lse, stream);
+  else
+    e = launch_gqa_t<D, 1>(q, Kc, Vc, B, H, H_kv, L, scale_log2, ws_o, ws_lse, stream);
+  if (e != cudaSuccess) return e;
+  attn_decode_combine_kernel<D><<<(BH + 3) / 4, 128, 0, stream>>>(
+      ws_o, ws_lse, static_cast<__nv_bfloat16 *>(O), BH, nsplit);
+  return cudaGetLastError();
+}
+}  // namespace dec
+
+cudaError_t launch_decode_gqa(const void *q, const void *Kc, const void *Vc, void *O, int B, int H,
+                              int H_kv, int L, int d, float scale, void *ws, cudaStream_t stream) {
+  if (H_kv == H) return launch_decode(q, Kc, Vc, O, B, H, L, d, scale, ws, stream);
+  const float scale_log2 = scale * 1.44269504088896340736f;
+  if (d == 128) return dec::launch_gqa_d<128>(q, Kc, Vc, O, B, H, H_kv, L, scale_log2, ws, stream);
+  return dec::launch_gqa_d<64>(q, Kc, Vc, O, B, H, H_kv, L, scale_log2, ws, stream);
 }
 
 }  // namespace ea

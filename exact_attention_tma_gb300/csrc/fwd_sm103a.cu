@@ -155,8 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                     __nv_bfloat16 *__restrict__ O,
-                    float *__restrict__ LSE, int N, int BH, int n_blk, float scale_log2,
-                    unsigned *status) {
+                    float *__restrict__ LSE, int N, int BH, int n_blk, int H, int group,
+                    float scale_log2, unsigned *status) {
   using C = Cfg<D>;
   constexpr int SK = C::SK;
   constexpr int SV = C::SV;
@@ -173,6 +173,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // cost the same, so query blocks vary fastest and the co-resident CTAs share
   // a few heads' K/V through L2 instead of each streaming its own head.
   const int bh = CAUSAL ? static_cast<int>(blockIdx.x % BH) : static_cast<int>(blockIdx.x / n_blk);
+  // K/V head read by query head bh: H query heads per batch share H / group
+  // K/V heads in contiguous groups ("Why Fast GPUs Still Wait for Memory",
+  // Attention III: GQA with group size g; g = 1 is multi-head attention).
+  const int kvh = (bh / H) * (H / group) + (bh % H) / group;
   const int blk = CAUSAL ? n_blk - 1 - static_cast<int>(blockIdx.x / BH)
                          : static_cast<int>(blockIdx.x % n_blk);
   const int q0 = blk * (QT * BM);
@@ -236,11 +240,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     load_q(0);
     mbar_arrive_expect_tx(B_KF(0), C::KV_BYTES);
     for (int kb = 0; kb < C::KB; ++kb)
-      tma_load_3d(sb + C::OFF_K + kb * kBoxBytes, &tmK, kb * 64, 0, bh, B_KF(0));
+      tma_load_3d(sb + C::OFF_K + kb * kBoxBytes, &tmK, kb * 64, 0, kvh, B_KF(0));
     for (int i = 1; i < QT; ++i) load_q(i);
     mbar_arrive_expect_tx(B_VF(0), C::KV_BYTES);
     for (int kb = 0; kb < C::KB; ++kb)
-      tma_load_3d(sb + C::OFF_V + kb * kBoxBytes, &tmV, kb * 64, 0, bh, B_VF(0));
+      tma_load_3d(sb + C::OFF_V + kb * kBoxBytes, &tmV, kb * 64, 0, kvh, B_VF(0));
   }
   if (warp == kWarpMMA) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -495,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kb = 0; kb < C::KB; ++kb)
             tma_load_3d(sb + C::OFF_K + sk * C::KV_BYTES + kb * kBoxBytes, &tmK, kb * 64, j * BN,
-                        bh, B_KF(sk));
+                        kvh, B_KF(sk));
         }
         issued_k = j + 1;
         const int sv = j % SV;
@@ -506,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kb = 0; kb < C::KB; ++kb)
             tma_load_3d(sb + C::OFF_V + sv * C::KV_BYTES + kb * kBoxBytes, &tmV, kb * 64, j * BN,
-                        bh, B_VF(sv));
+                        kvh, B_VF(sv));
         }
         issued_v = j + 1;
       }
@@ -683,8 +687,8 @@ static bool make_map(CUtensorMap *m, const void *base, int BH, int N, int d) {
 
 template <int D, bool CAUSAL>
 static cudaError_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                            const CUtensorMap &mo, void *O, float *LSE, int BH, int N, float scale_log2,
-                            unsigned *status, cudaStream_t stream) {
+                            const CUtensorMap &mo, void *O, float *LSE, int BH, int N, int H,
+                            int group, float scale_log2, unsigned *status, cudaStream_t stream) {
   using C = Cfg<D>;
   auto kern = attn_fwd_kernel<D, CAUSAL>;
   static std::atomic<unsigned long long> configured{0};   // one bit per device
@@ -701,27 +705,29 @@ static cudaError_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const 
   const int n_blk = (N + QT * BM - 1) / (QT * BM);
   const long long grid = static_cast<long long>(BH) * n_blk;
   kern<<<static_cast<unsigned>(grid), kThreads, C::SMEM_ALLOC, stream>>>(
-      mq, mk, mv, mo, static_cast<__nv_bfloat16 *>(O), LSE, N, BH, n_blk, scale_log2, status);
+      mq, mk, mv, mo, static_cast<__nv_bfloat16 *>(O), LSE, N, BH, n_blk, H, group, scale_log2,
+      status);
   return cudaGetLastError();
 }
 
 }  // namespace fwd
 
 cudaError_t launch_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
-                       int H, int N, int d, float scale, int causal, unsigned *status,
+                       int H, int H_kv, int N, int d, float scale, int causal, unsigned *status,
                        cudaStream_t stream) {
   using namespace fwd;
   const int BH = B * H;
+  const int group = H / H_kv;
   CUtensorMap mq, mk, mv, mo;
-  if (!make_map(&mq, Q, BH, N, d) || !make_map(&mk, K, BH, N, d) || !make_map(&mv, V, BH, N, d) ||
-      !make_map(&mo, O, BH, N, d))
+  if (!make_map(&mq, Q, BH, N, d) || !make_map(&mk, K, B * H_kv, N, d) ||
+      !make_map(&mv, V, B * H_kv, N, d) || !make_map(&mo, O, BH, N, d))
     return cudaErrorInvalidValue;
   const float scale_log2 = scale * 1.44269504088896340736f;
   if (d == 128)
-    return causal ? launch_t<128, true>(mq, mk, mv, mo, O, LSE, BH, N, scale_log2, status, stream)
-                  : launch_t<128, false>(mq, mk, mv, mo, O, LSE, BH, N, scale_log2, status, stream);
-  return causal ? launch_t<64, true>(mq, mk, mv, mo, O, LSE, BH, N, scale_log2, status, stream)
-                : launch_t<64, false>(mq, mk, mv, mo, O, LSE, BH, N, scale_log2, status, stream);
+    return causal ? launch_t<128, true>(mq, mk, mv, mo, O, LSE, BH, N, H, group, scale_log2, status, stream)
+                  : launch_t<128, false>(mq, mk, mv, mo, O, LSE, BH, N, H, group, scale_log2, status, stream);
+  return causal ? launch_t<64, true>(mq, mk, mv, mo, O, LSE, BH, N, H, group, scale_log2, status, stream)
+                : launch_t<64, false>(mq, mk, mv, mo, O, LSE, BH, N, H, group, scale_log2, status, stream);
 }
 
 }  // namespace ea

@@ -34,10 +34,13 @@ class Workload:
     v_dist: str = "normal"   # "normal": N(0,1); "uniform": U(-1, 1)
     nsplit: int = 0      # decode only: KV splits per head
     scale: float = field(default=0.0)
+    H_kv: int = 0        # K/V heads (grouped-query attention); 0 means H_kv = H
 
     def __post_init__(self):
         if self.scale == 0.0:
             object.__setattr__(self, "scale", 1.0 / math.sqrt(self.d))
+        if self.H_kv == 0:
+            object.__setattr__(self, "H_kv", self.H)
 
 
 WORKLOADS = {
@@ -47,6 +50,11 @@ WORKLOADS = {
                               qk_std=1.5, v_dist="uniform"),
     "long_causal_fwd": Workload("long_causal_fwd", "fwd", 1, 32, 16384, 128, True, 3),
     "decode": Workload("decode", "decode", 16, 32, 8192, 128, False, 4, nsplit=32),
+    # Grouped-query shapes (h = 64 query heads over h_kv = 8 K/V heads, g = 8, the
+    # example on the pages), forward and decode.
+    "gqa_fwd": Workload("gqa_fwd", "fwd", 4, 64, 2048, 128, True, 5, H_kv=8),
+    "gqa_decode": Workload("gqa_decode", "decode", 16, 64, 8192, 128, False, 6, nsplit=32,
+                           H_kv=8),
 }
 
 
@@ -62,25 +70,28 @@ def _draw(gen: torch.Generator, shape, std: float, dist: str) -> torch.Tensor:
 
 
 def fwd_inputs(B: int, H: int, N: int, d: int, seed: int, qk_std: float = 1.0,
-               v_dist: str = "normal", device="cpu"):
-    """Q, K, V as contiguous bf16 [B, H, N, d] tensors on ``device``."""
+               v_dist: str = "normal", device="cpu", H_kv: int | None = None):
+    """Q [B, H, N, d] and K, V [B, H_kv, N, d] (H_kv defaults to H), bf16 on ``device``."""
+    H_kv = H if H_kv is None else H_kv
     gen = torch.Generator(device="cpu").manual_seed(seed)
     q = _draw(gen, (B, H, N, d), qk_std, "normal").to(torch.bfloat16)
-    k = _draw(gen, (B, H, N, d), qk_std, "normal").to(torch.bfloat16)
-    v = _draw(gen, (B, H, N, d), 1.0, v_dist).to(torch.bfloat16)
+    k = _draw(gen, (B, H_kv, N, d), qk_std, "normal").to(torch.bfloat16)
+    v = _draw(gen, (B, H_kv, N, d), 1.0, v_dist).to(torch.bfloat16)
     return q.to(device), k.to(device), v.to(device)
 
 
-def decode_inputs(B: int, H: int, L: int, d: int, seed: int, device="cpu"):
-    """q [B, H, d] and Kcache, Vcache [B, H, L, d], all bf16 on ``device``."""
+def decode_inputs(B: int, H: int, L: int, d: int, seed: int, device="cpu",
+                  H_kv: int | None = None):
+    """q [B, H, d] and Kcache, Vcache [B, H_kv, L, d] (H_kv defaults to H), bf16."""
+    H_kv = H if H_kv is None else H_kv
     gen = torch.Generator(device="cpu").manual_seed(seed)
     q = _draw(gen, (B, H, d), 1.0, "normal").to(torch.bfloat16)
-    k = _draw(gen, (B, H, L, d), 1.0, "normal").to(torch.bfloat16)
-    v = _draw(gen, (B, H, L, d), 1.0, "normal").to(torch.bfloat16)
+    k = _draw(gen, (B, H_kv, L, d), 1.0, "normal").to(torch.bfloat16)
+    v = _draw(gen, (B, H_kv, L, d), 1.0, "normal").to(torch.bfloat16)
     return q.to(device), k.to(device), v.to(device)
 
 
 def workload_inputs(w: Workload, device="cpu"):
     if w.kind == "fwd":
-        return fwd_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_std, w.v_dist, device)
-    return decode_inputs(w.B, w.H, w.N, w.d, w.seed, device)
+        return fwd_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_std, w.v_dist, device, w.H_kv)
+    return decode_inputs(w.B, w.H, w.N, w.d, w.seed, device, w.H_kv)

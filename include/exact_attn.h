@@ -112,6 +112,40 @@ attn_status attn_decode_ws(const void *q, const void *Kcache, const void *Vcache
                            size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * Grouped-query attention ("Why Fast GPUs Still Wait for Memory", section
+ * "Attention III · KV cache, GQA, MLA": h query heads share h_kv key/value
+ * heads, group size g = h / h_kv, MQA being g = h; "M4.2 GPU Execution Model
+ * for Transformer Kernels", example "logical GQA savings require a physical
+ * grouped path").  Query head h of a batch reads K/V head floor(h / g)
+ * (contiguous groups).  The K/V tensors keep their H_kv heads: nothing is
+ * expanded, and each K/V tile is loaded once per group (the decode) or shared
+ * through L2 by the group's neighbouring CTAs (the forward).
+ *
+ * attn_fwd_gqa — attn_fwd with Q, O bf16 [B, H, N, d], LSE fp32 [B, H, N] and
+ * K, V bf16 [B, H_kv, N, d].  1 <= H_kv, H % H_kv == 0 (else ATTN_ERR_SHAPE);
+ * H_kv == H is attn_fwd.  Everything else as attn_fwd.
+ */
+attn_status attn_fwd_gqa(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                         int B, int H, int H_kv, int N, int d, float scale, int causal,
+                         cudaStream_t stream);
+
+/*
+ * attn_decode_gqa — attn_decode with q, O bf16 [B, H, d] and Kcache, Vcache
+ * bf16 [B, H_kv, L, d].  One CTA per (batch, K/V head, up to 8 query heads of
+ * its group, split) streams its K/V chunk once for all of those query heads.
+ * Uses the library-owned workspace of attn_decode (same size rule, same
+ * stream caveats); H_kv == H is attn_decode.
+ * attn_decode_gqa_ws — the same with a caller-owned workspace of at least
+ * attn_decode_workspace_bytes(B, H, L, d) bytes (per query head).
+ */
+attn_status attn_decode_gqa(const void *q, const void *Kcache, const void *Vcache, void *O,
+                            int B, int H, int H_kv, int L, int d, float scale,
+                            cudaStream_t stream);
+attn_status attn_decode_gqa_ws(const void *q, const void *Kcache, const void *Vcache, void *O,
+                               int B, int H, int H_kv, int L, int d, float scale, void *ws,
+                               size_t ws_bytes, cudaStream_t stream);
+
+/*
  * attn_decode_noalloc — attn_decode for callers that cannot allocate device
  * memory.  (The pages describe no such entry point; it has no counterpart
  * there.)

@@ -43,7 +43,8 @@ def test_library_exports_every_declared_symbol(lib):
     names = _declared_functions()
     assert {"attn_fwd", "attn_decode", "attn_decode_ws", "attn_get_device_status",
             "attn_status_string", "attn_decode_workspace_bytes",
-            "attn_decode_num_splits"} <= names
+            "attn_decode_num_splits", "attn_fwd_gqa", "attn_decode_gqa",
+            "attn_decode_gqa_ws"} <= names
     for n in names:
         assert hasattr(lib, n), f"{n} declared in include/ but not exported"
 
@@ -121,3 +122,28 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(ea, "_LIB_PATH", str(tmp_path / "nope.so"))
     with pytest.raises(RuntimeError, match="missing"):
         ea.load()
+
+
+@pytest.mark.parametrize("H,H_kv,code", [(8, 0, SHAPE), (8, 3, SHAPE), (8, -2, SHAPE), (6, 4, SHAPE)])
+def test_gqa_rejects_bad_group_before_launch(lib, H, H_kv, code):
+    vp = ctypes.c_void_p
+    assert lib.attn_fwd_gqa(vp(P), vp(P), vp(P), vp(P), vp(P), 1, H, H_kv, 128, 64, 0.125, 0,
+                            None) == code
+    assert lib.attn_decode_gqa(vp(P), vp(P), vp(P), vp(P), 1, H, H_kv, 128, 64, 0.125,
+                               None) == code
+    assert lib.attn_decode_gqa_ws(vp(P), vp(P), vp(P), vp(P), 1, H, H_kv, 128, 64, 0.125, vp(P),
+                                  1 << 20, None) == code
+
+
+def test_gqa_validates_like_the_multi_head_calls(lib):
+    vp = ctypes.c_void_p
+    assert lib.attn_fwd_gqa(vp(0), vp(P), vp(P), vp(P), vp(P), 1, 8, 2, 128, 64, 0.125, 0,
+                            None) == NULL
+    assert lib.attn_fwd_gqa(vp(P), vp(P + 8), vp(P), vp(P), vp(P), 1, 8, 2, 128, 64, 0.125, 0,
+                            None) == ALIGN
+    assert lib.attn_fwd_gqa(vp(P), vp(P), vp(P), vp(P), vp(P), 1, 8, 2, 128, 96, 0.125, 0,
+                            None) == HEADDIM
+    assert lib.attn_decode_gqa(vp(P), vp(P), vp(P), vp(P), 1, 8, 2, 0, 64, 0.125, None) == SHAPE
+    need = ea.attn_decode_workspace_bytes(1, 8, 100, 64)
+    assert lib.attn_decode_gqa_ws(vp(P), vp(P), vp(P), vp(P), 1, 8, 2, 100, 64, 0.125, vp(P),
+                                  need - 1, None) == NOMEM

@@ -28,6 +28,13 @@ def test_algorithmic_flops_and_bytes():
     f, b = bench.dec_work(WORKLOADS["decode"])
     assert f == pytest.approx(4 * 16 * 32 * 8192 * 128)
     assert b == 2_147_745_792
+    # Grouped-query: K and V have h_kv = 8 heads for h = 64 query heads.
+    f, b = bench.fwd_work(WORKLOADS["gqa_fwd"])
+    assert f == pytest.approx(0.5 * 4 * 4 * 64 * 2048 ** 2 * 128)
+    assert b == 2 * (4 * 64 * 2048 * 128) * 2 + 2 * (4 * 8 * 2048 * 128) * 2 + 4 * 64 * 2048 * 4
+    f, b = bench.dec_work(WORKLOADS["gqa_decode"])
+    assert f == pytest.approx(4 * 16 * 64 * 8192 * 128)
+    assert b == 2 * 16 * 8 * 8192 * 128 * 2 + 2 * 16 * 64 * 128 * 2
 
 
 def test_roofline_time_takes_the_slower_roof():
