@@ -273,6 +273,58 @@ def decode_gqa(q, K, V, scale: float, heads=None, threads: int | None = None):
     return O, LSE
 
 
+def paged_rows(pages, block_table_row, seq_len: int, kv_head: int):
+    """The first ``seq_len`` K (or V) rows of one sequence from a paged cache.
+
+    "M4.2 - GPU Execution Model for Transformer Kernels" (pitfall 16 and the
+    kernel contract of its coalescing section): logical K/V continuity does
+    not imply contiguous physical addresses; the decode walks the page/block
+    layout.  Reading: ``pages`` is (num_pages, H_kv, page_size, d), logical
+    token t of the sequence lives in page ``block_table_row[t // page_size]``
+    at slot ``t % page_size``.
+    """
+    page_size = pages.shape[2]
+    t = np.arange(seq_len)
+    ids = np.asarray(block_table_row)[t // page_size]
+    return pages[ids, kv_head, t % page_size]
+
+
+def decode_paged(q, K_pages, V_pages, block_table, seq_lens, scale: float, heads=None,
+                 threads: int | None = None):
+    """Paged (and grouped-query) decode: q (B, H, d); K/V pages
+    (num_pages, H_kv, page_size, d); block_table (B, max_blocks) page ids;
+    seq_lens (B).  Query head h reads K/V head ``kv_head_of(h)`` over the
+    sequence's first seq_lens[b] tokens.  Returns O (B, H, d), LSE (B, H), or
+    per listed flat head.
+    """
+    lib = _load()
+    q, Kp, Vp = _f64(q), _f64(K_pages), _f64(V_pages)
+    B, H, d = q.shape
+    H_kv = Kp.shape[1]
+    hs = list(range(B * H)) if heads is None else list(heads)
+    O = np.empty((len(hs), d), np.float64)
+    LSE = np.empty((len(hs),), np.float64)
+
+    def one(t):
+        b, h = divmod(hs[t], H)
+        kh = kv_head_of(h, H, H_kv)
+        L = int(seq_lens[b])
+        Kh = np.ascontiguousarray(paged_rows(Kp, block_table[b], L, kh))
+        Vh = np.ascontiguousarray(paged_rows(Vp, block_table[b], L, kh))
+        qh = np.ascontiguousarray(q[b, h])
+        o = np.empty((d,), np.float64)
+        lse = np.empty((1,), np.float64)
+        rc = lib.oracle_decode(_ptr(qh), _ptr(Kh), _ptr(Vh), L, d, float(scale), _ptr(o),
+                               _ptr(lse))
+        _check(rc, "oracle_decode")
+        O[t], LSE[t] = o, lse[0]
+
+    _run(one, len(hs), threads)
+    if heads is None:
+        return O.reshape(B, H, d), LSE.reshape(B, H)
+    return O, LSE
+
+
 def _run(fn, n: int, threads: int | None) -> None:
     if n == 0:
         return

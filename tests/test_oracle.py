@@ -294,3 +294,49 @@ def test_gqa_with_one_group_per_head_is_mha():
     Od2, Ld2 = oracle.decode(q, K, V, 0.5)
     np.testing.assert_array_equal(Od, Od2)
     np.testing.assert_array_equal(Ld, Ld2)
+
+
+# ---------------------------------------------------------------- paged caches
+# "M4.2 - GPU Execution Model for Transformer Kernels": logical K/V continuity
+# does not imply contiguous physical addresses.  Reading: block table of page
+# ids per sequence, token t in page table[t // page_size], slot t % page_size.
+
+def _scatter_to_pages(K, V, page_size, rng, extra_pages=3):
+    """Contiguous (B, H_kv, L, d) caches -> shuffled K/V pages and one block table."""
+    B, H_kv, L, d = K.shape
+    nblk = -(-L // page_size)
+    n_pages = B * nblk + extra_pages
+    perm = rng.permutation(n_pages)[: B * nblk].reshape(B, nblk)
+    Kp = rng.standard_normal((n_pages, H_kv, page_size, d))   # junk everywhere else
+    Vp = rng.standard_normal((n_pages, H_kv, page_size, d))
+    for b in range(B):
+        for i in range(nblk):
+            t0, t1 = i * page_size, min(L, (i + 1) * page_size)
+            Kp[perm[b, i], :, : t1 - t0] = K[b, :, t0:t1]
+            Vp[perm[b, i], :, : t1 - t0] = V[b, :, t0:t1]
+    return Kp, Vp, perm
+
+
+@pytest.mark.parametrize("page_size", [1, 4, 16])
+def test_paged_decode_equals_contiguous_decode(page_size):
+    rng = np.random.default_rng(21)
+    B, H, H_kv, L, d = 3, 4, 2, 37, 8
+    q = rng.standard_normal((B, H, d))
+    K = rng.standard_normal((B, H_kv, L, d))
+    V = rng.standard_normal((B, H_kv, L, d))
+    Kp, Vp, table = _scatter_to_pages(K, V, page_size, rng)
+    lens = np.array([L, 1, 20])
+    O, LSE = oracle.decode_paged(q, Kp, Vp, table, lens, 0.3)
+    for b in range(B):
+        Ob, Lb = oracle.decode_gqa(q[b:b + 1], K[b:b + 1, :, : lens[b]], V[b:b + 1, :, : lens[b]], 0.3)
+        np.testing.assert_allclose(O[b], Ob[0], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(LSE[b], Lb[0], rtol=0, atol=1e-13)
+
+
+def test_paged_rows_follow_the_block_table():
+    # token t -> page table[t // S], slot t % S; a transposed index would fail.
+    S = 3
+    pages = np.arange(5 * 1 * S * 1, dtype=np.float64).reshape(5, 1, S, 1)
+    table = np.array([4, 0, 2])
+    rows = oracle.paged_rows(pages, table, 7, 0)[:, 0]
+    assert list(rows) == [12, 13, 14, 0, 1, 2, 6]
