@@ -459,7 +459,7 @@ def per_config(ea, peaks, dev, stream, reps=10):
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     out = {}
     for name in ("causal_fwd", "noncausal_fwd", "long_causal_fwd", "decode", "gqa_fwd",
-                 "gqa_decode"):
+                 "gqa_decode", "paged_decode"):
         w = WORKLOADS[name]
         ins = workload_inputs(w, dev)
         gqa = w.H_kv != w.H
@@ -469,6 +469,10 @@ def per_config(ea, peaks, dev, stream, reps=10):
             fn = ea.attn_fwd_gqa if gqa else ea.attn_fwd
             call = lambda: fn(*ins, o, lse, w.causal, w.scale, stream)  # noqa: E731
             flops, nbytes = fwd_work(w)
+        elif w.kind == "paged":
+            o = torch.empty_like(ins[0])
+            call = lambda: ea.attn_decode_paged(*ins, o, w.scale, stream)  # noqa: E731
+            flops, nbytes = dec_work(w)
         else:
             o = torch.empty_like(ins[0])
             fn = ea.attn_decode_gqa if gqa else ea.attn_decode

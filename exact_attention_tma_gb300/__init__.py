@@ -27,7 +27,9 @@ _LIB_PATH = os.path.join(_PKG, "lib", "libexact_attn.so")
 _lib = None
 _lock = threading.Lock()
 
-ATTN_OK = 0
+# attn_status codes (include/exact_attn.h)
+(ATTN_OK, ATTN_ERR_NULL, ATTN_ERR_SHAPE, ATTN_ERR_HEADDIM, ATTN_ERR_ALIGN, ATTN_ERR_CUDA,
+ ATTN_ERR_NOMEM, ATTN_ERR_TIMEOUT, ATTN_ERR_ARG) = range(9)
 
 
 class AttnError(RuntimeError):
@@ -59,6 +61,7 @@ def load():
             lib.attn_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
             lib.attn_decode_gqa.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp]
             lib.attn_decode_gqa_ws.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
+            lib.attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
             lib.attn_selftest_bounded_wait.argtypes = [i, vp]
             lib.attn_selftest_bounded_wait.restype = ctypes.c_int
             lib.attn_decode_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, f, vp]
@@ -70,7 +73,7 @@ def load():
             lib.attn_status_string.restype = ctypes.c_char_p
             lib.attn_decode_num_splits.argtypes = []
             for fn in (lib.attn_fwd, lib.attn_decode, lib.attn_decode_ws, lib.attn_fwd_gqa,
-                       lib.attn_decode_gqa, lib.attn_decode_gqa_ws,
+                       lib.attn_decode_gqa, lib.attn_decode_gqa_ws, lib.attn_decode_paged,
                        lib.attn_get_device_status, lib.attn_decode_num_splits):
                 fn.restype = ctypes.c_int
             _lib = lib
@@ -184,6 +187,34 @@ def attn_decode_gqa_ws(q, Kcache, Vcache, O, scale: float, ws, stream=None) -> N
     _check(load().attn_decode_gqa_ws(*args, B, H, H_kv, L, d, float(scale),
                                      ctypes.c_void_p(ws.data_ptr()), nbytes, _stream(stream)),
            "attn_decode_gqa_ws")
+
+
+def attn_decode_paged(q, K_pages, V_pages, block_table, seq_lens, O, scale: float,
+                      stream=None) -> None:
+    """Decode against a paged cache: q, O [B, H, d] bf16; K/V pages
+    [num_pages, H_kv, page_size, d] bf16; block_table [B, max_blocks] int32;
+    seq_lens [B] int32 (all on the GPU)."""
+    import torch
+
+    num_pages, H_kv, page_size, d = K_pages.shape
+    if tuple(V_pages.shape) != tuple(K_pages.shape):
+        raise ValueError("V_pages shape must match K_pages")
+    if q.dim() != 3 or q.shape[2] != d:
+        raise ValueError(f"q shape {tuple(q.shape)} must be (B, H, {d})")
+    B, H = q.shape[0], q.shape[1]
+    if tuple(O.shape) != (B, H, d):
+        raise ValueError(f"O shape {tuple(O.shape)} != {(B, H, d)}")
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be (B, max_blocks)")
+    if tuple(seq_lens.shape) != (B,):
+        raise ValueError("seq_lens must be (B,)")
+    max_blocks = block_table.shape[1]
+    args = [_dev(q, "q", torch.bfloat16), _dev(K_pages, "K_pages", torch.bfloat16),
+            _dev(V_pages, "V_pages", torch.bfloat16),
+            _dev(block_table, "block_table", torch.int32), _dev(seq_lens, "seq_lens", torch.int32),
+            _dev(O, "O", torch.bfloat16)]
+    _check(load().attn_decode_paged(*args, B, H, H_kv, num_pages, page_size, max_blocks, d,
+                                    float(scale), _stream(stream)), "attn_decode_paged")
 
 
 def attn_decode(q, Kcache, Vcache, O, scale: float, stream=None) -> None:

@@ -156,6 +156,51 @@ attn_status attn_decode(const void *q, const void *Kcache, const void *Vcache, v
   return attn_decode_gqa(q, Kcache, Vcache, O, B, H, H, L, d, scale, stream);
 }
 
+attn_status attn_decode_paged(const void *q, const void *K_pages, const void *V_pages,
+                              const int *block_table, const int *seq_lens, void *O, int B, int H,
+                              int H_kv, int num_pages, int page_size, int max_blocks, int d,
+                              float scale, cudaStream_t stream) {
+  if (!q || !K_pages || !V_pages || !block_table || !seq_lens || !O) return ATTN_ERR_NULL;
+  if (num_pages < 1 || max_blocks < 1 || page_size < 1 || page_size > (1 << 16) ||
+      (page_size & (page_size - 1)) != 0)
+    return ATTN_ERR_SHAPE;
+  if (static_cast<long long>(max_blocks) * page_size > kMaxLen) return ATTN_ERR_SHAPE;
+  attn_status st = check_common(B, H, max_blocks * page_size, d, scale);
+  if (st != ATTN_OK) return st;
+  if (H_kv < 1 || H % H_kv != 0) return ATTN_ERR_SHAPE;
+  if (misaligned(q) || misaligned(K_pages) || misaligned(V_pages) || misaligned(O) ||
+      (reinterpret_cast<uintptr_t>(block_table) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u) != 0)
+    return ATTN_ERR_ALIGN;
+  unsigned *status = nullptr;
+  st = status_ptr(&status);
+  if (st != ATTN_OK) return st;
+  int dev;
+  st = current_device(&dev);
+  if (st != ATTN_OK) return st;
+  const size_t need = ea::decode_ws_bytes(B, H, d);
+  void *ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_ws_bytes[dev] < need) {
+      // Grow-only workspace; cudaFree waits for work already using the old one.
+      if (g_ws_ptr[dev]) cudaFree(g_ws_ptr[dev]);
+      g_ws_ptr[dev] = nullptr;
+      g_ws_bytes[dev] = 0;
+      if (cudaMalloc(&g_ws_ptr[dev], need) != cudaSuccess) {
+        g_ws_ptr[dev] = nullptr;
+        return ATTN_ERR_NOMEM;
+      }
+      g_ws_bytes[dev] = need;
+    }
+    ws = g_ws_ptr[dev];
+  }
+  cudaError_t e = ea::launch_decode_paged(q, K_pages, V_pages, block_table, seq_lens, O, B, H, H_kv,
+                                          num_pages, page_size, max_blocks, d, scale, ws, status,
+                                          stream);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 attn_status attn_get_device_status(cudaStream_t stream) {
   unsigned *p = nullptr;
   attn_status st = status_ptr(&p);
@@ -166,7 +211,8 @@ attn_status attn_get_device_status(cudaStream_t stream) {
   if (cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
   if (v != 0 && cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  return (v & ea::kStatusTimeoutBit) ? ATTN_ERR_TIMEOUT : ATTN_OK;
+  if (v & ea::kStatusTimeoutBit) return ATTN_ERR_TIMEOUT;
+  return (v & ea::kStatusBadInputBit) ? ATTN_ERR_ARG : ATTN_OK;
 }
 
 const char *attn_status_string(attn_status status) {

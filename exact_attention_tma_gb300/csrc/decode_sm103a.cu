@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(128)
       o[1] = fmaf(ws, v.y, o[1]);
     }
   }
-  const float inv = 1.f / wsum;
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;   // a sequence with no tokens gives O = 0
   __nv_bfloat16 *out = O + static_cast<size_t>(head) * D + lane * E;
   if constexpr (E == 4) {
     const uint32_t a = pack_bf16x2(o[0] * inv, o[1] * inv);
@@ -222,13 +222,27 @@ __global__ void __launch_bounds__(128)
 // h0 + i of the CTA's chunk).  Lane mapping, online softmax and the merge are
 // those of attn_decode_split_kernel, per query head; the partials go to the
 // same per-query-head workspace slots, so the combine kernel is shared.
-template <int D, int GQ>
+// Paged caches ("M4.2 GPU Execution Model for Transformer Kernels", pitfall 16:
+// logical K/V continuity does not imply contiguous physical addresses): with
+// PAGED, Kc/Vc hold pages [num_pages][H_kv][page_size][D], token t of sequence
+// b lives in page block_table[b * max_blocks + t / page_size] at slot
+// t % page_size, and the sequence has seq_lens[b] tokens (clamped to
+// [0, max_blocks * page_size]).  A page id outside [0, num_pages) is not read:
+// its tokens are skipped and kStatusBadInputBit is raised in *status.
+struct Paging {
+  const int *block_table;
+  const int *seq_lens;
+  int max_blocks, num_pages, log2_page;
+  unsigned *status;
+};
+
+template <int D, int GQ, bool PAGED>
 __global__ void __launch_bounds__(kWarps * 32)
     attn_decode_gqa_split_kernel(const __nv_bfloat16 *__restrict__ q,
                                  const __nv_bfloat16 *__restrict__ Kc,
                                  const __nv_bfloat16 *__restrict__ Vc, float *__restrict__ ws_o,
                                  float *__restrict__ ws_lse, int H, int H_kv, int L, int chunk,
-                                 int nsplit, float scale_log2) {
+                                 int nsplit, float scale_log2, Paging pg) {
   constexpr int U = (GQ >= 8) ? 4 : 8;   // keys per lane group per batch (register budget)
   constexpr int LPK = D / 8;             // lanes per key row
   constexpr int KPI = 32 / LPK;          // keys per warp-wide load
@@ -248,6 +262,10 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int lane = threadIdx.x & 31;
   const int sub = lane / LPK;
   const int dl = lane % LPK;
+  if constexpr (PAGED) {   // this sequence's length and split size
+    L = min(max(pg.seq_lens[b], 0), pg.max_blocks << pg.log2_page);
+    chunk = (L + nsplit - 1) / nsplit;
+  }
   const int lo = split * chunk;
   const int hi = min(L, lo + chunk);
 
@@ -260,9 +278,24 @@ __global__ void __launch_bounds__(kWarps * 32)
 #pragma unroll
     for (int e = 0; e < 4; ++e) qf[i][e] = make_float2(bf16lo(w[e]), bf16hi(w[e]));
   }
-  const size_t kv_off = (static_cast<size_t>(b) * H_kv + hk) * L * D;
+  const size_t kv_off = PAGED ? 0 : (static_cast<size_t>(b) * H_kv + hk) * L * D;
   const __nv_bfloat16 *Kh = Kc + kv_off + dl * 8;
   const __nv_bfloat16 *Vh = Vc + kv_off + dl * 8;
+  // Element offset of token `key`'s row (from Kh / Vh), or -1 for a bad page.
+  auto row = [&](int key) -> long long {
+    if constexpr (PAGED) {
+      const int page = __ldg(pg.block_table + static_cast<size_t>(b) * pg.max_blocks +
+                             (key >> pg.log2_page));
+      if (page < 0 || page >= pg.num_pages) {
+        atomicOr(pg.status, kStatusBadInputBit);
+        return -1;
+      }
+      const int slot = key & ((1 << pg.log2_page) - 1);
+      return ((static_cast<long long>(page) * H_kv + hk) << pg.log2_page | slot) * D;
+    } else {
+      return static_cast<long long>(key) * D;
+    }
+  };
 
   float m[GQ], lsum[GQ];
   float2 acc[GQ][4];
@@ -276,12 +309,15 @@ __global__ void __launch_bounds__(kWarps * 32)
 
   for (int base = lo; base < hi; base += BATCH) {
     uint4 kr[U], vr[U];
+    bool valid[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int key = base + (warp * U + u) * KPI + sub;
-      if (key < hi) {
-        kr[u] = ld_stream_v4(Kh + static_cast<size_t>(key) * D);
-        vr[u] = ld_stream_v4(Vh + static_cast<size_t>(key) * D);
+      const long long off = (key < hi) ? row(key) : -1;
+      valid[u] = off >= 0;
+      if (valid[u]) {
+        kr[u] = ld_stream_v4(Kh + off);
+        vr[u] = ld_stream_v4(Vh + off);
       } else {
         kr[u] = make_uint4(0, 0, 0, 0);
         vr[u] = make_uint4(0, 0, 0, 0);
@@ -299,8 +335,7 @@ __global__ void __launch_bounds__(kWarps * 32)
         float s = part.x + part.y;
 #pragma unroll
         for (int off = LPK / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-        const int key = base + (warp * U + u) * KPI + sub;
-        x[u] = (key < hi) ? s * scale_log2 : -INFINITY;
+        x[u] = valid[u] ? s * scale_log2 : -INFINITY;
       }
       float mb = x[0];
 #pragma unroll
@@ -369,16 +404,18 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
 }
 
-template <int D, int GQ>
+template <int D, int GQ, bool PAGED>
 static cudaError_t launch_gqa_t(const void *q, const void *Kc, const void *Vc, int B, int H, int H_kv,
                                 int L, float scale_log2, float *ws_o, float *ws_lse,
-                                cudaStream_t stream) {
+                                const Paging &pg, cudaStream_t stream) {
   const int nsplit = kDecodeSplits;
   const int chunk = (L + nsplit - 1) / nsplit;
   const long long grid = static_cast<long long>(B) * H_kv * (H / H_kv / GQ) * nsplit;
-  attn_decode_gqa_split_kernel<D, GQ><<<static_cast<unsigned>(grid), kWarps * 32, 0, stream>>>(
-      static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(Kc),
-      static_cast<const __nv_bfloat16 *>(Vc), ws_o, ws_lse, H, H_kv, L, chunk, nsplit, scale_log2);
+  attn_decode_gqa_split_kernel<D, GQ, PAGED>
+      <<<static_cast<unsigned>(grid), kWarps * 32, 0, stream>>>(
+          static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(Kc),
+          static_cast<const __nv_bfloat16 *>(Vc), ws_o, ws_lse, H, H_kv, L, chunk, nsplit,
+          scale_log2, pg);
   return cudaGetLastError();
 }
 
@@ -414,9 +451,10 @@ cudaError_t launch_decode(const void *q, const void *Kc, const void *Vc, void *O
 }
 
 namespace dec {
-template <int D>
+template <int D, bool PAGED>
 static cudaError_t launch_gqa_d(const void *q, const void *Kc, const void *Vc, void *O, int B, int H,
-                                int H_kv, int L, float scale_log2, void *ws, cudaStream_t stream) {
+                                int H_kv, int L, float scale_log2, void *ws, const Paging &pg,
+                                cudaStream_t stream) {
   const int BH = B * H;
   const int nsplit = kDecodeSplits;
   float *ws_o = static_cast<float *>(ws);
@@ -425,13 +463,13 @@ static cudaError_t launch_gqa_d(const void *q, const void *Kc, const void *Vc, v
   // Query heads per CTA: the largest of 8, 4, 2 dividing the group size.
   cudaError_t e;
   if (group % 8 == 0)
-    e = launch_gqa_t<D, 8>(q, Kc, Vc, B, H, H_kv, L, scale_log2, ws_o, ws_lse, stream);
+    e = launch_gqa_t<D, 8, PAGED>(q, Kc, Vc, B, H, H_kv, L, scale_log2, ws_o, ws_lse, pg, stream);
   else if (group % 4 == 0)
-    e = launch_gqa_t<D, 4>(q, Kc, Vc, B, H, H_kv, L, scale_log2, ws_o, ws_lse, stream);
+    e = launch_gqa_t<D, 4, PAGED>(q, Kc, Vc, B, H, H_kv, L, scale_log2, ws_o, ws_lse, pg, stream);
   else if (group % 2 == 0)
-    e = launch_gqa_t<D, 2>(q, Kc, Vc, B, H, H_kv, L, scale_log2, ws_o, ws_lse, stream);
+    e = launch_gqa_t<D, 2, PAGED>(q, Kc, Vc, B, H, H_kv, L, scale_log2, ws_o, ws_lse, pg, stream);
   else
-    e = launch_gqa_t<D, 1>(q, Kc, Vc, B, H, H_kv, L, scale_log2, ws_o, ws_lse, stream);
+    e = launch_gqa_t<D, 1, PAGED>(q, Kc, Vc, B, H, H_kv, L, scale_log2, ws_o, ws_lse, pg, stream);
   if (e != cudaSuccess) return e;
   attn_decode_combine_kernel<D><<<(BH + 3) / 4, 128, 0, stream>>>(
       ws_o, ws_lse, static_cast<__nv_bfloat16 *>(O), BH, nsplit);
@@ -443,8 +481,28 @@ cudaError_t launch_decode_gqa(const void *q, const void *Kc, const void *Vc, voi
                               int H_kv, int L, int d, float scale, void *ws, cudaStream_t stream) {
   if (H_kv == H) return launch_decode(q, Kc, Vc, O, B, H, L, d, scale, ws, stream);
   const float scale_log2 = scale * 1.44269504088896340736f;
-  if (d == 128) return dec::launch_gqa_d<128>(q, Kc, Vc, O, B, H, H_kv, L, scale_log2, ws, stream);
-  return dec::launch_gqa_d<64>(q, Kc, Vc, O, B, H, H_kv, L, scale_log2, ws, stream);
+  const dec::Paging none{};
+  if (d == 128)
+    return dec::launch_gqa_d<128, false>(q, Kc, Vc, O, B, H, H_kv, L, scale_log2, ws, none, stream);
+  return dec::launch_gqa_d<64, false>(q, Kc, Vc, O, B, H, H_kv, L, scale_log2, ws, none, stream);
+}
+
+cudaError_t launch_decode_paged(const void *q, const void *K_pages, const void *V_pages,
+                                const int *block_table, const int *seq_lens, void *O, int B, int H,
+                                int H_kv, int num_pages, int page_size, int max_blocks, int d,
+                                float scale, void *ws, unsigned *status, cudaStream_t stream) {
+  const float scale_log2 = scale * 1.44269504088896340736f;
+  int log2_page = 0;
+  while ((1 << log2_page) < page_size) ++log2_page;
+  const dec::Paging pg{block_table, seq_lens, max_blocks, num_pages, log2_page, status};
+  // L bounds the split size only for the host's grid; each CTA recomputes it
+  // from its sequence's length.
+  const int L = max_blocks * page_size;
+  if (d == 128)
+    return dec::launch_gqa_d<128, true>(q, K_pages, V_pages, O, B, H, H_kv, L, scale_log2, ws, pg,
+                                        stream);
+  return dec::launch_gqa_d<64, true>(q, K_pages, V_pages, O, B, H, H_kv, L, scale_log2, ws, pg,
+                                     stream);
 }
 
 }  // namespace ea

@@ -7,6 +7,7 @@ namespace ea {
 
 // Bits of the device status word (see attn_get_device_status).
 constexpr unsigned kStatusTimeoutBit = 1u;
+constexpr unsigned kStatusBadInputBit = 2u;   // a kernel met an invalid index (a page id)
 
 // Forward: one launch of the fused tcgen05/TMA kernel; H query heads over
 // H_kv K/V heads per batch (H % H_kv == 0; H_kv == H is multi-head).  Arguments
@@ -28,5 +29,10 @@ cudaError_t launch_decode(const void *q, const void *Kc, const void *Vc, void *O
 // same workspace layout as launch_decode (per query head).
 cudaError_t launch_decode_gqa(const void *q, const void *Kc, const void *Vc, void *O, int B, int H,
                               int H_kv, int L, int d, float scale, void *ws, cudaStream_t stream);
+// Paged decode (page_size a power of two): same workspace layout.
+cudaError_t launch_decode_paged(const void *q, const void *K_pages, const void *V_pages,
+                                const int *block_table, const int *seq_lens, void *O, int B, int H,
+                                int H_kv, int num_pages, int page_size, int max_blocks, int d,
+                                float scale, void *ws, unsigned *status, cudaStream_t stream);
 
 }  // namespace ea

@@ -35,6 +35,7 @@ class Workload:
     nsplit: int = 0      # decode only: KV splits per head
     scale: float = field(default=0.0)
     H_kv: int = 0        # K/V heads (grouped-query attention); 0 means H_kv = H
+    page_size: int = 0   # paged decode only: tokens per page
 
     def __post_init__(self):
         if self.scale == 0.0:
@@ -55,6 +56,10 @@ WORKLOADS = {
     "gqa_fwd": Workload("gqa_fwd", "fwd", 4, 64, 2048, 128, True, 5, H_kv=8),
     "gqa_decode": Workload("gqa_decode", "decode", 16, 64, 8192, 128, False, 6, nsplit=32,
                            H_kv=8),
+    # The decode workload's cache in pages of 64 tokens scattered over a shuffled
+    # page pool (one block table per sequence, all sequences full length).
+    "paged_decode": Workload("paged_decode", "paged", 16, 32, 8192, 128, False, 7, nsplit=32,
+                             page_size=64),
 }
 
 
@@ -91,7 +96,32 @@ def decode_inputs(B: int, H: int, L: int, d: int, seed: int, device="cpu",
     return q.to(device), k.to(device), v.to(device)
 
 
+def paged_decode_inputs(B: int, H: int, L: int, d: int, page_size: int, seed: int, device="cpu",
+                        H_kv: int | None = None, seq_lens=None, extra_pages: int = 0):
+    """q [B, H, d], K/V pages [num_pages, H_kv, page_size, d] (bf16), block table
+    [B, ceil(L / page_size)] and seq_lens [B] (int32).
+
+    Pages are drawn in fp32 like the contiguous caches (q, then K pages, then V
+    pages, all pages including unused ones), then a random permutation of the
+    page pool (from the same generator) assigns pages to the sequences' blocks.
+    """
+    H_kv = H if H_kv is None else H_kv
+    max_blocks = -(-L // page_size)
+    num_pages = B * max_blocks + extra_pages
+    gen = torch.Generator(device="cpu").manual_seed(seed)
+    q = _draw(gen, (B, H, d), 1.0, "normal").to(torch.bfloat16)
+    kp = _draw(gen, (num_pages, H_kv, page_size, d), 1.0, "normal").to(torch.bfloat16)
+    vp = _draw(gen, (num_pages, H_kv, page_size, d), 1.0, "normal").to(torch.bfloat16)
+    perm = torch.randperm(num_pages, generator=gen)[: B * max_blocks]
+    table = perm.reshape(B, max_blocks).to(torch.int32)
+    lens = torch.full((B,), L, dtype=torch.int32) if seq_lens is None else \
+        torch.as_tensor(seq_lens, dtype=torch.int32)
+    return (q.to(device), kp.to(device), vp.to(device), table.to(device), lens.to(device))
+
+
 def workload_inputs(w: Workload, device="cpu"):
     if w.kind == "fwd":
         return fwd_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_std, w.v_dist, device, w.H_kv)
+    if w.kind == "paged":
+        return paged_decode_inputs(w.B, w.H, w.N, w.d, w.page_size, w.seed, device, w.H_kv)
     return decode_inputs(w.B, w.H, w.N, w.d, w.seed, device, w.H_kv)

@@ -53,7 +53,8 @@ typedef enum {
     ATTN_ERR_CUDA = 5,     /* a CUDA runtime/driver call or launch failed       */
     ATTN_ERR_NOMEM = 6,    /* workspace allocation failed / too small           */
     ATTN_ERR_TIMEOUT = 7,  /* a bounded device-side wait expired                */
-    ATTN_ERR_ARG = 8       /* another argument is invalid (scale, causal flag)  */
+    ATTN_ERR_ARG = 8       /* another argument is invalid (scale, causal flag),
+                              or a kernel met an invalid index (a page id)      */
 } attn_status;
 
 /*
@@ -144,6 +145,37 @@ attn_status attn_decode_gqa(const void *q, const void *Kcache, const void *Vcach
 attn_status attn_decode_gqa_ws(const void *q, const void *Kcache, const void *Vcache, void *O,
                                int B, int H, int H_kv, int L, int d, float scale, void *ws,
                                size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * attn_decode_paged — decode against a paged KV cache ("M4.2 GPU Execution
+ * Model for Transformer Kernels": logical K/V continuity does not imply
+ * contiguous physical addresses; the kernel contract includes the page/block
+ * layout; pitfall 16 of the same page).
+ *
+ *   q, O        : bf16 [B, H, d].
+ *   K_pages,
+ *   V_pages     : bf16 [num_pages, H_kv, page_size, d] (one page holds
+ *                 page_size consecutive tokens of every K/V head).
+ *   block_table : int32 [B, max_blocks], device memory: token t of sequence b
+ *                 is in page block_table[b * max_blocks + t / page_size],
+ *                 slot t % page_size.
+ *   seq_lens    : int32 [B], device memory: tokens of each sequence (clamped
+ *                 to [0, max_blocks * page_size]; a sequence with no tokens
+ *                 gets O = 0).
+ *   page_size   : power of two, 1..65536; max_blocks * page_size <= 2^24.
+ *   H_kv        : K/V heads (grouped-query attention as in attn_decode_gqa;
+ *                 H_kv == H for multi-head).
+ *
+ * All sequences attend to all of their tokens (no mask).  Same split-KV
+ * scheme, library-owned workspace and stream caveats as attn_decode.  A page
+ * id outside [0, num_pages) is never dereferenced: the kernel skips those
+ * tokens and records the error, which the next attn_get_device_status call
+ * reports as ATTN_ERR_ARG (the outputs of that call are then not meaningful).
+ */
+attn_status attn_decode_paged(const void *q, const void *K_pages, const void *V_pages,
+                              const int *block_table, const int *seq_lens, void *O, int B, int H,
+                              int H_kv, int num_pages, int page_size, int max_blocks, int d,
+                              float scale, cudaStream_t stream);
 
 /*
  * attn_decode_noalloc — attn_decode for callers that cannot allocate device

@@ -44,7 +44,7 @@ def test_library_exports_every_declared_symbol(lib):
     assert {"attn_fwd", "attn_decode", "attn_decode_ws", "attn_get_device_status",
             "attn_status_string", "attn_decode_workspace_bytes",
             "attn_decode_num_splits", "attn_fwd_gqa", "attn_decode_gqa",
-            "attn_decode_gqa_ws"} <= names
+            "attn_decode_gqa_ws", "attn_decode_paged"} <= names
     for n in names:
         assert hasattr(lib, n), f"{n} declared in include/ but not exported"
 
@@ -147,3 +147,22 @@ def test_gqa_validates_like_the_multi_head_calls(lib):
     need = ea.attn_decode_workspace_bytes(1, 8, 100, 64)
     assert lib.attn_decode_gqa_ws(vp(P), vp(P), vp(P), vp(P), 1, 8, 2, 100, 64, 0.125, vp(P),
                                   need - 1, None) == NOMEM
+
+
+def _paged(lib, q=P, Kp=P, Vp=P, bt=P, sl=P, O=P, B=2, H=4, H_kv=2, num_pages=8, page_size=16,
+           max_blocks=4, d=64, scale=0.125):
+    vp = ctypes.c_void_p
+    return lib.attn_decode_paged(vp(q), vp(Kp), vp(Vp), vp(bt), vp(sl), vp(O), B, H, H_kv,
+                                 num_pages, page_size, max_blocks, d, scale, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), NULL), (dict(bt=0), NULL), (dict(sl=0), NULL), (dict(Vp=0), NULL),
+    (dict(page_size=12), SHAPE), (dict(page_size=0), SHAPE), (dict(page_size=1 << 17), SHAPE),
+    (dict(num_pages=0), SHAPE), (dict(max_blocks=0), SHAPE), (dict(H_kv=3), SHAPE),
+    (dict(max_blocks=1 << 20, page_size=1 << 5), SHAPE),
+    (dict(d=96), HEADDIM), (dict(Kp=P + 8), ALIGN), (dict(bt=P + 2), ALIGN),
+    (dict(sl=P + 1), ALIGN), (dict(scale=float("nan")), ARG),
+])
+def test_paged_decode_rejects_bad_arguments_before_launch(lib, kw, code):
+    assert _paged(lib, **kw) == code
