@@ -110,8 +110,11 @@ attn_status attn_decode_gqa_ws(const void *q, const void *Kcache, const void *Vc
   if (!ws) return ATTN_ERR_NULL;
   if (misaligned(ws)) return ATTN_ERR_ALIGN;
   if (ws_bytes < ea::decode_ws_bytes(B, H, d)) return ATTN_ERR_NOMEM;
+  unsigned *status = nullptr;
+  st = status_ptr(&status);
+  if (st != ATTN_OK) return st;
   cudaError_t e =
-      ea::launch_decode_gqa(q, Kcache, Vcache, O, B, H, H_kv, L, d, scale, ws, stream);
+      ea::launch_decode_gqa(q, Kcache, Vcache, O, B, H, H_kv, L, d, scale, ws, status, stream);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -128,6 +131,9 @@ attn_status attn_decode_gqa(const void *q, const void *Kcache, const void *Vcach
   if (H_kv < 1 || H % H_kv != 0) return ATTN_ERR_SHAPE;
   int dev;
   st = current_device(&dev);
+  if (st != ATTN_OK) return st;
+  unsigned *status = nullptr;
+  st = status_ptr(&status);
   if (st != ATTN_OK) return st;
   const size_t need = ea::decode_ws_bytes(B, H, d);
   void *ws = nullptr;
@@ -147,7 +153,7 @@ attn_status attn_decode_gqa(const void *q, const void *Kcache, const void *Vcach
     ws = g_ws_ptr[dev];
   }
   cudaError_t e =
-      ea::launch_decode_gqa(q, Kcache, Vcache, O, B, H, H_kv, L, d, scale, ws, stream);
+      ea::launch_decode_gqa(q, Kcache, Vcache, O, B, H, H_kv, L, d, scale, ws, status, stream);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

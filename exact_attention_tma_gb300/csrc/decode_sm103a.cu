@@ -438,6 +438,17 @@ static cudaError_t launch_t(const void *q, const void *Kc, const void *Vc, void 
 
 }  // namespace dec
 
+cudaError_t launch_decode_combine(const float *ws_o, const float *ws_lse, void *O, int BH, int d,
+                                  cudaStream_t stream) {
+  if (d == 128)
+    dec::attn_decode_combine_kernel<128><<<(BH + 3) / 4, 128, 0, stream>>>(
+        ws_o, ws_lse, static_cast<__nv_bfloat16 *>(O), BH, kDecodeSplits);
+  else
+    dec::attn_decode_combine_kernel<64><<<(BH + 3) / 4, 128, 0, stream>>>(
+        ws_o, ws_lse, static_cast<__nv_bfloat16 *>(O), BH, kDecodeSplits);
+  return cudaGetLastError();
+}
+
 size_t decode_ws_bytes(int B, int H, int d) {
   const size_t parts = static_cast<size_t>(B) * H * kDecodeSplits;
   return parts * static_cast<size_t>(d) * 4 + parts * 4;
@@ -478,13 +489,11 @@ static cudaError_t launch_gqa_d(const void *q, const void *Kc, const void *Vc, v
 }  // namespace dec
 
 cudaError_t launch_decode_gqa(const void *q, const void *Kc, const void *Vc, void *O, int B, int H,
-                              int H_kv, int L, int d, float scale, void *ws, cudaStream_t stream) {
+                              int H_kv, int L, int d, float scale, void *ws, unsigned *status,
+                              cudaStream_t stream) {
   if (H_kv == H) return launch_decode(q, Kc, Vc, O, B, H, L, d, scale, ws, stream);
-  const float scale_log2 = scale * 1.44269504088896340736f;
-  const dec::Paging none{};
-  if (d == 128)
-    return dec::launch_gqa_d<128, false>(q, Kc, Vc, O, B, H, H_kv, L, scale_log2, ws, none, stream);
-  return dec::launch_gqa_d<64, false>(q, Kc, Vc, O, B, H, H_kv, L, scale_log2, ws, none, stream);
+  // Grouped heads: the query group is the M dimension of tensor-core products.
+  return launch_decode_gqa_mma(q, Kc, Vc, O, B, H, H_kv, L, d, scale, ws, status, stream);
 }
 
 cudaError_t launch_decode_paged(const void *q, const void *K_pages, const void *V_pages,

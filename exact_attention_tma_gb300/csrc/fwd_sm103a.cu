@@ -670,14 +670,14 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // [B*H, N, d] bf16 viewed as a 3-D tensor; boxes of 64 columns x 128 rows x 1
 // head with 128-byte swizzle.  Rows past N read as zeros.
-static bool make_map(CUtensorMap *m, const void *base, int BH, int N, int d) {
+static bool make_map(CUtensorMap *m, const void *base, int BH, int N, int d, int box_rows = 128) {
   auto enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                         static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                            static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -711,6 +711,10 @@ static cudaError_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const 
 }
 
 }  // namespace fwd
+
+bool make_bhnd_map(CUtensorMap *m, const void *base, int heads, int rows, int d, int box_rows) {
+  return fwd::make_map(m, base, heads, rows, d, box_rows);
+}
 
 cudaError_t launch_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
                        int H, int H_kv, int N, int d, float scale, int causal, unsigned *status,

@@ -1,6 +1,7 @@
 // internal.h — launchers shared between the C-ABI layer and the kernel files.
 #pragma once
 #include <cstddef>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace ea {
@@ -17,6 +18,10 @@ cudaError_t launch_fwd(const void *Q, const void *K, const void *V, void *O, flo
                        int H, int H_kv, int N, int d, float scale, int causal, unsigned *status,
                        cudaStream_t stream);
 
+// TMA map of a bf16 [heads, rows, d] tensor (d contiguous): boxes of 64
+// columns x box_rows rows x 1 head, 128-byte swizzle, rows past `rows` read 0.
+bool make_bhnd_map(CUtensorMap *m, const void *base, int heads, int rows, int d, int box_rows);
+
 // Device address of the current device's status word (looked up once per device).
 cudaError_t device_status_word(unsigned **out);
 
@@ -26,9 +31,20 @@ size_t decode_ws_bytes(int B, int H, int d);
 cudaError_t launch_decode(const void *q, const void *Kc, const void *Vc, void *O, int B, int H,
                           int L, int d, float scale, void *ws, cudaStream_t stream);
 // Grouped-query decode: H query heads over H_kv K/V heads (H % H_kv == 0);
-// same workspace layout as launch_decode (per query head).
+// same workspace layout as launch_decode (per query head).  `status` is the
+// device status word the grouped kernel's bounded waits report into.
 cudaError_t launch_decode_gqa(const void *q, const void *Kc, const void *Vc, void *O, int B, int H,
-                              int H_kv, int L, int d, float scale, void *ws, cudaStream_t stream);
+                              int H_kv, int L, int d, float scale, void *ws, unsigned *status,
+                              cudaStream_t stream);
+// The combine launch of the split-KV decode (one warp per query head).
+cudaError_t launch_decode_combine(const float *ws_o, const float *ws_lse, void *O, int BH, int d,
+                                  cudaStream_t stream);
+// Grouped-query decode on the tensor cores (mma.sync, query heads of a group
+// as the M dimension); same workspace layout.
+cudaError_t launch_decode_gqa_mma(const void *q, const void *Kc, const void *Vc, void *O, int B,
+                                  int H, int H_kv, int L, int d, float scale, void *ws,
+                                  unsigned *status, cudaStream_t stream);
+
 // Paged decode (page_size a power of two): same workspace layout.
 cudaError_t launch_decode_paged(const void *q, const void *K_pages, const void *V_pages,
                                 const int *block_table, const int *seq_lens, void *O, int B, int H,

@@ -260,6 +260,34 @@ __device__ __forceinline__ void mma_bf16_ts_lo(uint32_t d_tmem, uint32_t a_tmem,
       : "memory");
 }
 
+// ------------------------------------------------ warp-level mma.sync (HMMA)
+// Four 8x8 b16 matrices from shared memory; lane i supplies the address of
+// row i % 8 of matrix i / 8.  Plain: lane l receives row l / 4, columns
+// 2 (l % 4) and 2 (l % 4) + 1 of each matrix; .trans: rows 2 (l % 4) and
+// 2 (l % 4) + 1 of column l / 4.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+// C[16x8] (+)= A[16x16] B[16x8], bf16 inputs, fp32 accumulate (A row-major,
+// B column-major fragments; lane l holds rows l/4 and l/4 + 8 of A and C).
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 // Arrive once on `bar` when every tcgen05 async op this thread issued so far
 // has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {

@@ -95,6 +95,38 @@ def test_decode_small_full(L, H, H_kv, d):
     _assert_close(o, O_ref)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("H,H_kv", [(16, 1), (20, 1), (24, 1), (64, 2)])
+@pytest.mark.parametrize("L", [5, 5000])
+def test_decode_large_groups_and_multi_tile_splits(L, H, H_kv, d):
+    # Groups of more than 16 query heads span several CTAs (16 rows each, the
+    # last one ragged); L = 5000 gives splits of several 64-key tiles with a
+    # ragged last tile.
+    q, K, V = decode_inputs(1, H, L, d, seed=L + H + d, device="cuda", H_kv=H_kv)
+    o = _dec(q, K, V, d ** -0.5)
+    O_ref, _ = oracle.decode_gqa(to_f64(q), to_f64(K), to_f64(V), d ** -0.5)
+    _assert_close(o, O_ref)
+
+
+@pytest.mark.parametrize("H,H_kv", [(128, 8), (64, 8)])
+def test_decode_gqa_run_to_run_identical(H, H_kv):
+    # Every launch must give the same bits: the K/V stages are rewritten by
+    # TMA while other warps may still be reading the previous tile, so any
+    # ordering gap between the readers and the refill shows up here first.
+    q, K, V = decode_inputs(16, H, 8192, 128, seed=11, device="cuda", H_kv=H_kv)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(q)
+    first = None
+    for _ in range(40):
+        flush.zero_()
+        ea.attn_decode_gqa(q, K, V, o, 128 ** -0.5)
+        if first is None:
+            first = o.clone()
+        else:
+            assert torch.equal(o, first)
+    torch.cuda.synchronize()
+
+
 def test_decode_gqa_with_caller_workspace_matches():
     q, K, V = decode_inputs(2, 16, 700, 128, seed=3, device="cuda", H_kv=4)
     o1 = _dec(q, K, V, 0.1)
