@@ -68,8 +68,13 @@ def _load():
             lib.oracle_lse_combine.argtypes = [
                 _dp, _dp, ctypes.c_long, ctypes.c_long, _dp, _dp,
             ]
+            lib.oracle_attention_backward.argtypes = [
+                _dp, _dp, _dp, _dp, ctypes.c_long, ctypes.c_long, ctypes.c_double,
+                ctypes.c_int, _dp, _dp, _dp,
+            ]
             for fn in (lib.oracle_attention, lib.oracle_decode,
-                       lib.oracle_decode_split, lib.oracle_lse_combine):
+                       lib.oracle_decode_split, lib.oracle_lse_combine,
+                       lib.oracle_attention_backward):
                 fn.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -323,6 +328,65 @@ def decode_paged(q, K_pages, V_pages, block_table, seq_lens, scale: float, heads
     if heads is None:
         return O.reshape(B, H, d), LSE.reshape(B, H)
     return O, LSE
+
+
+def attention_backward_head(Q, K, V, dO, scale: float, causal: bool):
+    """Gradients of one head: Q, K, V, dO (n, d).  Returns (dQ, dK, dV).
+
+    The chain rule through S = scale QK^T (masked), P = softmax(S), O = PV,
+    with S and P materialised ("Why Fast GPUs Still Wait for Memory",
+    "FlashAttention is an IO algorithm": the backward pass recomputes S).
+    """
+    lib = _load()
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    n, d = Q.shape
+    dQ = np.empty((n, d), np.float64)
+    dK = np.empty((n, d), np.float64)
+    dV = np.empty((n, d), np.float64)
+    rc = lib.oracle_attention_backward(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), n, d, float(scale),
+                                       int(bool(causal)), _ptr(dQ), _ptr(dK), _ptr(dV))
+    _check(rc, "oracle_attention_backward")
+    return dQ, dK, dV
+
+
+def attention_backward(Q, K, V, dO, scale: float, causal: bool, heads=None,
+                       threads: int | None = None):
+    """Batched gradients: Q, dO (B, H, N, d); K, V (B, H_kv, N, d) with
+    H % H_kv == 0 (H_kv = H is plain multi-head attention).
+
+    Returns dQ (B, H, N, d) and dK, dV (B, H_kv, N, d): under grouped-query
+    attention a K/V head's gradient is the sum over the query heads that read
+    it (query head h reads K/V head kv_head_of(h)).  With ``heads`` (flat
+    query-head indices) only those heads are computed and the per-query-head
+    gradients are returned unsummed, each of shape (len(heads), N, d).
+    """
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    B, H, N, d = Q.shape
+    H_kv = K.shape[1]
+    if H % H_kv:
+        raise ValueError("H must be a multiple of H_kv")
+    hs = list(range(B * H)) if heads is None else list(heads)
+    dQh = np.empty((len(hs), N, d), np.float64)
+    dKh = np.empty((len(hs), N, d), np.float64)
+    dVh = np.empty((len(hs), N, d), np.float64)
+
+    def one(t):
+        b, h = divmod(hs[t], H)
+        kh = kv_head_of(h, H, H_kv)
+        dQh[t], dKh[t], dVh[t] = attention_backward_head(Q[b, h], K[b, kh], V[b, kh], dO[b, h],
+                                                         scale, causal)
+
+    _run(one, len(hs), threads)
+    if heads is not None:
+        return dQh, dKh, dVh
+    dK = np.zeros((B, H_kv, N, d), np.float64)
+    dV = np.zeros((B, H_kv, N, d), np.float64)
+    for t, flat in enumerate(hs):
+        b, h = divmod(flat, H)
+        kh = kv_head_of(h, H, H_kv)
+        dK[b, kh] += dKh[t]
+        dV[b, kh] += dVh[t]
+    return dQh.reshape(B, H, N, d), dK, dV
 
 
 def _run(fn, n: int, threads: int | None) -> None:

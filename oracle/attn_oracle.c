@@ -189,3 +189,88 @@ int oracle_lse_combine(const double *O_s, const double *lse_s, long nsplit, long
     *LSE = m + log(wsum);
     return ORACLE_OK;
 }
+
+/*
+ * Gradients of one head's attention with respect to Q, K and V, given the
+ * upstream gradient dO (n x d) of the output.  "Why Fast GPUs Still Wait for
+ * Memory", section "FlashAttention is an IO algorithm", notes that the
+ * backward pass recomputes S instead of storing it; the pages print no
+ * formula for it, so this is the chain rule through the definition above,
+ * written out with S and P materialised:
+ *     dV = P^T dO
+ *     dP = dO V^T
+ *     dS_ij = P_ij (dP_ij - sum_k P_ik dP_ik)     (Jacobian of the row softmax)
+ *     dQ = scale * dS K,   dK = scale * dS^T Q
+ * Masked entries have P = 0 and so dS = 0.  Q, K, V, dO, dQ, dK, dV are n x d.
+ */
+int oracle_attention_backward(const double *Q, const double *K, const double *V,
+                              const double *dO, long n, long d, double scale, int causal,
+                              double *dQ, double *dK, double *dV)
+{
+    if (!Q || !K || !V || !dO || !dQ || !dK || !dV || n < 1 || d < 1)
+        return ORACLE_ERR_ARG;
+    double *P = (double *)malloc(sizeof(double) * (size_t)n * (size_t)n);
+    double *dS = (double *)malloc(sizeof(double) * (size_t)n * (size_t)n);
+    double *O = (double *)malloc(sizeof(double) * (size_t)n * (size_t)d);
+    double *LSE = (double *)malloc(sizeof(double) * (size_t)n);
+    if (!P || !dS || !O || !LSE) {
+        free(P);
+        free(dS);
+        free(O);
+        free(LSE);
+        return ORACLE_ERR_NOMEM;
+    }
+    int rc = oracle_attention(Q, n, K, V, n, d, scale, causal, NULL, n, O, LSE, P, NULL);
+    if (rc) {
+        free(P);
+        free(dS);
+        free(O);
+        free(LSE);
+        return rc;
+    }
+
+    /* dV = P^T dO. */
+    for (long j = 0; j < n; ++j)
+        for (long k = 0; k < d; ++k) {
+            double acc = 0.0;
+            for (long i = 0; i < n; ++i)
+                acc += P[i * n + j] * dO[i * d + k];
+            dV[j * d + k] = acc;
+        }
+
+    /* dP = dO V^T, then dS = P * (dP - rowsum(P * dP)). */
+    for (long i = 0; i < n; ++i) {
+        double dot = 0.0;
+        for (long j = 0; j < n; ++j) {
+            double acc = 0.0;
+            for (long k = 0; k < d; ++k)
+                acc += dO[i * d + k] * V[j * d + k];
+            dS[i * n + j] = acc; /* dP for now */
+            dot += P[i * n + j] * acc;
+        }
+        for (long j = 0; j < n; ++j)
+            dS[i * n + j] = P[i * n + j] * (dS[i * n + j] - dot);
+    }
+
+    /* dQ = scale * dS K;  dK = scale * dS^T Q. */
+    for (long i = 0; i < n; ++i)
+        for (long k = 0; k < d; ++k) {
+            double acc = 0.0;
+            for (long j = 0; j < n; ++j)
+                acc += dS[i * n + j] * K[j * d + k];
+            dQ[i * d + k] = scale * acc;
+        }
+    for (long j = 0; j < n; ++j)
+        for (long k = 0; k < d; ++k) {
+            double acc = 0.0;
+            for (long i = 0; i < n; ++i)
+                acc += dS[i * n + j] * Q[i * d + k];
+            dK[j * d + k] = scale * acc;
+        }
+
+    free(P);
+    free(dS);
+    free(O);
+    free(LSE);
+    return ORACLE_OK;
+}
