@@ -62,6 +62,11 @@ def load():
             lib.attn_decode_gqa.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp]
             lib.attn_decode_gqa_ws.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
             lib.attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+            lib.attn_bwd.argtypes = [vp] * 9 + [i, i, i, i, f, i, vp]
+            lib.attn_bwd_gqa.argtypes = [vp] * 9 + [i, i, i, i, i, f, i, vp]
+            lib.attn_bwd_gqa_ws.argtypes = [vp] * 9 + [i, i, i, i, i, f, i, vp, sz, vp]
+            lib.attn_bwd_workspace_bytes.argtypes = [i, i, i, i]
+            lib.attn_bwd_workspace_bytes.restype = sz
             lib.attn_selftest_bounded_wait.argtypes = [i, vp]
             lib.attn_selftest_bounded_wait.restype = ctypes.c_int
             lib.attn_decode_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, f, vp]
@@ -74,7 +79,8 @@ def load():
             lib.attn_decode_num_splits.argtypes = []
             for fn in (lib.attn_fwd, lib.attn_decode, lib.attn_decode_ws, lib.attn_fwd_gqa,
                        lib.attn_decode_gqa, lib.attn_decode_gqa_ws, lib.attn_decode_paged,
-                       lib.attn_get_device_status, lib.attn_decode_num_splits):
+                       lib.attn_get_device_status, lib.attn_decode_num_splits, lib.attn_bwd,
+                       lib.attn_bwd_gqa, lib.attn_bwd_gqa_ws):
                 fn.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -151,6 +157,54 @@ def attn_fwd_gqa(Q, K, V, O, LSE, causal: bool, scale: float, stream=None) -> No
             _dev(LSE, "LSE", torch.float32)]
     _check(load().attn_fwd_gqa(*args, B, H, H_kv, N, d, float(scale), int(bool(causal)),
                                _stream(stream)), "attn_fwd_gqa")
+
+
+def _bwd_args(Q, K, V, O, dO, LSE, dQ, dK, dV):
+    import torch
+
+    B, H, N, d = Q.shape
+    H_kv = K.shape[1]
+    for name, t in (("K", K), ("V", V), ("dK", dK), ("dV", dV)):
+        if tuple(t.shape) != (B, H_kv, N, d):
+            raise ValueError(f"{name} shape {tuple(t.shape)} != {(B, H_kv, N, d)}")
+    for name, t in (("O", O), ("dO", dO), ("dQ", dQ)):
+        if tuple(t.shape) != (B, H, N, d):
+            raise ValueError(f"{name} shape {tuple(t.shape)} != {(B, H, N, d)}")
+    if tuple(LSE.shape) != (B, H, N):
+        raise ValueError(f"LSE shape {tuple(LSE.shape)} != {(B, H, N)}")
+    args = [_dev(Q, "Q", torch.bfloat16), _dev(K, "K", torch.bfloat16),
+            _dev(V, "V", torch.bfloat16), _dev(O, "O", torch.bfloat16),
+            _dev(dO, "dO", torch.bfloat16), _dev(LSE, "LSE", torch.float32),
+            _dev(dQ, "dQ", torch.bfloat16), _dev(dK, "dK", torch.bfloat16),
+            _dev(dV, "dV", torch.bfloat16)]
+    return args, B, H, H_kv, N, d
+
+
+def attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, causal: bool, scale: float, stream=None) -> None:
+    """Backward of attn_fwd / attn_fwd_gqa: writes dQ [B, H, N, d] and dK, dV
+    [B, H_kv, N, d] (bf16) from Q, K, V, the forward's O and LSE, and dO.
+    H_kv = K.shape[1] (H_kv < H: grouped-query; dK, dV sum over each group)."""
+    args, B, H, H_kv, N, d = _bwd_args(Q, K, V, O, dO, LSE, dQ, dK, dV)
+    _check(load().attn_bwd_gqa(*args, B, H, H_kv, N, d, float(scale), int(bool(causal)),
+                               _stream(stream)), "attn_bwd_gqa")
+
+
+def attn_bwd_ws(Q, K, V, O, dO, LSE, dQ, dK, dV, causal: bool, scale: float, ws,
+                stream=None) -> None:
+    """attn_bwd with a caller-owned workspace tensor ``ws`` (any dtype, CUDA)."""
+    import torch
+
+    args, B, H, H_kv, N, d = _bwd_args(Q, K, V, O, dO, LSE, dQ, dK, dV)
+    if not (isinstance(ws, torch.Tensor) and ws.is_cuda and ws.is_contiguous()):
+        raise ValueError("ws must be a contiguous CUDA tensor")
+    nbytes = ws.numel() * ws.element_size()
+    _check(load().attn_bwd_gqa_ws(*args, B, H, H_kv, N, d, float(scale), int(bool(causal)),
+                                  ctypes.c_void_p(ws.data_ptr()), nbytes, _stream(stream)),
+           "attn_bwd_gqa_ws")
+
+
+def attn_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(load().attn_bwd_workspace_bytes(B, H, N, d))
 
 
 def _gqa_decode_args(q, Kcache, Vcache, O):

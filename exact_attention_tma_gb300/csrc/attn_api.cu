@@ -23,6 +23,26 @@ std::mutex g_mu;
 unsigned *g_status_ptr[kMaxDevices];
 void *g_ws_ptr[kMaxDevices];
 size_t g_ws_bytes[kMaxDevices];
+void *g_bws_ptr[kMaxDevices];      // backward row statistics (separate from decode's)
+size_t g_bws_bytes[kMaxDevices];
+
+// Grow-only library workspace slot of the current device.
+attn_status grow_ws(void **slot, size_t *slot_bytes, size_t need, void **out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (*slot_bytes < need) {
+    // cudaFree waits for work already using the old buffer.
+    if (*slot) cudaFree(*slot);
+    *slot = nullptr;
+    *slot_bytes = 0;
+    if (cudaMalloc(slot, need) != cudaSuccess) {
+      *slot = nullptr;
+      return ATTN_ERR_NOMEM;
+    }
+    *slot_bytes = need;
+  }
+  *out = *slot;
+  return ATTN_OK;
+}
 
 attn_status current_device(int *dev) {
   if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= kMaxDevices) return ATTN_ERR_CUDA;
@@ -51,6 +71,25 @@ attn_status check_common(int B, int H, int len, int d, float scale) {
   if (static_cast<long long>(B) * H > (1LL << 24)) return ATTN_ERR_SHAPE;
   if (d != 64 && d != 128) return ATTN_ERR_HEADDIM;
   if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_ARG;
+  return ATTN_OK;
+}
+
+attn_status check_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                      const float *LSE, const void *dQ, const void *dK, const void *dV, int B,
+                      int H, int H_kv, int N, int d, float scale, int causal) {
+  if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return ATTN_ERR_NULL;
+  attn_status st = check_common(B, H, N, d, scale);
+  if (st != ATTN_OK) return st;
+  if (H_kv < 1 || H % H_kv != 0) return ATTN_ERR_SHAPE;
+  if (causal != 0 && causal != 1) return ATTN_ERR_ARG;
+  // One CTA per (head, 128-row tile) and one prep warp per padded row must
+  // fit 1-D grids.
+  const long long tiles = static_cast<long long>(B) * H * ((N + 127) / 128);
+  if (tiles >= (1LL << 31) || tiles * 128 / 8 >= (1LL << 31)) return ATTN_ERR_SHAPE;
+  if (misaligned(Q) || misaligned(K) || misaligned(V) || misaligned(O) || misaligned(dO) ||
+      misaligned(dQ) || misaligned(dK) || misaligned(dV) ||
+      (reinterpret_cast<uintptr_t>(LSE) & 3u) != 0)
+    return ATTN_ERR_ALIGN;
   return ATTN_OK;
 }
 
@@ -160,6 +199,50 @@ attn_status attn_decode_gqa(const void *q, const void *Kcache, const void *Vcach
 attn_status attn_decode(const void *q, const void *Kcache, const void *Vcache, void *O, int B,
                         int H, int L, int d, float scale, cudaStream_t stream) {
   return attn_decode_gqa(q, Kcache, Vcache, O, B, H, H, L, d, scale, stream);
+}
+
+size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
+  if (check_common(B, H, N, d, 1.f) != ATTN_OK) return 0;
+  return ea::bwd_ws_bytes(B, H, N);
+}
+
+attn_status attn_bwd_gqa_ws(const void *Q, const void *K, const void *V, const void *O,
+                            const void *dO, const float *LSE, void *dQ, void *dK, void *dV, int B,
+                            int H, int H_kv, int N, int d, float scale, int causal, void *ws,
+                            size_t ws_bytes, cudaStream_t stream) {
+  attn_status st = check_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, H_kv, N, d, scale, causal);
+  if (st != ATTN_OK) return st;
+  if (!ws) return ATTN_ERR_NULL;
+  if (misaligned(ws)) return ATTN_ERR_ALIGN;
+  if (ws_bytes < ea::bwd_ws_bytes(B, H, N)) return ATTN_ERR_NOMEM;
+  unsigned *status = nullptr;
+  st = status_ptr(&status);
+  if (st != ATTN_OK) return st;
+  cudaError_t e = ea::launch_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, H_kv, N, d, scale, causal,
+                                 ws, status, stream);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status attn_bwd_gqa(const void *Q, const void *K, const void *V, const void *O,
+                         const void *dO, const float *LSE, void *dQ, void *dK, void *dV, int B,
+                         int H, int H_kv, int N, int d, float scale, int causal,
+                         cudaStream_t stream) {
+  attn_status st = check_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, H_kv, N, d, scale, causal);
+  if (st != ATTN_OK) return st;
+  int dev;
+  st = current_device(&dev);
+  if (st != ATTN_OK) return st;
+  void *ws = nullptr;
+  st = grow_ws(&g_bws_ptr[dev], &g_bws_bytes[dev], ea::bwd_ws_bytes(B, H, N), &ws);
+  if (st != ATTN_OK) return st;
+  return attn_bwd_gqa_ws(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, H_kv, N, d, scale, causal, ws,
+                         ea::bwd_ws_bytes(B, H, N), stream);
+}
+
+attn_status attn_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                     const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int N, int d,
+                     float scale, int causal, cudaStream_t stream) {
+  return attn_bwd_gqa(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, H, N, d, scale, causal, stream);
 }
 
 attn_status attn_decode_paged(const void *q, const void *K_pages, const void *V_pages,

@@ -1,0 +1,761 @@
+// bwd_sm103a.cu — attention backward (dQ, dK, dV) on tcgen05 / TMEM / TMA.
+//
+// "Why Fast GPUs Still Wait for Memory", section "FlashAttention is an IO
+// algorithm": the backward pass keeps the forward's tiling and recomputes S
+// from Q and K instead of storing it, trading extra arithmetic for traffic.
+// With the forward's log-sum-exp L_i saved, each tile recomputes
+//     P_ij = exp(s_ij - L_i)                  (s = scale q_i . k_j, masked)
+// exactly, with no running maximum, and the gradients follow from the chain
+// rule through the row softmax:
+//     dV = P^T dO,   dP = dO V^T,   dS = P * (dP - delta),
+//     delta_i = sum_k dO_ik O_ik  (= sum_j P_ij dP_ij),
+//     dQ = scale dS K,   dK = scale dS^T Q.
+//
+// Three launches:
+//   1. prep:  delta_i and L_i log2(e) per query row, into a workspace padded
+//             to whole 128-row tiles (padding: delta = 0, L = +inf, so padded
+//             query rows get P = 0 in every tile that reads them);
+//   2. dK/dV: one CTA per (K/V head, 128-key tile).  K and V stay in shared
+//             memory; the query tiles of every query head of the group stream
+//             through a two-stage TMA ring (Q, dO, L, delta).  Per query tile
+//             the MMA warp computes S^T = K Q^T and dP^T = V dO^T into TMEM,
+//             eight compute warps turn them into P^T and dS^T (bf16, written
+//             back over S^T and dP^T), and the MMA warp accumulates
+//             dV += P^T dO and dK += dS^T Q in TMEM.  Summing over the group's
+//             query heads in the loop gives grouped-query K/V gradients
+//             without atomics.
+//   3. dQ:    one CTA per (query head, 128-query tile); K/V tiles stream
+//             through the ring; S = Q K^T and dP = dO V^T into TMEM, dS back
+//             over S, dQ += dS K in TMEM.
+// dQ is computed by its own kernel (recomputing S and dP once more) rather
+// than accumulated with atomics across the dK/dV CTAs: the gradient
+// reduction stays deterministic and free of the atomic contention that the
+// "Validating Memory-Optimal Transformer Kernels on Real Hardware" paper
+// (section 4, the fused forward+backward kernel) measured on GPUs.
+//
+// Warp roles (320 threads): warps 0-7 compute (warp w owns TMEM lanes
+// 32 (w % 4) .. +31, i.e. those tile rows, and columns half w / 4 of each
+// 128-wide score tile), warp 8 issues MMAs, warp 9 issues TMA.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace ea {
+namespace bwd {
+
+constexpr int BT = 128;                        // rows per tile (queries or keys)
+constexpr int kThreads = 320;
+constexpr int kComputeWarps = 8;
+constexpr int kWarpMMA = 8;
+constexpr int kWarpTMA = 9;
+constexpr int kStages = 2;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kBoxBytes = 64 * BT * 2;    // one TMA box: 64 columns x 128 rows bf16
+constexpr float kLog2e = 1.44269504088896340736f;
+
+// dK/dV kernel: shared memory K | V | stages (Q, dO, L, delta); TMEM
+// dV | dK | S^T (P^T) | dP^T (dS^T).
+template <int D>
+struct CfgKV {
+  static_assert(D == 64 || D == 128, "head dimension");
+  static constexpr int KB = D / 64;
+  static constexpr uint32_t TILE = BT * D * 2;
+  static constexpr uint32_t OFF_K = 0;
+  static constexpr uint32_t OFF_V = TILE;
+  static constexpr uint32_t OFF_STAGE = 2 * TILE;
+  static constexpr uint32_t ST_Q = 0;
+  static constexpr uint32_t ST_DO = TILE;
+  static constexpr uint32_t ST_LSE = 2 * TILE;          // 128 fp32
+  static constexpr uint32_t ST_DELTA = 2 * TILE + 512;  // 128 fp32
+  static constexpr uint32_t STAGE_BYTES = 2 * TILE + 1024;
+  static constexpr uint32_t STAGE_TX = 2 * TILE + 1024;
+  static constexpr uint32_t OFF_BAR = OFF_STAGE + kStages * STAGE_BYTES;
+  // kv, full[2], empty[2], s, dp, p, done, drain
+  static constexpr int NBAR = 1 + 2 * kStages + 5;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;   // tmem slot, abort flag
+  // At least 116 KB so that one CTA runs per SM: each allocates all 512 TMEM
+  // columns, and a second CTA would only wait for them.
+  static constexpr uint32_t SMEM_ALLOC =
+      SMEM_BYTES + 1024 > 118784u ? SMEM_BYTES + 1024 : 118784u;
+  static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+  static constexpr uint32_t TM_DV = 0;
+  static constexpr uint32_t TM_DK = D;
+  static constexpr uint32_t TM_ST = 2 * D;
+  static constexpr uint32_t TM_DPT = 2 * D + BT;
+  static_assert(TM_DPT + BT <= kTmemCols, "tensor memory budget");
+};
+
+// dQ kernel: shared memory Q | dO | stages (K, V); TMEM S (dS) | dP | dQ.
+template <int D>
+struct CfgQ {
+  static_assert(D == 64 || D == 128, "head dimension");
+  static constexpr int KB = D / 64;
+  static constexpr uint32_t TILE = BT * D * 2;
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_DO = TILE;
+  static constexpr uint32_t OFF_STAGE = 2 * TILE;
+  static constexpr uint32_t ST_K = 0;
+  static constexpr uint32_t ST_V = TILE;
+  static constexpr uint32_t STAGE_BYTES = 2 * TILE;
+  static constexpr uint32_t OFF_BAR = OFF_STAGE + kStages * STAGE_BYTES;
+  // q, full[2], empty[2], s, dp, p, done, drain
+  static constexpr int NBAR = 1 + 2 * kStages + 5;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;
+  static constexpr uint32_t SMEM_ALLOC =
+      SMEM_BYTES + 1024 > 118784u ? SMEM_BYTES + 1024 : 118784u;   // one CTA per SM
+  static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+  static constexpr uint32_t TM_S = 0;
+  static constexpr uint32_t TM_DP = BT;
+  static constexpr uint32_t TM_DQ = 2 * BT;
+  static_assert(TM_DQ + D <= kTmemCols, "tensor memory budget");
+};
+
+// ------------------------------------------------------------------ prep
+// One warp per (head, padded row): delta = sum_k dO O (fp32) and L log2(e).
+template <int D>
+__global__ void __launch_bounds__(256)
+    attn_bwd_prep_kernel(const __nv_bfloat16 *__restrict__ O, const __nv_bfloat16 *__restrict__ dO,
+                         const float *__restrict__ LSE, float *__restrict__ lse2,
+                         float *__restrict__ delta, int N, int N_pad, long long rows) {
+  const long long r = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const long long bh = r / N_pad;
+  const int i = static_cast<int>(r % N_pad);
+  if (i >= N) {
+    if (lane == 0) {
+      lse2[r] = INFINITY;
+      delta[r] = 0.f;
+    }
+    return;
+  }
+  const size_t base = (static_cast<size_t>(bh) * N + i) * D;
+  float acc = 0.f;
+  if constexpr (D == 128) {
+    const uint2 o = *reinterpret_cast<const uint2 *>(O + base + lane * 4);
+    const uint2 g = *reinterpret_cast<const uint2 *>(dO + base + lane * 4);
+    acc = bf16lo(o.x) * bf16lo(g.x) + bf16hi(o.x) * bf16hi(g.x) + bf16lo(o.y) * bf16lo(g.y) +
+          bf16hi(o.y) * bf16hi(g.y);
+  } else {
+    const uint32_t o = *reinterpret_cast<const uint32_t *>(O + base + lane * 2);
+    const uint32_t g = *reinterpret_cast<const uint32_t *>(dO + base + lane * 2);
+    acc = bf16lo(o) * bf16lo(g) + bf16hi(o) * bf16hi(g);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) {
+    delta[r] = acc;
+    lse2[r] = LSE[static_cast<size_t>(bh) * N + i] * kLog2e;
+  }
+}
+
+// Writes 32 fp32 accumulator columns of one row as bf16 (times `mul`).
+__device__ __forceinline__ void store_row32(__nv_bfloat16 *dst, const uint32_t (&r)[32], float mul) {
+  uint32_t pk[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k)
+    pk[k] = pack_bf16x2(__uint_as_float(r[2 * k]) * mul, __uint_as_float(r[2 * k + 1]) * mul);
+#pragma unroll
+  for (int v = 0; v < 4; ++v)
+    st_global_v4(dst + 8 * v, pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+}
+
+// ------------------------------------------------------------------ dK / dV
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
+                         const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV,
+                         const __grid_constant__ CUtensorMap tmdO, const float *__restrict__ lse2,
+                         const float *__restrict__ delta, __nv_bfloat16 *__restrict__ dK,
+                         __nv_bfloat16 *__restrict__ dV, int N, int N_pad, int H, int H_kv,
+                         int n_blk, float scale_log2, float scale, unsigned *status) {
+  using C = CfgKV<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // Causal: K/V heads vary fastest and key tiles go in ascending order (the
+  // first key tiles are seen by the most query tiles: longest first).
+  // Non-causal: key tiles vary fastest, so co-resident CTAs share their
+  // head's Q and dO through L2.
+  const int BHkv = static_cast<int>(gridDim.x) / n_blk;
+  const int bkv = CAUSAL ? static_cast<int>(blockIdx.x % BHkv) : static_cast<int>(blockIdx.x / n_blk);
+  const int jt = CAUSAL ? static_cast<int>(blockIdx.x / BHkv) : static_cast<int>(blockIdx.x % n_blk);
+  const int group = H / H_kv;
+  const int b = bkv / H_kv;
+  const int hk = bkv % H_kv;
+  const int it0 = CAUSAL ? jt : 0;
+  const int n_q = n_blk - it0;                 // query tiles per query head
+  const int n_it = group * n_q;                // (query head of the group, query tile) pairs
+  auto q_head = [&](int t) { return b * H + hk * group + t / n_q; };
+  auto q_tile = [&](int t) { return it0 + t % n_q; };
+
+  const uint32_t bar0 = sb + C::OFF_BAR;
+  const uint32_t B_KV = bar0;
+  auto B_FULL = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto B_EMPTY = [&](int s) { return bar0 + 8u * (1 + kStages + s); };
+  const uint32_t B_S = bar0 + 8u * (1 + 2 * kStages);
+  const uint32_t B_DP = B_S + 8;
+  const uint32_t B_P = B_S + 16;
+  const uint32_t B_DONE = B_S + 24;
+  const uint32_t B_DRAIN = B_S + 32;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+
+  if (threadIdx.x == kWarpTMA * 32) {
+    mbar_init(B_KV, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(B_FULL(s), 1);
+      mbar_init(B_EMPTY(s), 1);
+    }
+    mbar_init(B_S, 1);
+    mbar_init(B_DP, 1);
+    mbar_init(B_P, kComputeWarps);
+    mbar_init(B_DONE, 1);
+    mbar_init(B_DRAIN, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmdO);
+    mbar_arrive_expect_tx(B_KV, 2 * C::TILE);
+    for (int kb = 0; kb < C::KB; ++kb) {
+      tma_load_3d(sb + C::OFF_K + kb * kBoxBytes, &tmK, kb * 64, jt * BT, bkv, B_KV);
+      tma_load_3d(sb + C::OFF_V + kb * kBoxBytes, &tmV, kb * 64, jt * BT, bkv, B_KV);
+    }
+  }
+  if (warp == kWarpMMA) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kWarpTMA) {
+    // ------------------------------------------------------------ TMA
+    const bool leader = elect_one();
+    int issued = 0;
+    for (int t = 0; t < n_it; ++t) {
+      const int s = t % kStages;
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(B_EMPTY(s), ((t / kStages) & 1) ^ 1u, status, abort_flag)))
+        break;
+      if (leader) {
+        const int bh = q_head(t);
+        const int it = q_tile(t);
+        const uint32_t st = sb + C::OFF_STAGE + s * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(B_FULL(s), C::STAGE_TX);
+        for (int kb = 0; kb < C::KB; ++kb) {
+          tma_load_3d(st + C::ST_Q + kb * kBoxBytes, &tmQ, kb * 64, it * BT, bh, B_FULL(s));
+          tma_load_3d(st + C::ST_DO + kb * kBoxBytes, &tmdO, kb * 64, it * BT, bh, B_FULL(s));
+        }
+        const size_t row0 = static_cast<size_t>(bh) * N_pad + static_cast<size_t>(it) * BT;
+        bulk_load_1d(st + C::ST_LSE, lse2 + row0, BT * 4, B_FULL(s));
+        bulk_load_1d(st + C::ST_DELTA, delta + row0, BT * 4, B_FULL(s));
+      }
+      issued = t + 1;
+    }
+    if (leader && *abort_flag) {
+      mbar_wait_drain(B_KV, 0, 100000000ull);
+      for (int j = 0; j < kStages && j < issued; ++j) {
+        const int tt = issued - 1 - j;
+        mbar_wait_drain(B_FULL(tt % kStages), (tt / kStages) & 1, 100000000ull);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kWarpMMA) {
+    // ------------------------------------------------------------ MMA
+    const bool leader = elect_one();
+    constexpr uint32_t kIdescS = make_idesc_bf16(BT, BT, 0, 0);
+    constexpr uint32_t kIdescG = make_idesc_bf16(BT, D, 0, 1);
+    // Low words of the shared-memory descriptors (one common high word):
+    // K-major (head dim contiguous, 16-element k-steps inside a 64-column
+    // box) and MN-major (the stage's Q / dO as B operands with the query
+    // index as the reduction dimension: 16-row k-steps, 64-column boxes
+    // kBoxBytes apart).
+    const uint64_t dK0 = make_sdesc_sw128(sb + C::OFF_K, 16, 1024);
+    const uint32_t hi = static_cast<uint32_t>(dK0 >> 32);
+    const uint32_t k_lo = static_cast<uint32_t>(dK0);
+    const uint32_t v_lo = static_cast<uint32_t>(make_sdesc_sw128(sb + C::OFF_V, 16, 1024));
+    const uint32_t stk_lo = static_cast<uint32_t>(make_sdesc_sw128(sb + C::OFF_STAGE, 16, 1024));
+    const uint32_t stm_lo =
+        static_cast<uint32_t>(make_sdesc_sw128(sb + C::OFF_STAGE, kBoxBytes, 1024));
+    auto wait_all = [&](uint32_t bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, abort_flag));
+    };
+    // S^T = K Q^T and dP^T = V dO^T (both operands K-major).
+    auto issue_scores = [&](int s) {
+      const uint32_t so = (s * C::STAGE_BYTES) >> 4;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t koff = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+        mma_bf16_ss_lo(tmem + C::TM_ST, k_lo + koff, stk_lo + so + (C::ST_Q >> 4) + koff, hi,
+                       kIdescS, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(B_S);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t koff = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+        mma_bf16_ss_lo(tmem + C::TM_DPT, v_lo + koff, stk_lo + so + (C::ST_DO >> 4) + koff, hi,
+                       kIdescS, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(B_DP);
+    };
+    // dV += P^T dO and dK += dS^T Q: A from TMEM (8 columns = 16 queries per
+    // step; queries 0-63 in columns 0-31, 64-127 in columns 64-95 of its
+    // region), B = the stage's dO / Q, MN-major.
+    auto issue_grads = [&](int s, bool acc) {
+      const uint32_t so = (s * C::STAGE_BYTES) >> 4;
+#pragma unroll
+      for (int kk = 0; kk < BT / 16; ++kk) {
+        const uint32_t acol = (kk >> 2) * 64 + (kk & 3) * 8;
+        const uint32_t boff = (kk * 16 * 128) >> 4;
+        mma_bf16_ts_lo(tmem + C::TM_DV, tmem + C::TM_ST + acol,
+                       stm_lo + so + (C::ST_DO >> 4) + boff, hi, kIdescG, (acc || kk > 0) ? 1u : 0u);
+      }
+#pragma unroll
+      for (int kk = 0; kk < BT / 16; ++kk) {
+        const uint32_t acol = (kk >> 2) * 64 + (kk & 3) * 8;
+        const uint32_t boff = (kk * 16 * 128) >> 4;
+        mma_bf16_ts_lo(tmem + C::TM_DK, tmem + C::TM_DPT + acol,
+                       stm_lo + so + (C::ST_Q >> 4) + boff, hi, kIdescG, (acc || kk > 0) ? 1u : 0u);
+      }
+    };
+    bool ok = wait_all(B_KV, 0);
+    for (int t = 0; ok && t < n_it; ++t) {
+      const int s = t % kStages;
+      if (!(ok = wait_all(B_FULL(s), (t / kStages) & 1))) break;
+      if (t > 0) {
+        // The compute warps are done with S^T / dP^T of tile t-1 and have
+        // written P^T / dS^T over them: accumulate, then reuse the regions
+        // (MMAs from one thread run in issue order).
+        if (!(ok = wait_all(B_P, (t - 1) & 1))) break;
+        tc_fence_after();
+        if (leader) {
+          issue_grads((t - 1) % kStages, t > 1);
+          mma_commit(B_EMPTY((t - 1) % kStages));
+        }
+        __syncwarp();
+      }
+      tc_fence_after();
+      if (leader) issue_scores(s);
+      __syncwarp();
+    }
+    if (ok && (ok = wait_all(B_P, (n_it - 1) & 1))) {
+      tc_fence_after();
+      if (leader) {
+        issue_grads((n_it - 1) % kStages, n_it > 1);
+        mma_commit(B_DONE);
+      }
+      __syncwarp();
+    }
+    if (leader) {
+      mma_commit(B_DRAIN);
+      mbar_wait_drain(B_DRAIN, 0, 100000000ull);
+    }
+    __syncwarp();
+  } else {
+    // --------------------------------------------------------- compute
+    const int q = warp & 3;                  // TMEM lanes 32q..32q+31 = key rows
+    const int hf = warp >> 2;                // query columns 64 hf .. 64 hf + 63
+    const int row = 32 * q + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    bool ok = true;
+    for (int t = 0; t < n_it; ++t) {
+      const int s = t % kStages;
+      const int it = q_tile(t);
+      ok = __all_sync(0xffffffffu, mbar_wait(B_FULL(s), (t / kStages) & 1, status, abort_flag)) &&
+           __all_sync(0xffffffffu, mbar_wait(B_S, t & 1, status, abort_flag)) &&
+           __all_sync(0xffffffffu, mbar_wait(B_DP, t & 1, status, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      const float *lse_s =
+          reinterpret_cast<const float *>(smem + C::OFF_STAGE + s * C::STAGE_BYTES + C::ST_LSE);
+      const float *del_s =
+          reinterpret_cast<const float *>(smem + C::OFF_STAGE + s * C::STAGE_BYTES + C::ST_DELTA);
+      const bool diag = CAUSAL && it == jt;
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        const int col0 = 64 * hf + 32 * c;
+        uint32_t sr[32], dp[32];
+        tmem_ld_32cols(tmem + lane_base + C::TM_ST + col0, sr);
+        tmem_ld_32cols(tmem + lane_base + C::TM_DPT + col0, dp);
+        tmem_ld_wait_regs(sr);
+        reg_fence32(dp);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int k = 0; k < 32; k += 4) {
+          const float4 lv = *reinterpret_cast<const float4 *>(lse_s + col0 + k);
+          const float4 dv = *reinterpret_cast<const float4 *>(del_s + col0 + k);
+          const float lsev[4] = {lv.x, lv.y, lv.z, lv.w};
+          const float delv[4] = {dv.x, dv.y, dv.z, dv.w};
+          float p[4], ds[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float pe = ex2_approx(fmaf(__uint_as_float(sr[k + e]), scale_log2, -lsev[e]));
+            if (diag && col0 + k + e < row) pe = 0.f;   // query before key: masked
+            p[e] = pe;
+            ds[e] = pe * (__uint_as_float(dp[k + e]) - delv[e]);
+          }
+          pk[k / 2] = pack_bf16x2(p[0], p[1]);
+          pk[k / 2 + 1] = pack_bf16x2(p[2], p[3]);
+          dk[k / 2] = pack_bf16x2(ds[0], ds[1]);
+          dk[k / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+        }
+        tmem_st_16cols(tmem + lane_base + C::TM_ST + 64 * hf + 16 * c, pk);
+        tmem_st_16cols(tmem + lane_base + C::TM_DPT + 64 * hf + 16 * c, dk);
+      }
+      tmem_st_wait();
+      // The stage's L / delta were read through the generic proxy and the
+      // next TMA refill writes them through the async proxy.
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(B_P);
+    }
+    if (ok && __all_sync(0xffffffffu, mbar_wait(B_DONE, 0, status, abort_flag))) {
+      tc_fence_after();
+      const int key = jt * BT + row;
+      const size_t out = (static_cast<size_t>(bkv) * N + key) * D + hf * (D / 2);
+#pragma unroll 1
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t r[32];
+        tmem_ld_32cols(tmem + lane_base + C::TM_DV + hf * (D / 2) + 32 * c, r);
+        tmem_ld_wait_regs(r);
+        if (key < N) store_row32(dV + out + 32 * c, r, 1.f);
+        tmem_ld_32cols(tmem + lane_base + C::TM_DK + hf * (D / 2) + 32 * c, r);
+        tmem_ld_wait_regs(r);
+        if (key < N) store_row32(dK + out + 32 * c, r, scale);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ dQ
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
+                       const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ CUtensorMap tmdO, const float *__restrict__ lse2,
+                       const float *__restrict__ delta, __nv_bfloat16 *__restrict__ dQ, int N,
+                       int N_pad, int H, int H_kv, int n_blk, float scale_log2, float scale,
+                       unsigned *status) {
+  using C = CfgQ<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // Causal: heads fastest, query tiles in descending order (longest first).
+  // Non-causal: query tiles fastest (co-resident CTAs share K/V through L2).
+  const int BH = static_cast<int>(gridDim.x) / n_blk;
+  const int bh = CAUSAL ? static_cast<int>(blockIdx.x % BH) : static_cast<int>(blockIdx.x / n_blk);
+  const int it = CAUSAL ? n_blk - 1 - static_cast<int>(blockIdx.x / BH)
+                        : static_cast<int>(blockIdx.x % n_blk);
+  const int group = H / H_kv;
+  const int kvh = (bh / H) * H_kv + (bh % H) / group;
+  const int n_j = CAUSAL ? it + 1 : n_blk;
+
+  const uint32_t bar0 = sb + C::OFF_BAR;
+  const uint32_t B_Q = bar0;
+  auto B_FULL = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto B_EMPTY = [&](int s) { return bar0 + 8u * (1 + kStages + s); };
+  const uint32_t B_S = bar0 + 8u * (1 + 2 * kStages);
+  const uint32_t B_DP = B_S + 8;
+  const uint32_t B_P = B_S + 16;
+  const uint32_t B_DONE = B_S + 24;
+  const uint32_t B_DRAIN = B_S + 32;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+
+  if (threadIdx.x == kWarpTMA * 32) {
+    mbar_init(B_Q, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(B_FULL(s), 1);
+      mbar_init(B_EMPTY(s), 1);
+    }
+    mbar_init(B_S, 1);
+    mbar_init(B_DP, 1);
+    mbar_init(B_P, kComputeWarps);
+    mbar_init(B_DONE, 1);
+    mbar_init(B_DRAIN, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmdO);
+    mbar_arrive_expect_tx(B_Q, 2 * C::TILE);
+    for (int kb = 0; kb < C::KB; ++kb) {
+      tma_load_3d(sb + C::OFF_Q + kb * kBoxBytes, &tmQ, kb * 64, it * BT, bh, B_Q);
+      tma_load_3d(sb + C::OFF_DO + kb * kBoxBytes, &tmdO, kb * 64, it * BT, bh, B_Q);
+    }
+  }
+  if (warp == kWarpMMA) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kWarpTMA) {
+    // ------------------------------------------------------------ TMA
+    const bool leader = elect_one();
+    int issued = 0;
+    for (int j = 0; j < n_j; ++j) {
+      const int s = j % kStages;
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(B_EMPTY(s), ((j / kStages) & 1) ^ 1u, status, abort_flag)))
+        break;
+      if (leader) {
+        const uint32_t st = sb + C::OFF_STAGE + s * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(B_FULL(s), 2 * C::TILE);
+        for (int kb = 0; kb < C::KB; ++kb) {
+          tma_load_3d(st + C::ST_K + kb * kBoxBytes, &tmK, kb * 64, j * BT, kvh, B_FULL(s));
+          tma_load_3d(st + C::ST_V + kb * kBoxBytes, &tmV, kb * 64, j * BT, kvh, B_FULL(s));
+        }
+      }
+      issued = j + 1;
+    }
+    if (leader && *abort_flag) {
+      mbar_wait_drain(B_Q, 0, 100000000ull);
+      for (int u = 0; u < kStages && u < issued; ++u) {
+        const int jj = issued - 1 - u;
+        mbar_wait_drain(B_FULL(jj % kStages), (jj / kStages) & 1, 100000000ull);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kWarpMMA) {
+    // ------------------------------------------------------------ MMA
+    const bool leader = elect_one();
+    constexpr uint32_t kIdescS = make_idesc_bf16(BT, BT, 0, 0);
+    constexpr uint32_t kIdescG = make_idesc_bf16(BT, D, 0, 1);
+    const uint64_t dQ0 = make_sdesc_sw128(sb + C::OFF_Q, 16, 1024);
+    const uint32_t hi = static_cast<uint32_t>(dQ0 >> 32);
+    const uint32_t q_lo = static_cast<uint32_t>(dQ0);
+    const uint32_t do_lo = static_cast<uint32_t>(make_sdesc_sw128(sb + C::OFF_DO, 16, 1024));
+    const uint32_t stk_lo = static_cast<uint32_t>(make_sdesc_sw128(sb + C::OFF_STAGE, 16, 1024));
+    const uint32_t stm_lo =
+        static_cast<uint32_t>(make_sdesc_sw128(sb + C::OFF_STAGE, kBoxBytes, 1024));
+    auto wait_all = [&](uint32_t bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, abort_flag));
+    };
+    // S = Q K^T and dP = dO V^T (K-major operands).
+    auto issue_scores = [&](int s) {
+      const uint32_t so = (s * C::STAGE_BYTES) >> 4;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t koff = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+        mma_bf16_ss_lo(tmem + C::TM_S, q_lo + koff, stk_lo + so + (C::ST_K >> 4) + koff, hi,
+                       kIdescS, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(B_S);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t koff = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+        mma_bf16_ss_lo(tmem + C::TM_DP, do_lo + koff, stk_lo + so + (C::ST_V >> 4) + koff, hi,
+                       kIdescS, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(B_DP);
+    };
+    // dQ += dS K: dS from TMEM (over S), K MN-major (16-key steps).
+    auto issue_dq = [&](int s, bool acc) {
+      const uint32_t so = (s * C::STAGE_BYTES) >> 4;
+#pragma unroll
+      for (int kk = 0; kk < BT / 16; ++kk) {
+        const uint32_t acol = (kk >> 2) * 64 + (kk & 3) * 8;
+        const uint32_t boff = (kk * 16 * 128) >> 4;
+        mma_bf16_ts_lo(tmem + C::TM_DQ, tmem + C::TM_S + acol, stm_lo + so + (C::ST_K >> 4) + boff,
+                       hi, kIdescG, (acc || kk > 0) ? 1u : 0u);
+      }
+    };
+    bool ok = wait_all(B_Q, 0);
+    for (int j = 0; ok && j < n_j; ++j) {
+      const int s = j % kStages;
+      if (!(ok = wait_all(B_FULL(s), (j / kStages) & 1))) break;
+      if (j > 0) {
+        if (!(ok = wait_all(B_P, (j - 1) & 1))) break;
+        tc_fence_after();
+        if (leader) {
+          issue_dq((j - 1) % kStages, j > 1);
+          mma_commit(B_EMPTY((j - 1) % kStages));
+        }
+        __syncwarp();
+      }
+      tc_fence_after();
+      if (leader) issue_scores(s);
+      __syncwarp();
+    }
+    if (ok && (ok = wait_all(B_P, (n_j - 1) & 1))) {
+      tc_fence_after();
+      if (leader) {
+        issue_dq((n_j - 1) % kStages, n_j > 1);
+        mma_commit(B_DONE);
+      }
+      __syncwarp();
+    }
+    if (leader) {
+      mma_commit(B_DRAIN);
+      mbar_wait_drain(B_DRAIN, 0, 100000000ull);
+    }
+    __syncwarp();
+  } else {
+    // --------------------------------------------------------- compute
+    const int q = warp & 3;                  // TMEM lanes 32q..32q+31 = query rows
+    const int hf = warp >> 2;                // key columns 64 hf .. 64 hf + 63
+    const int row = 32 * q + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    const size_t prow = static_cast<size_t>(bh) * N_pad + static_cast<size_t>(it) * BT + row;
+    const float l2 = lse2[prow];
+    const float dl = delta[prow];
+    bool ok = true;
+    for (int j = 0; j < n_j; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(B_S, j & 1, status, abort_flag)) &&
+           __all_sync(0xffffffffu, mbar_wait(B_DP, j & 1, status, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      const bool diag = CAUSAL && j == it;
+      const int kmax = N - j * BT;            // keys past the sequence are masked
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        const int col0 = 64 * hf + 32 * c;
+        uint32_t sr[32], dp[32];
+        tmem_ld_32cols(tmem + lane_base + C::TM_S + col0, sr);
+        tmem_ld_32cols(tmem + lane_base + C::TM_DP + col0, dp);
+        tmem_ld_wait_regs(sr);
+        reg_fence32(dp);
+        uint32_t dk[16];
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          float ds[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int col = col0 + k + e;
+            float pe = ex2_approx(fmaf(__uint_as_float(sr[k + e]), scale_log2, -l2));
+            if ((diag && col > row) || col >= kmax) pe = 0.f;
+            ds[e] = pe * (__uint_as_float(dp[k + e]) - dl);
+          }
+          dk[k / 2] = pack_bf16x2(ds[0], ds[1]);
+        }
+        tmem_st_16cols(tmem + lane_base + C::TM_S + 64 * hf + 16 * c, dk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(B_P);
+    }
+    if (ok && __all_sync(0xffffffffu, mbar_wait(B_DONE, 0, status, abort_flag))) {
+      tc_fence_after();
+      const int qi = it * BT + row;
+      const size_t out = (static_cast<size_t>(bh) * N + qi) * D + hf * (D / 2);
+#pragma unroll 1
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t r[32];
+        tmem_ld_32cols(tmem + lane_base + C::TM_DQ + hf * (D / 2) + 32 * c, r);
+        tmem_ld_wait_regs(r);
+        if (qi < N) store_row32(dQ + out + 32 * c, r, scale);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host
+template <int D, bool CAUSAL>
+static cudaError_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                            const CUtensorMap &mdo, const float *lse2, const float *delta,
+                            void *dQ, void *dK, void *dV, int B, int H, int H_kv, int N, int N_pad,
+                            int n_blk, float scale, unsigned *status, cudaStream_t stream) {
+  const float scale_log2 = scale * kLog2e;
+  auto kkv = attn_bwd_dkdv_kernel<D, CAUSAL>;
+  auto kq = attn_bwd_dq_kernel<D, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(CfgKV<D>::SMEM_ALLOC));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(CfgQ<D>::SMEM_ALLOC));
+  if (e != cudaSuccess) return e;
+  kkv<<<static_cast<unsigned>(B * H_kv * n_blk), kThreads, CfgKV<D>::SMEM_ALLOC, stream>>>(
+      mq, mk, mv, mdo, lse2, delta, static_cast<__nv_bfloat16 *>(dK),
+      static_cast<__nv_bfloat16 *>(dV), N, N_pad, H, H_kv, n_blk, scale_log2, scale, status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  kq<<<static_cast<unsigned>(B * H * n_blk), kThreads, CfgQ<D>::SMEM_ALLOC, stream>>>(
+      mq, mk, mv, mdo, lse2, delta, static_cast<__nv_bfloat16 *>(dQ), N, N_pad, H, H_kv, n_blk,
+      scale_log2, scale, status);
+  return cudaGetLastError();
+}
+
+}  // namespace bwd
+
+size_t bwd_ws_bytes(int B, int H, int N) {
+  const size_t n_pad = static_cast<size_t>((N + bwd::BT - 1) / bwd::BT) * bwd::BT;
+  return 2 * static_cast<size_t>(B) * H * n_pad * 4;
+}
+
+cudaError_t launch_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                       const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int H_kv,
+                       int N, int d, float scale, int causal, void *ws, unsigned *status,
+                       cudaStream_t stream) {
+  using namespace bwd;
+  const int n_blk = (N + BT - 1) / BT;
+  const int N_pad = n_blk * BT;
+  const long long rows = static_cast<long long>(B) * H * N_pad;
+  float *lse2 = static_cast<float *>(ws);
+  float *delta = lse2 + rows;
+  const unsigned prep_grid = static_cast<unsigned>((rows + 7) / 8);
+  if (d == 128)
+    attn_bwd_prep_kernel<128><<<prep_grid, 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(O), static_cast<const __nv_bfloat16 *>(dO), LSE, lse2,
+        delta, N, N_pad, rows);
+  else
+    attn_bwd_prep_kernel<64><<<prep_grid, 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(O), static_cast<const __nv_bfloat16 *>(dO), LSE, lse2,
+        delta, N, N_pad, rows);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  CUtensorMap mq, mk, mv, mdo;
+  if (!make_bhnd_map(&mq, Q, B * H, N, d, BT) || !make_bhnd_map(&mk, K, B * H_kv, N, d, BT) ||
+      !make_bhnd_map(&mv, V, B * H_kv, N, d, BT) || !make_bhnd_map(&mdo, dO, B * H, N, d, BT))
+    return cudaErrorInvalidValue;
+  if (d == 128)
+    return causal ? launch_t<128, true>(mq, mk, mv, mdo, lse2, delta, dQ, dK, dV, B, H, H_kv, N,
+                                        N_pad, n_blk, scale, status, stream)
+                  : launch_t<128, false>(mq, mk, mv, mdo, lse2, delta, dQ, dK, dV, B, H, H_kv, N,
+                                         N_pad, n_blk, scale, status, stream);
+  return causal ? launch_t<64, true>(mq, mk, mv, mdo, lse2, delta, dQ, dK, dV, B, H, H_kv, N, N_pad,
+                                     n_blk, scale, status, stream)
+                : launch_t<64, false>(mq, mk, mv, mdo, lse2, delta, dQ, dK, dV, B, H, H_kv, N,
+                                      N_pad, n_blk, scale, status, stream);
+}
+
+}  // namespace ea

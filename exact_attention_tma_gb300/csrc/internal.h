@@ -45,6 +45,14 @@ cudaError_t launch_decode_gqa_mma(const void *q, const void *Kc, const void *Vc,
                                   int H, int H_kv, int L, int d, float scale, void *ws,
                                   unsigned *status, cudaStream_t stream);
 
+// Backward: row statistics (2 fp32 per padded query row) in `ws`, then the
+// dK/dV and dQ kernels, all on `stream`.
+size_t bwd_ws_bytes(int B, int H, int N);
+cudaError_t launch_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                       const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int H_kv,
+                       int N, int d, float scale, int causal, void *ws, unsigned *status,
+                       cudaStream_t stream);
+
 // Paged decode (page_size a power of two): same workspace layout.
 cudaError_t launch_decode_paged(const void *q, const void *K_pages, const void *V_pages,
                                 const int *block_table, const int *seq_lens, void *O, int B, int H,

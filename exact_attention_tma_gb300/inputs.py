@@ -60,6 +60,9 @@ WORKLOADS = {
     # page pool (one block table per sequence, all sequences full length).
     "paged_decode": Workload("paged_decode", "paged", 16, 32, 8192, 128, False, 7, nsplit=32,
                              page_size=64),
+    # Backward of the causal forward shape: Q, K, V as the forward draws them,
+    # then the upstream gradient dO ~ N(0, 1).
+    "causal_bwd": Workload("causal_bwd", "bwd", 4, 16, 2048, 128, True, 8),
 }
 
 
@@ -119,7 +122,21 @@ def paged_decode_inputs(B: int, H: int, L: int, d: int, page_size: int, seed: in
     return (q.to(device), kp.to(device), vp.to(device), table.to(device), lens.to(device))
 
 
+def bwd_inputs(B: int, H: int, N: int, d: int, seed: int, qk_std: float = 1.0,
+               v_dist: str = "normal", device="cpu", H_kv: int | None = None):
+    """Q, K, V as fwd_inputs draws them, then dO [B, H, N, d] ~ N(0, 1), bf16."""
+    H_kv = H if H_kv is None else H_kv
+    gen = torch.Generator(device="cpu").manual_seed(seed)
+    q = _draw(gen, (B, H, N, d), qk_std, "normal").to(torch.bfloat16)
+    k = _draw(gen, (B, H_kv, N, d), qk_std, "normal").to(torch.bfloat16)
+    v = _draw(gen, (B, H_kv, N, d), 1.0, v_dist).to(torch.bfloat16)
+    do = _draw(gen, (B, H, N, d), 1.0, "normal").to(torch.bfloat16)
+    return q.to(device), k.to(device), v.to(device), do.to(device)
+
+
 def workload_inputs(w: Workload, device="cpu"):
+    if w.kind == "bwd":
+        return bwd_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_std, w.v_dist, device, w.H_kv)
     if w.kind == "fwd":
         return fwd_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_std, w.v_dist, device, w.H_kv)
     if w.kind == "paged":

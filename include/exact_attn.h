@@ -132,8 +132,9 @@ attn_status attn_fwd_gqa(const void *Q, const void *K, const void *V, void *O, f
 
 /*
  * attn_decode_gqa — attn_decode with q, O bf16 [B, H, d] and Kcache, Vcache
- * bf16 [B, H_kv, L, d].  One CTA per (batch, K/V head, up to 8 query heads of
- * its group, split) streams its K/V chunk once for all of those query heads.
+ * bf16 [B, H_kv, L, d].  One CTA per (batch, K/V head, up to 16 query heads of
+ * its group, split) streams its K/V chunk once for all of those query heads,
+ * which form the rows of tensor-core products against each K/V tile.
  * Uses the library-owned workspace of attn_decode (same size rule, same
  * stream caveats); H_kv == H is attn_decode.
  * attn_decode_gqa_ws — the same with a caller-owned workspace of at least
@@ -176,6 +177,55 @@ attn_status attn_decode_paged(const void *q, const void *K_pages, const void *V_
                               const int *block_table, const int *seq_lens, void *O, int B, int H,
                               int H_kv, int num_pages, int page_size, int max_blocks, int d,
                               float scale, cudaStream_t stream);
+
+/*
+ * attn_bwd — gradients of attn_fwd with respect to Q, K and V ("Why Fast GPUs
+ * Still Wait for Memory", section "FlashAttention is an IO algorithm": the
+ * backward pass keeps the tiling and recomputes S from Q and K instead of
+ * storing it).  With the forward's output O and log-sum-exp LSE:
+ *     P  = exp(scale Q K^T - LSE)      (causal mask as attn_fwd)
+ *     dV = P^T dO,   dP = dO V^T,   dS = P * (dP - rowsum(dO * O))
+ *     dQ = scale dS K,   dK = scale dS^T Q
+ *
+ *   Q, O, dO, dQ : bf16 [B, H, N, d], contiguous, 16-byte aligned.
+ *   K, V, dK, dV : bf16 [B, H, N, d] (attn_bwd_gqa: [B, H_kv, N, d]).
+ *   LSE          : fp32 [B, H, N], natural log, as attn_fwd wrote it
+ *                  (4-byte aligned).
+ *   scale, causal: those of the forward call.
+ *
+ * dQ, dK and dV are overwritten (never accumulated into) and must not overlap
+ * any input.  Three launches on `stream`: a row pass (rowsum(dO * O) and LSE
+ * in base 2 into the workspace), a dK/dV kernel (one CTA per K/V head and
+ * 128-key tile) and a dQ kernel (one CTA per query head and 128-query tile).
+ * No atomics: results are identical from run to run.  The workspace
+ * (attn_bwd_workspace_bytes) is library-owned and grow-only as for
+ * attn_decode, with the same synchronisation and stream caveats; it is not
+ * shared with the decode workspace.  Validation and errors as attn_fwd.
+ */
+attn_status attn_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                     const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int N, int d,
+                     float scale, int causal, cudaStream_t stream);
+
+/*
+ * attn_bwd_gqa — attn_bwd with H_kv K/V heads (1 <= H_kv, H % H_kv == 0, else
+ * ATTN_ERR_SHAPE): K, V, dK, dV are [B, H_kv, N, d] and the gradient of a
+ * K/V head sums those of the g = H / H_kv query heads that read it.
+ * attn_bwd_gqa_ws — the same with a caller-owned workspace of at least
+ * attn_bwd_workspace_bytes(B, H, N, d) bytes, 16-byte aligned (ATTN_ERR_NOMEM
+ * if smaller); it is only used while the call's launches run.
+ */
+attn_status attn_bwd_gqa(const void *Q, const void *K, const void *V, const void *O,
+                         const void *dO, const float *LSE, void *dQ, void *dK, void *dV, int B,
+                         int H, int H_kv, int N, int d, float scale, int causal,
+                         cudaStream_t stream);
+attn_status attn_bwd_gqa_ws(const void *Q, const void *K, const void *V, const void *O,
+                            const void *dO, const float *LSE, void *dQ, void *dK, void *dV, int B,
+                            int H, int H_kv, int N, int d, float scale, int causal, void *ws,
+                            size_t ws_bytes, cudaStream_t stream);
+
+/* Bytes of workspace the backward needs: 2 * B * H * ceil(N/128) * 128 * 4
+ * (0 if the shape is invalid). */
+size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
 
 /*
  * attn_decode_noalloc — attn_decode for callers that cannot allocate device
