@@ -39,6 +39,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cmath>
 
 #include "internal.h"
@@ -52,7 +53,6 @@ constexpr int kThreads = 320;
 constexpr int kComputeWarps = 8;
 constexpr int kWarpMMA = 8;
 constexpr int kWarpTMA = 9;
-constexpr int kStages = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kBoxBytes = 64 * BT * 2;    // one TMA box: 64 columns x 128 rows bf16
 constexpr float kLog2e = 1.44269504088896340736f;
@@ -73,9 +73,10 @@ struct CfgKV {
   static constexpr uint32_t ST_DELTA = 2 * TILE + 512;  // 128 fp32
   static constexpr uint32_t STAGE_BYTES = 2 * TILE + 1024;
   static constexpr uint32_t STAGE_TX = 2 * TILE + 1024;
-  static constexpr uint32_t OFF_BAR = OFF_STAGE + kStages * STAGE_BYTES;
-  // kv, full[2], empty[2], s, dp, p, done, drain
-  static constexpr int NBAR = 1 + 2 * kStages + 5;
+  static constexpr int NST = (D == 64) ? 4 : 2;          // query-tile ring depth
+  static constexpr uint32_t OFF_BAR = OFF_STAGE + NST * STAGE_BYTES;
+  // kv, full[NST], empty[NST], s[2], dp[2], p[2], done, drain
+  static constexpr int NBAR = 1 + 2 * NST + 8;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;   // tmem slot, abort flag
   // At least 116 KB so that one CTA runs per SM: each allocates all 512 TMEM
@@ -90,21 +91,23 @@ struct CfgKV {
   static_assert(TM_DPT + BT <= kTmemCols, "tensor memory budget");
 };
 
-// dQ kernel: shared memory Q | dO | stages (K, V); TMEM S (dS) | dP | dQ.
+// dQ kernel: shared memory = a ring of (K, V) tiles; TMEM S (dS) | dP | dQ |
+// Q | dO.  The query tile's Q and dO sit in TMEM as the A operands of
+// S = Q K^T and dP = dO V^T, so those products read only K / V from shared
+// memory (half the shared-memory operand traffic of two SS products).
 template <int D>
 struct CfgQ {
   static_assert(D == 64 || D == 128, "head dimension");
   static constexpr int KB = D / 64;
   static constexpr uint32_t TILE = BT * D * 2;
-  static constexpr uint32_t OFF_Q = 0;
-  static constexpr uint32_t OFF_DO = TILE;
-  static constexpr uint32_t OFF_STAGE = 2 * TILE;
+  static constexpr uint32_t OFF_STAGE = 0;
   static constexpr uint32_t ST_K = 0;
   static constexpr uint32_t ST_V = TILE;
   static constexpr uint32_t STAGE_BYTES = 2 * TILE;
-  static constexpr uint32_t OFF_BAR = OFF_STAGE + kStages * STAGE_BYTES;
-  // q, full[2], empty[2], s, dp, p, done, drain
-  static constexpr int NBAR = 1 + 2 * kStages + 5;
+  static constexpr int NST = (D == 64) ? 4 : 3;          // K/V ring depth
+  static constexpr uint32_t OFF_BAR = OFF_STAGE + NST * STAGE_BYTES;
+  // q (Q, dO in TMEM), full[NST], empty[NST], s[2], dp[2], p[2], done, drain
+  static constexpr int NBAR = 1 + 2 * NST + 8;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;
   static constexpr uint32_t SMEM_ALLOC =
@@ -113,45 +116,63 @@ struct CfgQ {
   static constexpr uint32_t TM_S = 0;
   static constexpr uint32_t TM_DP = BT;
   static constexpr uint32_t TM_DQ = 2 * BT;
-  static_assert(TM_DQ + D <= kTmemCols, "tensor memory budget");
+  static constexpr uint32_t TM_Q = 2 * BT + D;           // bf16 pairs: D / 2 columns
+  static constexpr uint32_t TM_DO = TM_Q + D / 2;
+  static_assert(TM_DO + D / 2 <= kTmemCols, "tensor memory budget");
 };
 
 // ------------------------------------------------------------------ prep
-// One warp per (head, padded row): delta = sum_k dO O (fp32) and L log2(e).
+// delta = sum_k dO O (fp32) and L log2(e) per (head, padded row).  D / 8
+// threads per row, 16-byte loads, two rows per thread (both loads issued
+// before either is used).
+constexpr int kPrepThreads = 256;
 template <int D>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kPrepThreads)
     attn_bwd_prep_kernel(const __nv_bfloat16 *__restrict__ O, const __nv_bfloat16 *__restrict__ dO,
                          const float *__restrict__ LSE, float *__restrict__ lse2,
-                         float *__restrict__ delta, int N, int N_pad, long long rows) {
-  const long long r = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (r >= rows) return;
-  const long long bh = r / N_pad;
-  const int i = static_cast<int>(r % N_pad);
-  if (i >= N) {
-    if (lane == 0) {
-      lse2[r] = INFINITY;
-      delta[r] = 0.f;
-    }
-    return;
-  }
-  const size_t base = (static_cast<size_t>(bh) * N + i) * D;
-  float acc = 0.f;
-  if constexpr (D == 128) {
-    const uint2 o = *reinterpret_cast<const uint2 *>(O + base + lane * 4);
-    const uint2 g = *reinterpret_cast<const uint2 *>(dO + base + lane * 4);
-    acc = bf16lo(o.x) * bf16lo(g.x) + bf16hi(o.x) * bf16hi(g.x) + bf16lo(o.y) * bf16lo(g.y) +
-          bf16hi(o.y) * bf16hi(g.y);
-  } else {
-    const uint32_t o = *reinterpret_cast<const uint32_t *>(O + base + lane * 2);
-    const uint32_t g = *reinterpret_cast<const uint32_t *>(dO + base + lane * 2);
-    acc = bf16lo(o) * bf16lo(g) + bf16hi(o) * bf16hi(g);
-  }
+                         float *__restrict__ delta, int N, int N_pad) {
+  constexpr int TPR = D / 8;                          // threads per row
+  constexpr int RPB = kPrepThreads / TPR;             // rows per block and pass
+  const int sub = threadIdx.x % TPR;
+  const size_t bh = blockIdx.x;                       // one head per grid row
+  const __nv_bfloat16 *Oh = O + bh * N * D;
+  const __nv_bfloat16 *dOh = dO + bh * N * D;
+  for (int i0 = static_cast<int>(blockIdx.y) * 2 * RPB; i0 < N_pad;
+       i0 += static_cast<int>(gridDim.y) * 2 * RPB) {
+    int ii[2];
+    uint4 o[2], g[2];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) {
-    delta[r] = acc;
-    lse2[r] = LSE[static_cast<size_t>(bh) * N + i] * kLog2e;
+    for (int u = 0; u < 2; ++u) {
+      ii[u] = i0 + u * RPB + static_cast<int>(threadIdx.x) / TPR;
+      o[u] = make_uint4(0, 0, 0, 0);
+      g[u] = o[u];
+      if (ii[u] < N) {
+        const size_t off = static_cast<size_t>(ii[u]) * D + sub * 8;
+        o[u] = *reinterpret_cast<const uint4 *>(Oh + off);
+        g[u] = *reinterpret_cast<const uint4 *>(dOh + off);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const uint32_t ow[4] = {o[u].x, o[u].y, o[u].z, o[u].w};
+      const uint32_t gw[4] = {g[u].x, g[u].y, g[u].z, g[u].w};
+      float acc = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        acc += bf16lo(ow[e]) * bf16lo(gw[e]) + bf16hi(ow[e]) * bf16hi(gw[e]);
+#pragma unroll
+      for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (sub == 0 && ii[u] < N_pad) {
+        const size_t r = bh * N_pad + ii[u];
+        if (ii[u] < N) {
+          delta[r] = acc;
+          lse2[r] = LSE[bh * N + ii[u]] * kLog2e;
+        } else {   // padding row: P = 0 wherever it is read
+          delta[r] = 0.f;
+          lse2[r] = INFINITY;
+        }
+      }
+    }
   }
 }
 
@@ -166,6 +187,13 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16 *dst, const uint32_t (
     st_global_v4(dst + 8 * v, pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
 }
 
+// Both kernels run two independent pipelines, one per half of the 128-wide
+// score tile (query columns 0-63 / 64-127 in the dK/dV kernel, key columns
+// in the dQ kernel).  Compute warps 4h..4h+3 own half h; the MMA warp issues
+// each half's score products (N = 64) as soon as that half's region is free
+// and each half's gradient products as soon as that half's P / dS are in.
+// While one half's warps compute, the tensor pipe works on the other half.
+
 // ------------------------------------------------------------------ dK / dV
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -177,6 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          __nv_bfloat16 *__restrict__ dV, int N, int N_pad, int H, int H_kv,
                          int n_blk, float scale_log2, float scale, unsigned *status) {
   using C = CfgKV<D>;
+  constexpr int NST = C::NST;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -203,24 +232,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar0 = sb + C::OFF_BAR;
   const uint32_t B_KV = bar0;
   auto B_FULL = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto B_EMPTY = [&](int s) { return bar0 + 8u * (1 + kStages + s); };
-  const uint32_t B_S = bar0 + 8u * (1 + 2 * kStages);
-  const uint32_t B_DP = B_S + 8;
-  const uint32_t B_P = B_S + 16;
-  const uint32_t B_DONE = B_S + 24;
-  const uint32_t B_DRAIN = B_S + 32;
+  auto B_EMPTY = [&](int s) { return bar0 + 8u * (1 + NST + s); };
+  const uint32_t bar1 = bar0 + 8u * (1 + 2 * NST);
+  auto B_S = [&](int h) { return bar1 + 8u * h; };          // S^T half h in TMEM
+  auto B_DP = [&](int h) { return bar1 + 8u * (2 + h); };   // dP^T half h in TMEM
+  auto B_P = [&](int h) { return bar1 + 8u * (4 + h); };    // P^T, dS^T half h written
+  const uint32_t B_DONE = bar1 + 48;
+  const uint32_t B_DRAIN = bar1 + 56;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
   if (threadIdx.x == kWarpTMA * 32) {
     mbar_init(B_KV, 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < NST; ++s) {
       mbar_init(B_FULL(s), 1);
       mbar_init(B_EMPTY(s), 1);
     }
-    mbar_init(B_S, 1);
-    mbar_init(B_DP, 1);
-    mbar_init(B_P, kComputeWarps);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(B_S(h), 1);
+      mbar_init(B_DP(h), 1);
+      mbar_init(B_P(h), kComputeWarps / 2);
+    }
     mbar_init(B_DONE, 1);
     mbar_init(B_DRAIN, 1);
     *abort_flag = 0;
@@ -249,9 +281,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool leader = elect_one();
     int issued = 0;
     for (int t = 0; t < n_it; ++t) {
-      const int s = t % kStages;
+      const int s = t % NST;
       if (!__all_sync(0xffffffffu,
-                      mbar_wait(B_EMPTY(s), ((t / kStages) & 1) ^ 1u, status, abort_flag)))
+                      mbar_wait(B_EMPTY(s), ((t / NST) & 1) ^ 1u, status, abort_flag)))
         break;
       if (leader) {
         const int bh = q_head(t);
@@ -270,16 +302,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (leader && *abort_flag) {
       mbar_wait_drain(B_KV, 0, 100000000ull);
-      for (int j = 0; j < kStages && j < issued; ++j) {
+      for (int j = 0; j < NST && j < issued; ++j) {
         const int tt = issued - 1 - j;
-        mbar_wait_drain(B_FULL(tt % kStages), (tt / kStages) & 1, 100000000ull);
+        mbar_wait_drain(B_FULL(tt % NST), (tt / NST) & 1, 100000000ull);
       }
     }
     __syncwarp();
   } else if (warp == kWarpMMA) {
     // ------------------------------------------------------------ MMA
     const bool leader = elect_one();
-    constexpr uint32_t kIdescS = make_idesc_bf16(BT, BT, 0, 0);
+    constexpr uint32_t kIdescS = make_idesc_bf16(BT, BT / 2, 0, 0);
     constexpr uint32_t kIdescG = make_idesc_bf16(BT, D, 0, 1);
     // Low words of the shared-memory descriptors (one common high word):
     // K-major (head dim contiguous, 16-element k-steps inside a 64-column
@@ -296,71 +328,75 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto wait_all = [&](uint32_t bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, abort_flag));
     };
-    // S^T = K Q^T and dP^T = V dO^T (both operands K-major).
-    auto issue_scores = [&](int s) {
-      const uint32_t so = (s * C::STAGE_BYTES) >> 4;
+    // Half h of S^T = K Q^T and of dP^T = V dO^T: queries 64h..64h+63 (rows
+    // 64h.. of the stage's tiles, 64 rows x 128 B = 8 KB into each box).
+    auto issue_scores = [&](int s, int h) {
+      const uint32_t so = (s * C::STAGE_BYTES + h * 64 * 128) >> 4;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t koff = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-        mma_bf16_ss_lo(tmem + C::TM_ST, k_lo + koff, stk_lo + so + (C::ST_Q >> 4) + koff, hi,
-                       kIdescS, kk > 0 ? 1u : 0u);
+        mma_bf16_ss_lo(tmem + C::TM_ST + 64 * h, k_lo + koff, stk_lo + so + (C::ST_Q >> 4) + koff,
+                       hi, kIdescS, kk > 0 ? 1u : 0u);
       }
-      mma_commit(B_S);
+      mma_commit(B_S(h));
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t koff = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-        mma_bf16_ss_lo(tmem + C::TM_DPT, v_lo + koff, stk_lo + so + (C::ST_DO >> 4) + koff, hi,
-                       kIdescS, kk > 0 ? 1u : 0u);
+        mma_bf16_ss_lo(tmem + C::TM_DPT + 64 * h, v_lo + koff, stk_lo + so + (C::ST_DO >> 4) + koff,
+                       hi, kIdescS, kk > 0 ? 1u : 0u);
       }
-      mma_commit(B_DP);
+      mma_commit(B_DP(h));
     };
-    // dV += P^T dO and dK += dS^T Q: A from TMEM (8 columns = 16 queries per
-    // step; queries 0-63 in columns 0-31, 64-127 in columns 64-95 of its
-    // region), B = the stage's dO / Q, MN-major.
-    auto issue_grads = [&](int s, bool acc) {
+    // Half h of dV += P^T dO and dK += dS^T Q: the 16-query steps 4h..4h+3,
+    // A from TMEM (8 columns per step; half h's P^T / dS^T sit in columns
+    // 64h..64h+31 of their regions), B = the stage's dO / Q, MN-major.
+    auto issue_grads = [&](int s, int h, bool acc) {
       const uint32_t so = (s * C::STAGE_BYTES) >> 4;
 #pragma unroll
-      for (int kk = 0; kk < BT / 16; ++kk) {
-        const uint32_t acol = (kk >> 2) * 64 + (kk & 3) * 8;
+      for (int u = 0; u < 4; ++u) {
+        const int kk = 4 * h + u;
         const uint32_t boff = (kk * 16 * 128) >> 4;
-        mma_bf16_ts_lo(tmem + C::TM_DV, tmem + C::TM_ST + acol,
-                       stm_lo + so + (C::ST_DO >> 4) + boff, hi, kIdescG, (acc || kk > 0) ? 1u : 0u);
+        mma_bf16_ts_lo(tmem + C::TM_DV, tmem + C::TM_ST + 64 * h + 8 * u,
+                       stm_lo + so + (C::ST_DO >> 4) + boff, hi, kIdescG, (acc || u > 0) ? 1u : 0u);
       }
 #pragma unroll
-      for (int kk = 0; kk < BT / 16; ++kk) {
-        const uint32_t acol = (kk >> 2) * 64 + (kk & 3) * 8;
+      for (int u = 0; u < 4; ++u) {
+        const int kk = 4 * h + u;
         const uint32_t boff = (kk * 16 * 128) >> 4;
-        mma_bf16_ts_lo(tmem + C::TM_DK, tmem + C::TM_DPT + acol,
-                       stm_lo + so + (C::ST_Q >> 4) + boff, hi, kIdescG, (acc || kk > 0) ? 1u : 0u);
+        mma_bf16_ts_lo(tmem + C::TM_DK, tmem + C::TM_DPT + 64 * h + 8 * u,
+                       stm_lo + so + (C::ST_Q >> 4) + boff, hi, kIdescG, (acc || u > 0) ? 1u : 0u);
       }
     };
-    bool ok = wait_all(B_KV, 0);
-    for (int t = 0; ok && t < n_it; ++t) {
-      const int s = t % kStages;
-      if (!(ok = wait_all(B_FULL(s), (t / kStages) & 1))) break;
-      if (t > 0) {
-        // The compute warps are done with S^T / dP^T of tile t-1 and have
-        // written P^T / dS^T over them: accumulate, then reuse the regions
-        // (MMAs from one thread run in issue order).
-        if (!(ok = wait_all(B_P, (t - 1) & 1))) break;
-        tc_fence_after();
-        if (leader) {
-          issue_grads((t - 1) % kStages, t > 1);
-          mma_commit(B_EMPTY((t - 1) % kStages));
-        }
-        __syncwarp();
-      }
-      tc_fence_after();
-      if (leader) issue_scores(s);
-      __syncwarp();
-    }
-    if (ok && (ok = wait_all(B_P, (n_it - 1) & 1))) {
+    bool ok = wait_all(B_KV, 0) && wait_all(B_FULL(0), 0);
+    if (ok) {
       tc_fence_after();
       if (leader) {
-        issue_grads((n_it - 1) % kStages, n_it > 1);
-        mma_commit(B_DONE);
+        issue_scores(0, 0);
+        issue_scores(0, 1);
       }
       __syncwarp();
+    }
+    for (int t = 0; ok && t < n_it; ++t) {
+      const int s = t % NST;
+      for (int h = 0; h < 2; ++h) {
+        // Half h's warps have read S^T / dP^T and written P^T / dS^T over
+        // them: accumulate, then reuse the half's regions for the next tile
+        // (MMAs from one thread run in issue order).
+        if (!(ok = wait_all(B_P(h), t & 1))) break;
+        tc_fence_after();
+        if (leader) {
+          issue_grads(s, h, t > 0 || h > 0);
+          if (h == 1) mma_commit(t + 1 < n_it ? B_EMPTY(s) : B_DONE);
+        }
+        __syncwarp();
+        if (t + 1 < n_it) {
+          if (h == 0 && !(ok = wait_all(B_FULL((t + 1) % NST), ((t + 1) / NST) & 1)))
+            break;
+          tc_fence_after();
+          if (leader) issue_scores((t + 1) % NST, h);
+          __syncwarp();
+        }
+      }
     }
     if (leader) {
       mma_commit(B_DRAIN);
@@ -370,16 +406,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // --------------------------------------------------------- compute
     const int q = warp & 3;                  // TMEM lanes 32q..32q+31 = key rows
-    const int hf = warp >> 2;                // query columns 64 hf .. 64 hf + 63
+    const int h = warp >> 2;                 // query columns 64h .. 64h + 63
     const int row = 32 * q + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
     bool ok = true;
     for (int t = 0; t < n_it; ++t) {
-      const int s = t % kStages;
+      const int s = t % NST;
       const int it = q_tile(t);
-      ok = __all_sync(0xffffffffu, mbar_wait(B_FULL(s), (t / kStages) & 1, status, abort_flag)) &&
-           __all_sync(0xffffffffu, mbar_wait(B_S, t & 1, status, abort_flag)) &&
-           __all_sync(0xffffffffu, mbar_wait(B_DP, t & 1, status, abort_flag));
+      ok = __all_sync(0xffffffffu, mbar_wait(B_FULL(s), (t / NST) & 1, status, abort_flag)) &&
+           __all_sync(0xffffffffu, mbar_wait(B_S(h), t & 1, status, abort_flag));
       if (!ok) break;
       tc_fence_after();
       const float *lse_s =
@@ -387,36 +422,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float *del_s =
           reinterpret_cast<const float *>(smem + C::OFF_STAGE + s * C::STAGE_BYTES + C::ST_DELTA);
       const bool diag = CAUSAL && it == jt;
-#pragma unroll 1
+      // P^T for the half's 64 queries while the dP^T product is still running.
+      float p[64];
+#pragma unroll
       for (int c = 0; c < 2; ++c) {
-        const int col0 = 64 * hf + 32 * c;
-        uint32_t sr[32], dp[32];
+        const int col0 = 64 * h + 32 * c;
+        uint32_t sr[32];
         tmem_ld_32cols(tmem + lane_base + C::TM_ST + col0, sr);
-        tmem_ld_32cols(tmem + lane_base + C::TM_DPT + col0, dp);
         tmem_ld_wait_regs(sr);
-        reg_fence32(dp);
-        uint32_t pk[16], dk[16];
 #pragma unroll
         for (int k = 0; k < 32; k += 4) {
           const float4 lv = *reinterpret_cast<const float4 *>(lse_s + col0 + k);
-          const float4 dv = *reinterpret_cast<const float4 *>(del_s + col0 + k);
           const float lsev[4] = {lv.x, lv.y, lv.z, lv.w};
-          const float delv[4] = {dv.x, dv.y, dv.z, dv.w};
-          float p[4], ds[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             float pe = ex2_approx(fmaf(__uint_as_float(sr[k + e]), scale_log2, -lsev[e]));
             if (diag && col0 + k + e < row) pe = 0.f;   // query before key: masked
-            p[e] = pe;
-            ds[e] = pe * (__uint_as_float(dp[k + e]) - delv[e]);
+            p[32 * c + k + e] = pe;
           }
-          pk[k / 2] = pack_bf16x2(p[0], p[1]);
-          pk[k / 2 + 1] = pack_bf16x2(p[2], p[3]);
+        }
+      }
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(B_DP(h), t & 1, status, abort_flag)))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int col0 = 64 * h + 32 * c;
+        uint32_t dp[32];
+        tmem_ld_32cols(tmem + lane_base + C::TM_DPT + col0, dp);
+        tmem_ld_wait_regs(dp);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int k = 0; k < 32; k += 4) {
+          const float4 dv = *reinterpret_cast<const float4 *>(del_s + col0 + k);
+          const float delv[4] = {dv.x, dv.y, dv.z, dv.w};
+          float ds[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            ds[e] = p[32 * c + k + e] * (__uint_as_float(dp[k + e]) - delv[e]);
+          pk[k / 2] = pack_bf16x2(p[32 * c + k], p[32 * c + k + 1]);
+          pk[k / 2 + 1] = pack_bf16x2(p[32 * c + k + 2], p[32 * c + k + 3]);
           dk[k / 2] = pack_bf16x2(ds[0], ds[1]);
           dk[k / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
         }
-        tmem_st_16cols(tmem + lane_base + C::TM_ST + 64 * hf + 16 * c, pk);
-        tmem_st_16cols(tmem + lane_base + C::TM_DPT + 64 * hf + 16 * c, dk);
+        tmem_st_16cols(tmem + lane_base + C::TM_ST + 64 * h + 16 * c, pk);
+        tmem_st_16cols(tmem + lane_base + C::TM_DPT + 64 * h + 16 * c, dk);
       }
       tmem_st_wait();
       // The stage's L / delta were read through the generic proxy and the
@@ -424,19 +473,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(B_P);
+      if (lane == 0) mbar_arrive(B_P(h));
     }
     if (ok && __all_sync(0xffffffffu, mbar_wait(B_DONE, 0, status, abort_flag))) {
       tc_fence_after();
       const int key = jt * BT + row;
-      const size_t out = (static_cast<size_t>(bkv) * N + key) * D + hf * (D / 2);
+      const size_t out = (static_cast<size_t>(bkv) * N + key) * D + h * (D / 2);
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         uint32_t r[32];
-        tmem_ld_32cols(tmem + lane_base + C::TM_DV + hf * (D / 2) + 32 * c, r);
+        tmem_ld_32cols(tmem + lane_base + C::TM_DV + h * (D / 2) + 32 * c, r);
         tmem_ld_wait_regs(r);
         if (key < N) store_row32(dV + out + 32 * c, r, 1.f);
-        tmem_ld_32cols(tmem + lane_base + C::TM_DK + hf * (D / 2) + 32 * c, r);
+        tmem_ld_32cols(tmem + lane_base + C::TM_DK + h * (D / 2) + 32 * c, r);
         tmem_ld_wait_regs(r);
         if (key < N) store_row32(dK + out + 32 * c, r, scale);
       }
@@ -453,14 +502,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------ dQ
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
-                       const __grid_constant__ CUtensorMap tmK,
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
-                       const __grid_constant__ CUtensorMap tmdO, const float *__restrict__ lse2,
-                       const float *__restrict__ delta, __nv_bfloat16 *__restrict__ dQ, int N,
-                       int N_pad, int H, int H_kv, int n_blk, float scale_log2, float scale,
-                       unsigned *status) {
+                       const __nv_bfloat16 *__restrict__ Q, const __nv_bfloat16 *__restrict__ dO,
+                       const float *__restrict__ lse2, const float *__restrict__ delta,
+                       __nv_bfloat16 *__restrict__ dQ, int N, int N_pad, int H, int H_kv,
+                       int n_blk, float scale_log2, float scale, unsigned *status) {
   using C = CfgQ<D>;
+  constexpr int NST = C::NST;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -479,39 +528,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_j = CAUSAL ? it + 1 : n_blk;
 
   const uint32_t bar0 = sb + C::OFF_BAR;
-  const uint32_t B_Q = bar0;
+  const uint32_t B_Q = bar0;   // the compute warps have put Q and dO into TMEM
   auto B_FULL = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto B_EMPTY = [&](int s) { return bar0 + 8u * (1 + kStages + s); };
-  const uint32_t B_S = bar0 + 8u * (1 + 2 * kStages);
-  const uint32_t B_DP = B_S + 8;
-  const uint32_t B_P = B_S + 16;
-  const uint32_t B_DONE = B_S + 24;
-  const uint32_t B_DRAIN = B_S + 32;
+  auto B_EMPTY = [&](int s) { return bar0 + 8u * (1 + NST + s); };
+  const uint32_t bar1 = bar0 + 8u * (1 + 2 * NST);
+  auto B_S = [&](int h) { return bar1 + 8u * h; };          // S half h in TMEM
+  auto B_DP = [&](int h) { return bar1 + 8u * (2 + h); };   // dP half h in TMEM
+  auto B_P = [&](int h) { return bar1 + 8u * (4 + h); };    // dS half h written
+  const uint32_t B_DONE = bar1 + 48;
+  const uint32_t B_DRAIN = bar1 + 56;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
   if (threadIdx.x == kWarpTMA * 32) {
-    mbar_init(B_Q, 1);
-    for (int s = 0; s < kStages; ++s) {
+    mbar_init(B_Q, kComputeWarps);
+    for (int s = 0; s < NST; ++s) {
       mbar_init(B_FULL(s), 1);
       mbar_init(B_EMPTY(s), 1);
     }
-    mbar_init(B_S, 1);
-    mbar_init(B_DP, 1);
-    mbar_init(B_P, kComputeWarps);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(B_S(h), 1);
+      mbar_init(B_DP(h), 1);
+      mbar_init(B_P(h), kComputeWarps / 2);
+    }
     mbar_init(B_DONE, 1);
     mbar_init(B_DRAIN, 1);
     *abort_flag = 0;
     fence_mbar_init();
-    tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
-    tma_prefetch_desc(&tmdO);
-    mbar_arrive_expect_tx(B_Q, 2 * C::TILE);
-    for (int kb = 0; kb < C::KB; ++kb) {
-      tma_load_3d(sb + C::OFF_Q + kb * kBoxBytes, &tmQ, kb * 64, it * BT, bh, B_Q);
-      tma_load_3d(sb + C::OFF_DO + kb * kBoxBytes, &tmdO, kb * 64, it * BT, bh, B_Q);
-    }
   }
   if (warp == kWarpMMA) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -527,9 +572,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool leader = elect_one();
     int issued = 0;
     for (int j = 0; j < n_j; ++j) {
-      const int s = j % kStages;
+      const int s = j % NST;
       if (!__all_sync(0xffffffffu,
-                      mbar_wait(B_EMPTY(s), ((j / kStages) & 1) ^ 1u, status, abort_flag)))
+                      mbar_wait(B_EMPTY(s), ((j / NST) & 1) ^ 1u, status, abort_flag)))
         break;
       if (leader) {
         const uint32_t st = sb + C::OFF_STAGE + s * C::STAGE_BYTES;
@@ -542,81 +587,83 @@ __global__ void __launch_bounds__(kThreads, 1)
       issued = j + 1;
     }
     if (leader && *abort_flag) {
-      mbar_wait_drain(B_Q, 0, 100000000ull);
-      for (int u = 0; u < kStages && u < issued; ++u) {
+      for (int u = 0; u < NST && u < issued; ++u) {
         const int jj = issued - 1 - u;
-        mbar_wait_drain(B_FULL(jj % kStages), (jj / kStages) & 1, 100000000ull);
+        mbar_wait_drain(B_FULL(jj % NST), (jj / NST) & 1, 100000000ull);
       }
     }
     __syncwarp();
   } else if (warp == kWarpMMA) {
     // ------------------------------------------------------------ MMA
     const bool leader = elect_one();
-    constexpr uint32_t kIdescS = make_idesc_bf16(BT, BT, 0, 0);
+    constexpr uint32_t kIdescS = make_idesc_bf16(BT, BT / 2, 0, 0);
     constexpr uint32_t kIdescG = make_idesc_bf16(BT, D, 0, 1);
-    const uint64_t dQ0 = make_sdesc_sw128(sb + C::OFF_Q, 16, 1024);
-    const uint32_t hi = static_cast<uint32_t>(dQ0 >> 32);
-    const uint32_t q_lo = static_cast<uint32_t>(dQ0);
-    const uint32_t do_lo = static_cast<uint32_t>(make_sdesc_sw128(sb + C::OFF_DO, 16, 1024));
-    const uint32_t stk_lo = static_cast<uint32_t>(make_sdesc_sw128(sb + C::OFF_STAGE, 16, 1024));
+    const uint64_t dst0 = make_sdesc_sw128(sb + C::OFF_STAGE, 16, 1024);
+    const uint32_t hi = static_cast<uint32_t>(dst0 >> 32);
+    const uint32_t stk_lo = static_cast<uint32_t>(dst0);
     const uint32_t stm_lo =
         static_cast<uint32_t>(make_sdesc_sw128(sb + C::OFF_STAGE, kBoxBytes, 1024));
     auto wait_all = [&](uint32_t bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, abort_flag));
     };
-    // S = Q K^T and dP = dO V^T (K-major operands).
-    auto issue_scores = [&](int s) {
-      const uint32_t so = (s * C::STAGE_BYTES) >> 4;
+    // Half h of S = Q K^T and of dP = dO V^T: keys 64h..64h+63 of the tile;
+    // Q / dO from TMEM (8 columns per 16-element step of the head dim).
+    auto issue_scores = [&](int s, int h) {
+      const uint32_t so = (s * C::STAGE_BYTES + h * 64 * 128) >> 4;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t koff = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-        mma_bf16_ss_lo(tmem + C::TM_S, q_lo + koff, stk_lo + so + (C::ST_K >> 4) + koff, hi,
-                       kIdescS, kk > 0 ? 1u : 0u);
+        mma_bf16_ts_lo(tmem + C::TM_S + 64 * h, tmem + C::TM_Q + 8 * kk,
+                       stk_lo + so + (C::ST_K >> 4) + koff, hi, kIdescS, kk > 0 ? 1u : 0u);
       }
-      mma_commit(B_S);
+      mma_commit(B_S(h));
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t koff = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-        mma_bf16_ss_lo(tmem + C::TM_DP, do_lo + koff, stk_lo + so + (C::ST_V >> 4) + koff, hi,
-                       kIdescS, kk > 0 ? 1u : 0u);
+        mma_bf16_ts_lo(tmem + C::TM_DP + 64 * h, tmem + C::TM_DO + 8 * kk,
+                       stk_lo + so + (C::ST_V >> 4) + koff, hi, kIdescS, kk > 0 ? 1u : 0u);
       }
-      mma_commit(B_DP);
+      mma_commit(B_DP(h));
     };
-    // dQ += dS K: dS from TMEM (over S), K MN-major (16-key steps).
-    auto issue_dq = [&](int s, bool acc) {
+    // Half h of dQ += dS K: key steps 4h..4h+3, dS from TMEM (columns
+    // 64h..64h+31 of the S region), K MN-major (16-key steps).
+    auto issue_dq = [&](int s, int h, bool acc) {
       const uint32_t so = (s * C::STAGE_BYTES) >> 4;
 #pragma unroll
-      for (int kk = 0; kk < BT / 16; ++kk) {
-        const uint32_t acol = (kk >> 2) * 64 + (kk & 3) * 8;
+      for (int u = 0; u < 4; ++u) {
+        const int kk = 4 * h + u;
         const uint32_t boff = (kk * 16 * 128) >> 4;
-        mma_bf16_ts_lo(tmem + C::TM_DQ, tmem + C::TM_S + acol, stm_lo + so + (C::ST_K >> 4) + boff,
-                       hi, kIdescG, (acc || kk > 0) ? 1u : 0u);
+        mma_bf16_ts_lo(tmem + C::TM_DQ, tmem + C::TM_S + 64 * h + 8 * u,
+                       stm_lo + so + (C::ST_K >> 4) + boff, hi, kIdescG, (acc || u > 0) ? 1u : 0u);
       }
     };
-    bool ok = wait_all(B_Q, 0);
-    for (int j = 0; ok && j < n_j; ++j) {
-      const int s = j % kStages;
-      if (!(ok = wait_all(B_FULL(s), (j / kStages) & 1))) break;
-      if (j > 0) {
-        if (!(ok = wait_all(B_P, (j - 1) & 1))) break;
-        tc_fence_after();
-        if (leader) {
-          issue_dq((j - 1) % kStages, j > 1);
-          mma_commit(B_EMPTY((j - 1) % kStages));
-        }
-        __syncwarp();
-      }
-      tc_fence_after();
-      if (leader) issue_scores(s);
-      __syncwarp();
-    }
-    if (ok && (ok = wait_all(B_P, (n_j - 1) & 1))) {
+    bool ok = wait_all(B_Q, 0) && wait_all(B_FULL(0), 0);
+    if (ok) {
       tc_fence_after();
       if (leader) {
-        issue_dq((n_j - 1) % kStages, n_j > 1);
-        mma_commit(B_DONE);
+        issue_scores(0, 0);
+        issue_scores(0, 1);
       }
       __syncwarp();
+    }
+    for (int j = 0; ok && j < n_j; ++j) {
+      const int s = j % NST;
+      for (int h = 0; h < 2; ++h) {
+        if (!(ok = wait_all(B_P(h), j & 1))) break;
+        tc_fence_after();
+        if (leader) {
+          issue_dq(s, h, j > 0 || h > 0);
+          if (h == 1) mma_commit(j + 1 < n_j ? B_EMPTY(s) : B_DONE);
+        }
+        __syncwarp();
+        if (j + 1 < n_j) {
+          if (h == 0 && !(ok = wait_all(B_FULL((j + 1) % NST), ((j + 1) / NST) & 1)))
+            break;
+          tc_fence_after();
+          if (leader) issue_scores((j + 1) % NST, h);
+          __syncwarp();
+        }
+      }
     }
     if (leader) {
       mma_commit(B_DRAIN);
@@ -626,56 +673,86 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // --------------------------------------------------------- compute
     const int q = warp & 3;                  // TMEM lanes 32q..32q+31 = query rows
-    const int hf = warp >> 2;                // key columns 64 hf .. 64 hf + 63
+    const int h = warp >> 2;                 // key columns 64h .. 64h + 63
     const int row = 32 * q + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
     const size_t prow = static_cast<size_t>(bh) * N_pad + static_cast<size_t>(it) * BT + row;
     const float l2 = lse2[prow];
     const float dl = delta[prow];
-    bool ok = true;
-    for (int j = 0; j < n_j; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(B_S, j & 1, status, abort_flag)) &&
-           __all_sync(0xffffffffu, mbar_wait(B_DP, j & 1, status, abort_flag));
-      if (!ok) break;
-      tc_fence_after();
-      const bool diag = CAUSAL && j == it;
-      const int kmax = N - j * BT;            // keys past the sequence are masked
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        const int col0 = 64 * hf + 32 * c;
-        uint32_t sr[32], dp[32];
-        tmem_ld_32cols(tmem + lane_base + C::TM_S + col0, sr);
-        tmem_ld_32cols(tmem + lane_base + C::TM_DP + col0, dp);
-        tmem_ld_wait_regs(sr);
-        reg_fence32(dp);
-        uint32_t dk[16];
+    {
+      // Warps of half 0 put this tile's Q rows into TMEM, warps of half 1
+      // its dO rows (row = lane, bf16 pairs along the columns; rows past N
+      // are zero).
+      const int qi = it * BT + row;
+      const __nv_bfloat16 *src = (h == 0 ? Q : dO) + (static_cast<size_t>(bh) * N + qi) * D;
 #pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          float ds[2];
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t w[32];
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int col = col0 + k + e;
-            float pe = ex2_approx(fmaf(__uint_as_float(sr[k + e]), scale_log2, -l2));
-            if ((diag && col > row) || col >= kmax) pe = 0.f;
-            ds[e] = pe * (__uint_as_float(dp[k + e]) - dl);
-          }
-          dk[k / 2] = pack_bf16x2(ds[0], ds[1]);
+        for (int v = 0; v < 8; ++v) {
+          uint4 x = make_uint4(0, 0, 0, 0);
+          if (qi < N) x = *reinterpret_cast<const uint4 *>(src + 64 * c + 8 * v);
+          w[4 * v] = x.x;
+          w[4 * v + 1] = x.y;
+          w[4 * v + 2] = x.z;
+          w[4 * v + 3] = x.w;
         }
-        tmem_st_16cols(tmem + lane_base + C::TM_S + 64 * hf + 16 * c, dk);
+        tmem_st_32cols(tmem + lane_base + (h == 0 ? C::TM_Q : C::TM_DO) + 32 * c, w);
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(B_P);
+      if (lane == 0) mbar_arrive(B_Q);
+    }
+    bool ok = true;
+    for (int j = 0; j < n_j; ++j) {
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(B_S(h), j & 1, status, abort_flag)))) break;
+      tc_fence_after();
+      const bool diag = CAUSAL && j == it;
+      const int kmax = N - j * BT;            // keys past the sequence are masked
+      float p[64];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int col0 = 64 * h + 32 * c;
+        uint32_t sr[32];
+        tmem_ld_32cols(tmem + lane_base + C::TM_S + col0, sr);
+        tmem_ld_wait_regs(sr);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int col = col0 + k;
+          float pe = ex2_approx(fmaf(__uint_as_float(sr[k]), scale_log2, -l2));
+          if ((diag && col > row) || col >= kmax) pe = 0.f;
+          p[32 * c + k] = pe;
+        }
+      }
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(B_DP(h), j & 1, status, abort_flag)))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int col0 = 64 * h + 32 * c;
+        uint32_t dp[32];
+        tmem_ld_32cols(tmem + lane_base + C::TM_DP + col0, dp);
+        tmem_ld_wait_regs(dp);
+        uint32_t dk[16];
+#pragma unroll
+        for (int k = 0; k < 32; k += 2)
+          dk[k / 2] = pack_bf16x2(p[32 * c + k] * (__uint_as_float(dp[k]) - dl),
+                                  p[32 * c + k + 1] * (__uint_as_float(dp[k + 1]) - dl));
+        tmem_st_16cols(tmem + lane_base + C::TM_S + 64 * h + 16 * c, dk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(B_P(h));
     }
     if (ok && __all_sync(0xffffffffu, mbar_wait(B_DONE, 0, status, abort_flag))) {
       tc_fence_after();
       const int qi = it * BT + row;
-      const size_t out = (static_cast<size_t>(bh) * N + qi) * D + hf * (D / 2);
+      const size_t out = (static_cast<size_t>(bh) * N + qi) * D + h * (D / 2);
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         uint32_t r[32];
-        tmem_ld_32cols(tmem + lane_base + C::TM_DQ + hf * (D / 2) + 32 * c, r);
+        tmem_ld_32cols(tmem + lane_base + C::TM_DQ + h * (D / 2) + 32 * c, r);
         tmem_ld_wait_regs(r);
         if (qi < N) store_row32(dQ + out + 32 * c, r, scale);
       }
@@ -692,7 +769,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------ host
 template <int D, bool CAUSAL>
 static cudaError_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                            const CUtensorMap &mdo, const float *lse2, const float *delta,
+                            const CUtensorMap &mdo, const void *Q, const void *dO,
+                            const float *lse2, const float *delta,
                             void *dQ, void *dK, void *dV, int B, int H, int H_kv, int N, int N_pad,
                             int n_blk, float scale, unsigned *status, cudaStream_t stream) {
   const float scale_log2 = scale * kLog2e;
@@ -710,8 +788,8 @@ static cudaError_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const 
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   kq<<<static_cast<unsigned>(B * H * n_blk), kThreads, CfgQ<D>::SMEM_ALLOC, stream>>>(
-      mq, mk, mv, mdo, lse2, delta, static_cast<__nv_bfloat16 *>(dQ), N, N_pad, H, H_kv, n_blk,
-      scale_log2, scale, status);
+      mk, mv, static_cast<const __nv_bfloat16 *>(Q), static_cast<const __nv_bfloat16 *>(dO), lse2,
+      delta, static_cast<__nv_bfloat16 *>(dQ), N, N_pad, H, H_kv, n_blk, scale_log2, scale, status);
   return cudaGetLastError();
 }
 
@@ -732,15 +810,19 @@ cudaError_t launch_bwd(const void *Q, const void *K, const void *V, const void *
   const long long rows = static_cast<long long>(B) * H * N_pad;
   float *lse2 = static_cast<float *>(ws);
   float *delta = lse2 + rows;
-  const unsigned prep_grid = static_cast<unsigned>((rows + 7) / 8);
+  // Grid: one row of blocks per head, up to 1024 blocks of 2 * 256 / (d / 8)
+  // rows each along a head (a block loops when the head is longer).
+  const int rows_per_block = 2 * kPrepThreads / (d / 8);
+  const dim3 prep_grid(static_cast<unsigned>(B * H),
+                       static_cast<unsigned>(std::min(1024, (N_pad + rows_per_block - 1) / rows_per_block)));
   if (d == 128)
-    attn_bwd_prep_kernel<128><<<prep_grid, 256, 0, stream>>>(
+    attn_bwd_prep_kernel<128><<<prep_grid, kPrepThreads, 0, stream>>>(
         static_cast<const __nv_bfloat16 *>(O), static_cast<const __nv_bfloat16 *>(dO), LSE, lse2,
-        delta, N, N_pad, rows);
+        delta, N, N_pad);
   else
-    attn_bwd_prep_kernel<64><<<prep_grid, 256, 0, stream>>>(
+    attn_bwd_prep_kernel<64><<<prep_grid, kPrepThreads, 0, stream>>>(
         static_cast<const __nv_bfloat16 *>(O), static_cast<const __nv_bfloat16 *>(dO), LSE, lse2,
-        delta, N, N_pad, rows);
+        delta, N, N_pad);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   CUtensorMap mq, mk, mv, mdo;
@@ -748,13 +830,13 @@ cudaError_t launch_bwd(const void *Q, const void *K, const void *V, const void *
       !make_bhnd_map(&mv, V, B * H_kv, N, d, BT) || !make_bhnd_map(&mdo, dO, B * H, N, d, BT))
     return cudaErrorInvalidValue;
   if (d == 128)
-    return causal ? launch_t<128, true>(mq, mk, mv, mdo, lse2, delta, dQ, dK, dV, B, H, H_kv, N,
+    return causal ? launch_t<128, true>(mq, mk, mv, mdo, Q, dO, lse2, delta, dQ, dK, dV, B, H, H_kv, N,
                                         N_pad, n_blk, scale, status, stream)
-                  : launch_t<128, false>(mq, mk, mv, mdo, lse2, delta, dQ, dK, dV, B, H, H_kv, N,
+                  : launch_t<128, false>(mq, mk, mv, mdo, Q, dO, lse2, delta, dQ, dK, dV, B, H, H_kv, N,
                                          N_pad, n_blk, scale, status, stream);
-  return causal ? launch_t<64, true>(mq, mk, mv, mdo, lse2, delta, dQ, dK, dV, B, H, H_kv, N, N_pad,
+  return causal ? launch_t<64, true>(mq, mk, mv, mdo, Q, dO, lse2, delta, dQ, dK, dV, B, H, H_kv, N, N_pad,
                                      n_blk, scale, status, stream)
-                : launch_t<64, false>(mq, mk, mv, mdo, lse2, delta, dQ, dK, dV, B, H, H_kv, N,
+                : launch_t<64, false>(mq, mk, mv, mdo, Q, dO, lse2, delta, dQ, dK, dV, B, H, H_kv, N,
                                       N_pad, n_blk, scale, status, stream);
 }
 
