@@ -62,6 +62,17 @@ def dec_work(w):
     return flops, float(nbytes)
 
 
+def bwd_work(w):
+    """Algorithmic flops and compulsory HBM bytes of one backward call: five
+    N x N x d products per head (S recomputed, dP, dV, dQ, dK), halved when
+    causal; read Q, K, V, O, dO, LSE once and write dQ, dK, dV once."""
+    flops = 10.0 * w.B * w.H * w.N * w.N * w.d * (0.5 if w.causal else 1.0)
+    q_elems = w.B * w.H * w.N * w.d
+    kv_elems = w.B * w.H_kv * w.N * w.d
+    nbytes = 4 * q_elems * 2 + 4 * kv_elems * 2 + w.B * w.H * w.N * 4
+    return flops, float(nbytes)
+
+
 def roof_time(flops, nbytes, peaks):
     return max(flops / (peaks["bf16_tflops"] * 1e12), nbytes / (peaks["hbm_gbs"] * 1e9))
 
@@ -459,7 +470,7 @@ def per_config(ea, peaks, dev, stream, reps=10):
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     out = {}
     for name in ("causal_fwd", "noncausal_fwd", "long_causal_fwd", "decode", "gqa_fwd",
-                 "gqa_decode", "paged_decode"):
+                 "gqa_decode", "paged_decode", "causal_bwd"):
         w = WORKLOADS[name]
         ins = workload_inputs(w, dev)
         gqa = w.H_kv != w.H
@@ -473,6 +484,16 @@ def per_config(ea, peaks, dev, stream, reps=10):
             o = torch.empty_like(ins[0])
             call = lambda: ea.attn_decode_paged(*ins, o, w.scale, stream)  # noqa: E731
             flops, nbytes = dec_work(w)
+        elif w.kind == "bwd":
+            # O and LSE of the forward are inputs; only the backward is timed.
+            q, k, v, do = ins
+            o = torch.empty_like(q)
+            lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+            ea.attn_fwd_gqa(q, k, v, o, lse, w.causal, w.scale, stream)
+            grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+            call = lambda: ea.attn_bwd(q, k, v, o, do, lse, *grads, w.causal, w.scale,  # noqa: E731
+                                       stream)
+            flops, nbytes = bwd_work(w)
         else:
             o = torch.empty_like(ins[0])
             fn = ea.attn_decode_gqa if gqa else ea.attn_decode
@@ -492,7 +513,7 @@ def per_config(ea, peaks, dev, stream, reps=10):
         t = statistics.median(times)
         roof = roof_time(flops, nbytes, peaks)
         rec = {"median_us": t * 1e6, "roofline_us": roof * 1e6, "frac_of_roofline": roof / t}
-        if w.kind == "fwd":
+        if w.kind in ("fwd", "bwd"):
             rec["tflops"] = flops / t / 1e12
         else:
             rec["gbs"] = nbytes / t / 1e9

@@ -35,6 +35,11 @@ def test_algorithmic_flops_and_bytes():
     f, b = bench.dec_work(WORKLOADS["gqa_decode"])
     assert f == pytest.approx(4 * 16 * 64 * 8192 * 128)
     assert b == 2 * 16 * 8 * 8192 * 128 * 2 + 2 * 16 * 64 * 128 * 2
+    # Backward: five N x N x d products per head (2.5x the forward), causal
+    # halved; Q, O, dO, dQ and K, V, dK, dV once each, plus the fp32 LSE.
+    f, b = bench.bwd_work(WORKLOADS["causal_bwd"])
+    assert f == pytest.approx(2.5 * bench.fwd_work(WORKLOADS["causal_fwd"])[0])
+    assert b == 8 * (4 * 16 * 2048 * 128) * 2 + 4 * 16 * 2048 * 4
 
 
 def test_roofline_time_takes_the_slower_roof():
