@@ -2,6 +2,8 @@
 
     python -m exact_attention_tma_gb300.profile_cases --case fwd-causal --iters 3
     python -m exact_attention_tma_gb300.profile_cases --case decode --batch 4 --iters 3
+    python -m exact_attention_tma_gb300.profile_cases --case gqa-decode --batch 4 --iters 3
+    python -m exact_attention_tma_gb300.profile_cases --case bwd-causal --batch 1 --iters 3
 
 Cases use the same shapes and seeded inputs as the bench workloads; decode
 can be run at a smaller batch so that a multi-pass Nsight Compute capture
@@ -19,7 +21,8 @@ import exact_attention_tma_gb300 as ea
 from exact_attention_tma_gb300.inputs import WORKLOADS
 
 CASES = {"fwd-causal": "causal_fwd", "fwd-noncausal": "noncausal_fwd",
-         "fwd-long-causal": "long_causal_fwd", "decode": "decode"}
+         "fwd-long-causal": "long_causal_fwd", "decode": "decode", "gqa-decode": "gqa_decode",
+         "paged-decode": "paged_decode", "bwd-causal": "causal_bwd"}
 
 
 def main(argv=None):
@@ -32,19 +35,34 @@ def main(argv=None):
     B = args.batch or w.B
     dev = torch.device("cuda", 0)
     g = torch.Generator(device=dev).manual_seed(w.seed)
+    def randn(*shape):
+        return torch.randn(shape, generator=g, device=dev).to(torch.bfloat16)
+
     if w.kind == "fwd":
         shape = (B, w.H, w.N, w.d)
-        q, k, v = (torch.randn(shape, generator=g, device=dev).to(torch.bfloat16)
-                   for _ in range(3))
+        q, k, v = (randn(*shape) for _ in range(3))
         o = torch.empty_like(q)
         lse = torch.empty(shape[:3], dtype=torch.float32, device=dev)
         call = lambda: ea.attn_fwd(q, k, v, o, lse, w.causal, w.scale)  # noqa: E731
-    else:
-        q = torch.randn((B, w.H, w.d), generator=g, device=dev).to(torch.bfloat16)
-        kc, vc = (torch.randn((B, w.H, w.N, w.d), generator=g, device=dev).to(torch.bfloat16)
-                  for _ in range(2))
+    elif w.kind == "bwd":
+        q, do = randn(B, w.H, w.N, w.d), randn(B, w.H, w.N, w.d)
+        k, v = randn(B, w.H_kv, w.N, w.d), randn(B, w.H_kv, w.N, w.d)
         o = torch.empty_like(q)
-        call = lambda: ea.attn_decode(q, kc, vc, o, w.scale)  # noqa: E731
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+        ea.attn_fwd_gqa(q, k, v, o, lse, w.causal, w.scale)
+        grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+        call = lambda: ea.attn_bwd(q, k, v, o, do, lse, *grads, w.causal, w.scale)  # noqa: E731
+    elif w.kind == "paged":
+        from exact_attention_tma_gb300.inputs import paged_decode_inputs
+
+        ins = paged_decode_inputs(B, w.H, w.N, w.d, w.page_size, w.seed, dev, w.H_kv)
+        o = torch.empty_like(ins[0])
+        call = lambda: ea.attn_decode_paged(*ins, o, w.scale)  # noqa: E731
+    else:
+        q = randn(B, w.H, w.d)
+        kc, vc = randn(B, w.H_kv, w.N, w.d), randn(B, w.H_kv, w.N, w.d)
+        o = torch.empty_like(q)
+        call = lambda: ea.attn_decode_gqa(q, kc, vc, o, w.scale)  # noqa: E731
     for _ in range(args.iters):
         call()
     torch.cuda.synchronize()
