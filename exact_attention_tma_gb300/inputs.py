@@ -63,6 +63,10 @@ WORKLOADS = {
     # Backward of the causal forward shape: Q, K, V as the forward draws them,
     # then the upstream gradient dO ~ N(0, 1).
     "causal_bwd": Workload("causal_bwd", "bwd", 4, 16, 2048, 128, True, 8),
+    # FP8 (E4M3) forward: the causal forward shapes with inputs drawn as for
+    # the bf16 forward and quantised per tensor (amax / 448 scaling).
+    "fp8_causal_fwd": Workload("fp8_causal_fwd", "fp8", 4, 16, 2048, 128, True, 9),
+    "fp8_long_causal_fwd": Workload("fp8_long_causal_fwd", "fp8", 1, 32, 16384, 128, True, 10),
 }
 
 
@@ -134,7 +138,25 @@ def bwd_inputs(B: int, H: int, N: int, d: int, seed: int, qk_std: float = 1.0,
     return q.to(device), k.to(device), v.to(device), do.to(device)
 
 
+def fp8_inputs(B: int, H: int, N: int, d: int, seed: int, device="cpu"):
+    """Q, K, V drawn as fwd_inputs draws them (fp32 N(0, 1), same order), then
+    each quantised to E4M3 with one descale factor per tensor, amax / 448
+    (the largest E4M3 value): code = round_to_nearest_even(x / descale).
+    Returns (Q8, K8, V8) as float8_e4m3fn tensors and (descale_q, descale_k,
+    descale_v)."""
+    gen = torch.Generator(device="cpu").manual_seed(seed)
+    xs = [_draw(gen, (B, H, N, d), 1.0, "normal") for _ in range(3)]
+    codes, descales = [], []
+    for x in xs:
+        ds = float(x.abs().max()) / 448.0
+        codes.append((x / ds).to(torch.float8_e4m3fn).to(device))
+        descales.append(ds)
+    return tuple(codes), tuple(descales)
+
+
 def workload_inputs(w: Workload, device="cpu"):
+    if w.kind == "fp8":
+        return fp8_inputs(w.B, w.H, w.N, w.d, w.seed, device)
     if w.kind == "bwd":
         return bwd_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_std, w.v_dist, device, w.H_kv)
     if w.kind == "fwd":

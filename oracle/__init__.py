@@ -389,6 +389,40 @@ def attention_backward(Q, K, V, dO, scale: float, causal: bool, heads=None,
     return dQh.reshape(B, H, N, d), dK, dV
 
 
+def e4m3_value(code: int) -> float:
+    """Value of one 8-bit E4M3 code (the "fn" encoding the tensor cores read
+    as e4m3): bit 7 sign, bits 6-3 exponent with bias 7, bits 2-0 mantissa.
+    Exponent field 0 is subnormal, value = mantissa/8 * 2^-6; codes 0x7F and
+    0xFF are NaN; there are no infinities (the largest finite value is 448)."""
+    sign = -1.0 if code & 0x80 else 1.0
+    e = (code >> 3) & 0xF
+    mant = code & 0x7
+    if e == 0xF and mant == 0x7:
+        return float("nan")
+    if e == 0:
+        return sign * (mant / 8.0) * 2.0 ** -6
+    return sign * (1.0 + mant / 8.0) * 2.0 ** (e - 7)
+
+
+_E4M3_TABLE = np.array([e4m3_value(c) for c in range(256)], dtype=np.float64)
+
+
+def decode_e4m3(codes) -> np.ndarray:
+    """Exact fp64 values of an array of E4M3 codes (uint8)."""
+    return _E4M3_TABLE[np.asarray(codes, dtype=np.uint8)]
+
+
+def attention_fp8(Q8, K8, V8, descale_q: float, descale_k: float, descale_v: float,
+                  scale: float, causal: bool, rows=None, heads=None, threads: int | None = None):
+    """Attention of FP8 inputs: each E4M3 code array (..., N, d) is decoded
+    exactly and multiplied by its tensor's descale factor, then the plain
+    definition (``attention``) runs on those fp64 values.  Returns O, LSE."""
+    Q = decode_e4m3(Q8) * float(descale_q)
+    K = decode_e4m3(K8) * float(descale_k)
+    V = decode_e4m3(V8) * float(descale_v)
+    return attention(Q, K, V, scale, causal, rows=rows, heads=heads, threads=threads)
+
+
 def _run(fn, n: int, threads: int | None) -> None:
     if n == 0:
         return

@@ -340,3 +340,42 @@ def test_paged_rows_follow_the_block_table():
     table = np.array([4, 0, 2])
     rows = oracle.paged_rows(pages, table, 7, 0)[:, 0]
     assert list(rows) == [12, 13, 14, 0, 1, 2, 6]
+
+
+# ---------------------------------------------------------------- FP8 (E4M3)
+def test_e4m3_decoder_matches_torch_for_every_code():
+    torch = pytest.importorskip("torch")
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.decode_e4m3(codes.numpy())
+    assert np.array_equal(np.isnan(ref), np.isnan(got))
+    keep = ~np.isnan(ref)
+    assert np.array_equal(ref[keep], got[keep])
+
+
+@pytest.mark.parametrize("code,value", [
+    (0x00, 0.0), (0x38, 1.0), (0x40, 2.0), (0x3C, 1.5), (0x7E, 448.0), (0xFE, -448.0),
+    (0x08, 2.0 ** -6), (0x01, 2.0 ** -9), (0x07, 7 * 2.0 ** -9), (0xB8, -1.0),
+])
+def test_e4m3_hand_values(code, value):
+    # Sign | exponent (bias 7) | 3-bit mantissa; exponent 0 is subnormal.
+    assert oracle.e4m3_value(code) == value
+
+
+def test_e4m3_nan_codes_and_negative_zero():
+    assert math.isnan(oracle.e4m3_value(0x7F)) and math.isnan(oracle.e4m3_value(0xFF))
+    z = oracle.e4m3_value(0x80)
+    assert z == 0.0 and math.copysign(1.0, z) == -1.0
+
+
+def test_fp8_attention_is_attention_of_the_descaled_values():
+    # Codes 0x38 (1.0) and 0x40 (2.0) with descales: every score equals
+    # scale * dq * dk * 1 * 2 * d, so P is uniform and O is the mean of V.
+    d, n = 4, 3
+    Q8 = np.full((n, d), 0x38, np.uint8)
+    K8 = np.full((n, d), 0x40, np.uint8)
+    V8 = np.array([[0x38] * d, [0x40] * d, [0x3C] * d], np.uint8)
+    O, L = oracle.attention_fp8(Q8[None], K8[None], V8[None], 0.5, 0.25, 2.0, 0.3, False)
+    assert np.allclose(O[0], np.full((n, d), 2.0 * (1.0 + 2.0 + 1.5) / 3), atol=1e-15)
+    s = 0.3 * 0.5 * 0.25 * 2.0 * d
+    assert np.allclose(L[0], s + math.log(n), atol=1e-14)
