@@ -470,7 +470,8 @@ def per_config(ea, peaks, dev, stream, reps=10):
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     out = {}
     for name in ("causal_fwd", "noncausal_fwd", "long_causal_fwd", "decode", "gqa_fwd",
-                 "gqa_decode", "paged_decode", "causal_bwd"):
+                 "gqa_decode", "paged_decode", "causal_bwd", "fp8_causal_fwd",
+                 "fp8_long_causal_fwd"):
         w = WORKLOADS[name]
         ins = workload_inputs(w, dev)
         gqa = w.H_kv != w.H
@@ -484,6 +485,14 @@ def per_config(ea, peaks, dev, stream, reps=10):
             o = torch.empty_like(ins[0])
             call = lambda: ea.attn_decode_paged(*ins, o, w.scale, stream)  # noqa: E731
             flops, nbytes = dec_work(w)
+        elif w.kind == "fp8":
+            (q8, k8, v8), ds = ins
+            o = torch.empty(q8.shape, dtype=torch.bfloat16, device=dev)
+            lse = torch.empty(q8.shape[:3], dtype=torch.float32, device=dev)
+            call = lambda: ea.attn_fwd_fp8(q8, k8, v8, o, lse, w.causal, w.scale,  # noqa: E731
+                                           *ds, stream)
+            flops, nbytes = fwd_work(w)
+            nbytes = nbytes - 3 * w.B * w.H * w.N * w.d   # 1-byte Q, K, V
         elif w.kind == "bwd":
             # O and LSE of the forward are inputs; only the backward is timed.
             q, k, v, do = ins
@@ -511,9 +520,13 @@ def per_config(ea, peaks, dev, stream, reps=10):
             b.synchronize()
             times.append(a.elapsed_time(b) / 1e3)
         t = statistics.median(times)
-        roof = roof_time(flops, nbytes, peaks)
+        if w.kind == "fp8":
+            # FP8 tensor peak: the measured bf16 peak x 2 (the nominal ratio).
+            roof = max(flops / (2 * peaks["bf16_tflops"] * 1e12), nbytes / (peaks["hbm_gbs"] * 1e9))
+        else:
+            roof = roof_time(flops, nbytes, peaks)
         rec = {"median_us": t * 1e6, "roofline_us": roof * 1e6, "frac_of_roofline": roof / t}
-        if w.kind in ("fwd", "bwd"):
+        if w.kind in ("fwd", "bwd", "fp8"):
             rec["tflops"] = flops / t / 1e12
         else:
             rec["gbs"] = nbytes / t / 1e9

@@ -62,6 +62,10 @@ def load():
             lib.attn_decode_gqa.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp]
             lib.attn_decode_gqa_ws.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
             lib.attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+            lib.attn_fwd_fp8.argtypes = [vp] * 5 + [i, i, i, i, f, f, f, f, i, vp]
+            lib.attn_fwd_fp8_ws.argtypes = [vp] * 5 + [i, i, i, i, f, f, f, f, i, vp, sz, vp]
+            lib.attn_fwd_fp8_workspace_bytes.argtypes = [i, i, i, i]
+            lib.attn_fwd_fp8_workspace_bytes.restype = sz
             lib.attn_bwd.argtypes = [vp] * 9 + [i, i, i, i, f, i, vp]
             lib.attn_bwd_gqa.argtypes = [vp] * 9 + [i, i, i, i, i, f, i, vp]
             lib.attn_bwd_gqa_ws.argtypes = [vp] * 9 + [i, i, i, i, i, f, i, vp, sz, vp]
@@ -80,7 +84,8 @@ def load():
             for fn in (lib.attn_fwd, lib.attn_decode, lib.attn_decode_ws, lib.attn_fwd_gqa,
                        lib.attn_decode_gqa, lib.attn_decode_gqa_ws, lib.attn_decode_paged,
                        lib.attn_get_device_status, lib.attn_decode_num_splits, lib.attn_bwd,
-                       lib.attn_bwd_gqa, lib.attn_bwd_gqa_ws):
+                       lib.attn_bwd_gqa, lib.attn_bwd_gqa_ws, lib.attn_fwd_fp8,
+                       lib.attn_fwd_fp8_ws):
                 fn.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -157,6 +162,37 @@ def attn_fwd_gqa(Q, K, V, O, LSE, causal: bool, scale: float, stream=None) -> No
             _dev(LSE, "LSE", torch.float32)]
     _check(load().attn_fwd_gqa(*args, B, H, H_kv, N, d, float(scale), int(bool(causal)),
                                _stream(stream)), "attn_fwd_gqa")
+
+
+def _fp8_args(Q8, K8, V8, O, LSE):
+    import torch
+
+    B, H, N, d = Q8.shape
+    for name, t in (("K8", K8), ("V8", V8)):
+        if tuple(t.shape) != (B, H, N, d):
+            raise ValueError(f"{name} shape {tuple(t.shape)} != {(B, H, N, d)}")
+    if tuple(O.shape) != (B, H, N, d):
+        raise ValueError(f"O shape {tuple(O.shape)} != {(B, H, N, d)}")
+    if tuple(LSE.shape) != (B, H, N):
+        raise ValueError(f"LSE shape {tuple(LSE.shape)} != {(B, H, N)}")
+    f8 = torch.float8_e4m3fn
+    args = [_dev(Q8, "Q8", f8), _dev(K8, "K8", f8), _dev(V8, "V8", f8),
+            _dev(O, "O", torch.bfloat16), _dev(LSE, "LSE", torch.float32)]
+    return args, B, H, N, d
+
+
+def attn_fwd_fp8(Q8, K8, V8, O, LSE, causal: bool, scale: float, descale_q: float,
+                 descale_k: float, descale_v: float, stream=None) -> None:
+    """FP8 forward: Q8, K8, V8 float8_e4m3fn [B, H, N, 128] with per-tensor
+    descale factors (value = code * descale); O bf16, LSE fp32 [B, H, N]."""
+    args, B, H, N, d = _fp8_args(Q8, K8, V8, O, LSE)
+    _check(load().attn_fwd_fp8(*args, B, H, N, d, float(scale), float(descale_q),
+                               float(descale_k), float(descale_v), int(bool(causal)),
+                               _stream(stream)), "attn_fwd_fp8")
+
+
+def attn_fwd_fp8_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(load().attn_fwd_fp8_workspace_bytes(B, H, N, d))
 
 
 def _bwd_args(Q, K, V, O, dO, LSE, dQ, dK, dV):

@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "lib")
 LIB = os.path.join(OUT_DIR, "libexact_attn.so")
 SOURCES = ["attn_api.cu", "fwd_sm103a.cu", "decode_sm103a.cu", "decode_gqa_mma_sm103a.cu",
-           "bwd_sm103a.cu", "decode_noalloc.cu", "selftest.cu"]
+           "bwd_sm103a.cu", "fwd_fp8_sm103a.cu", "decode_noalloc.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -25,6 +25,8 @@ void *g_ws_ptr[kMaxDevices];
 size_t g_ws_bytes[kMaxDevices];
 void *g_bws_ptr[kMaxDevices];      // backward row statistics (separate from decode's)
 size_t g_bws_bytes[kMaxDevices];
+void *g_fws_ptr[kMaxDevices];      // FP8 forward: V^T
+size_t g_fws_bytes[kMaxDevices];
 
 // Grow-only library workspace slot of the current device.
 attn_status grow_ws(void **slot, size_t *slot_bytes, size_t need, void **out) {
@@ -199,6 +201,65 @@ attn_status attn_decode_gqa(const void *q, const void *Kcache, const void *Vcach
 attn_status attn_decode(const void *q, const void *Kcache, const void *Vcache, void *O, int B,
                         int H, int L, int d, float scale, cudaStream_t stream) {
   return attn_decode_gqa(q, Kcache, Vcache, O, B, H, H, L, d, scale, stream);
+}
+
+size_t attn_fwd_fp8_workspace_bytes(int B, int H, int N, int d) {
+  if (check_common(B, H, N, d, 1.f) != ATTN_OK || d != 128) return 0;
+  return ea::fwd_fp8_ws_bytes(B, H, N);
+}
+
+namespace {
+attn_status check_fp8(const void *Q8, const void *K8, const void *V8, const void *O,
+                      const float *LSE, int B, int H, int N, int d, float scale, float descale_q,
+                      float descale_k, float descale_v, int causal) {
+  if (!Q8 || !K8 || !V8 || !O || !LSE) return ATTN_ERR_NULL;
+  attn_status st = check_common(B, H, N, d, scale);
+  if (st != ATTN_OK) return st;
+  if (d != 128) return ATTN_ERR_HEADDIM;
+  for (float f : {descale_q, descale_k, descale_v})
+    if (!std::isfinite(f) || !(f > 0.f)) return ATTN_ERR_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_ARG;
+  if (static_cast<long long>(B) * H * ((N + 127) / 128) >= (1LL << 31)) return ATTN_ERR_SHAPE;
+  if (misaligned(Q8) || misaligned(K8) || misaligned(V8) || misaligned(O) ||
+      (reinterpret_cast<uintptr_t>(LSE) & 3u) != 0)
+    return ATTN_ERR_ALIGN;
+  return ATTN_OK;
+}
+}  // namespace
+
+attn_status attn_fwd_fp8_ws(const void *Q8, const void *K8, const void *V8, void *O, float *LSE,
+                            int B, int H, int N, int d, float scale, float descale_q,
+                            float descale_k, float descale_v, int causal, void *ws,
+                            size_t ws_bytes, cudaStream_t stream) {
+  attn_status st = check_fp8(Q8, K8, V8, O, LSE, B, H, N, d, scale, descale_q, descale_k,
+                             descale_v, causal);
+  if (st != ATTN_OK) return st;
+  if (!ws) return ATTN_ERR_NULL;
+  if (misaligned(ws)) return ATTN_ERR_ALIGN;
+  if (ws_bytes < ea::fwd_fp8_ws_bytes(B, H, N)) return ATTN_ERR_NOMEM;
+  unsigned *status = nullptr;
+  st = status_ptr(&status);
+  if (st != ATTN_OK) return st;
+  cudaError_t e = ea::launch_fwd_fp8(Q8, K8, V8, O, LSE, B, H, N, scale, descale_q, descale_k,
+                                     descale_v, causal, ws, status, stream);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status attn_fwd_fp8(const void *Q8, const void *K8, const void *V8, void *O, float *LSE,
+                         int B, int H, int N, int d, float scale, float descale_q,
+                         float descale_k, float descale_v, int causal, cudaStream_t stream) {
+  attn_status st = check_fp8(Q8, K8, V8, O, LSE, B, H, N, d, scale, descale_q, descale_k,
+                             descale_v, causal);
+  if (st != ATTN_OK) return st;
+  int dev;
+  st = current_device(&dev);
+  if (st != ATTN_OK) return st;
+  const size_t need = ea::fwd_fp8_ws_bytes(B, H, N);
+  void *ws = nullptr;
+  st = grow_ws(&g_fws_ptr[dev], &g_fws_bytes[dev], need, &ws);
+  if (st != ATTN_OK) return st;
+  return attn_fwd_fp8_ws(Q8, K8, V8, O, LSE, B, H, N, d, scale, descale_q, descale_k, descale_v,
+                         causal, ws, need, stream);
 }
 
 size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {

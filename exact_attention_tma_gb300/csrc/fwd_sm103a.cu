@@ -716,6 +716,22 @@ bool make_bhnd_map(CUtensorMap *m, const void *base, int heads, int rows, int d,
   return fwd::make_map(m, base, heads, rows, d, box_rows);
 }
 
+bool make_bytes_map(CUtensorMap *m, const void *base, int heads, int rows, int cols,
+                    int row_stride, int box_cols, int box_rows) {
+  auto enc = fwd::encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_stride),
+                           static_cast<cuuint64_t>(row_stride) * static_cast<cuuint64_t>(rows)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 cudaError_t launch_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
                        int H, int H_kv, int N, int d, float scale, int causal, unsigned *status,
                        cudaStream_t stream) {

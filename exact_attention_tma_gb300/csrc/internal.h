@@ -21,6 +21,19 @@ cudaError_t launch_fwd(const void *Q, const void *K, const void *V, void *O, flo
 // TMA map of a bf16 [heads, rows, d] tensor (d contiguous): boxes of 64
 // columns x box_rows rows x 1 head, 128-byte swizzle, rows past `rows` read 0.
 bool make_bhnd_map(CUtensorMap *m, const void *base, int heads, int rows, int d, int box_rows);
+// TMA map of a byte tensor [heads, rows, cols] with the given row stride
+// (bytes, a multiple of 16): boxes of box_cols x box_rows x 1, 128-byte
+// swizzle; elements outside the tensor read 0.
+bool make_bytes_map(CUtensorMap *m, const void *base, int heads, int rows, int cols,
+                    int row_stride, int box_cols, int box_rows);
+
+// FP8 (E4M3) forward, d = 128: V^T into `ws` (fwd_fp8_ws_bytes), then the
+// forward kernel; O bf16, LSE fp32.
+size_t fwd_fp8_ws_bytes(int B, int H, int N);
+cudaError_t launch_fwd_fp8(const void *Q8, const void *K8, const void *V8, void *O, float *LSE,
+                           int B, int H, int N, float scale, float descale_q, float descale_k,
+                           float descale_v, int causal, void *ws, unsigned *status,
+                           cudaStream_t stream);
 
 // Device address of the current device's status word (looked up once per device).
 cudaError_t device_status_word(unsigned **out);

@@ -179,6 +179,36 @@ attn_status attn_decode_paged(const void *q, const void *K_pages, const void *V_
                               float scale, cudaStream_t stream);
 
 /*
+ * attn_fwd_fp8 — attn_fwd with 8-bit floating-point (E4M3) Q, K and V ("Why
+ * Fast GPUs Still Wait for Memory": the FP8 tensor ceiling is twice the bf16
+ * one, roofline ceiling table).  Each input is E4M3 codes [B, H, N, d] with
+ * one descale factor per tensor (value = code * descale, descale finite > 0);
+ * the scores, the softmax and the accumulators are fp32, P is rounded to E4M3
+ * (as P * 2^6, with every P <= 4) for the P V product.
+ *
+ *   Q8, K8, V8 : E4M3 [B, H, N, d], contiguous, 16-byte aligned; d == 128
+ *                (else ATTN_ERR_HEADDIM).
+ *   O          : bf16 [B, H, N, d];  LSE : fp32 [B, H, N] (natural log, with
+ *                scale and descales applied), 4-byte aligned.
+ *   scale      : multiplies the dequantised Q K^T, as in attn_fwd.
+ *
+ * Two launches on `stream`: a pass that writes V^T (d x N bytes per head)
+ * into the workspace, and the forward kernel (one CTA per head and 128-row
+ * query tile).  attn_fwd_fp8 uses a library-owned grow-only workspace (its
+ * own, same caveats as attn_decode); attn_fwd_fp8_ws takes a caller-owned one
+ * of at least attn_fwd_fp8_workspace_bytes(B, H, N, d) bytes (ATTN_ERR_NOMEM
+ * if smaller; 0 bytes is returned for an invalid shape).
+ */
+attn_status attn_fwd_fp8(const void *Q8, const void *K8, const void *V8, void *O, float *LSE,
+                         int B, int H, int N, int d, float scale, float descale_q,
+                         float descale_k, float descale_v, int causal, cudaStream_t stream);
+attn_status attn_fwd_fp8_ws(const void *Q8, const void *K8, const void *V8, void *O, float *LSE,
+                            int B, int H, int N, int d, float scale, float descale_q,
+                            float descale_k, float descale_v, int causal, void *ws,
+                            size_t ws_bytes, cudaStream_t stream);
+size_t attn_fwd_fp8_workspace_bytes(int B, int H, int N, int d);
+
+/*
  * attn_bwd — gradients of attn_fwd with respect to Q, K and V ("Why Fast GPUs
  * Still Wait for Memory", section "FlashAttention is an IO algorithm": the
  * backward pass keeps the tiling and recomputes S from Q and K instead of

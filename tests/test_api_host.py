@@ -44,7 +44,9 @@ def test_library_exports_every_declared_symbol(lib):
     assert {"attn_fwd", "attn_decode", "attn_decode_ws", "attn_get_device_status",
             "attn_status_string", "attn_decode_workspace_bytes",
             "attn_decode_num_splits", "attn_fwd_gqa", "attn_decode_gqa",
-            "attn_decode_gqa_ws", "attn_decode_paged"} <= names
+            "attn_decode_gqa_ws", "attn_decode_paged", "attn_bwd", "attn_bwd_gqa",
+            "attn_bwd_gqa_ws", "attn_bwd_workspace_bytes", "attn_fwd_fp8", "attn_fwd_fp8_ws",
+            "attn_fwd_fp8_workspace_bytes"} <= names
     for n in names:
         assert hasattr(lib, n), f"{n} declared in include/ but not exported"
 
@@ -166,3 +168,49 @@ def _paged(lib, q=P, Kp=P, Vp=P, bt=P, sl=P, O=P, B=2, H=4, H_kv=2, num_pages=8,
 ])
 def test_paged_decode_rejects_bad_arguments_before_launch(lib, kw, code):
     assert _paged(lib, **kw) == code
+
+
+def _fp8(lib, Q=P, K=P, V=P, O=P, L=P, B=1, H=2, N=300, d=128, scale=0.1, dq=0.01, dk=0.02,
+         dv=0.03, causal=1):
+    vp = ctypes.c_void_p
+    return lib.attn_fwd_fp8(vp(Q), vp(K), vp(V), vp(O), vp(L), B, H, N, d, scale, dq, dk, dv,
+                            causal, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Q=0), NULL), (dict(V=0), NULL), (dict(L=0), NULL),
+    (dict(N=0), SHAPE), (dict(B=0), SHAPE),
+    (dict(d=64), HEADDIM), (dict(d=96), HEADDIM),
+    (dict(Q=P + 8), ALIGN), (dict(O=P + 2), ALIGN), (dict(L=P + 2), ALIGN),
+    (dict(scale=0.0), ARG), (dict(dq=0.0), ARG), (dict(dk=-1.0), ARG),
+    (dict(dv=float("inf")), ARG), (dict(causal=3), ARG),
+])
+def test_fp8_fwd_rejects_bad_arguments_before_launch(lib, kw, code):
+    assert _fp8(lib, **kw) == code
+
+
+def test_fp8_workspace_bytes(lib):
+    # V^T: d x N_pad bytes per head, N_pad = N rounded up to 16.
+    assert ea.attn_fwd_fp8_workspace_bytes(2, 3, 300, 128) == 2 * 3 * 128 * 304
+    assert ea.attn_fwd_fp8_workspace_bytes(2, 3, 300, 64) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Q=0), NULL), (dict(dO=0), NULL), (dict(dV=0), NULL), (dict(LSE=0), NULL),
+    (dict(H_kv=3), SHAPE), (dict(N=0), SHAPE), (dict(d=96), HEADDIM),
+    (dict(dO=P + 8), ALIGN), (dict(dK=P + 4), ALIGN), (dict(LSE=P + 2), ALIGN),
+    (dict(scale=float("nan")), ARG), (dict(causal=2), ARG),
+])
+def test_bwd_rejects_bad_arguments_before_launch(lib, kw, code):
+    vp = ctypes.c_void_p
+    a = dict(Q=P, K=P, V=P, O=P, dO=P, LSE=P, dQ=P, dK=P, dV=P, B=1, H=4, H_kv=2, N=300, d=64,
+             scale=0.125, causal=1)
+    a.update(kw)
+    assert lib.attn_bwd_gqa(*(vp(a[k]) for k in ("Q", "K", "V", "O", "dO", "LSE", "dQ", "dK", "dV")),
+                            a["B"], a["H"], a["H_kv"], a["N"], a["d"], a["scale"], a["causal"],
+                            None) == code
+
+
+def test_bwd_workspace_bytes(lib):
+    assert ea.attn_bwd_workspace_bytes(2, 3, 300, 64) == 2 * 2 * 3 * 384 * 4
+    assert ea.attn_bwd_workspace_bytes(2, 3, 300, 96) == 0
