@@ -22,7 +22,8 @@ from exact_attention_tma_gb300.inputs import WORKLOADS
 
 CASES = {"fwd-causal": "causal_fwd", "fwd-noncausal": "noncausal_fwd",
          "fwd-long-causal": "long_causal_fwd", "decode": "decode", "gqa-decode": "gqa_decode",
-         "paged-decode": "paged_decode", "bwd-causal": "causal_bwd"}
+         "paged-decode": "paged_decode", "bwd-causal": "causal_bwd",
+         "fp8-causal": "fp8_causal_fwd", "fp8-long-causal": "fp8_long_causal_fwd"}
 
 
 def main(argv=None):
@@ -38,7 +39,15 @@ def main(argv=None):
     def randn(*shape):
         return torch.randn(shape, generator=g, device=dev).to(torch.bfloat16)
 
-    if w.kind == "fwd":
+    if w.kind == "fp8":
+        shape = (B, w.H, w.N, w.d)
+        q8, k8, v8 = (randn(*shape).float().clamp(-4, 4).to(torch.float8_e4m3fn)
+                      for _ in range(3))
+        o = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(shape[:3], dtype=torch.float32, device=dev)
+        call = lambda: ea.attn_fwd_fp8(q8, k8, v8, o, lse, w.causal, w.scale,  # noqa: E731
+                                       1.0, 1.0, 1.0)
+    elif w.kind == "fwd":
         shape = (B, w.H, w.N, w.d)
         q, k, v = (randn(*shape) for _ in range(3))
         o = torch.empty_like(q)
