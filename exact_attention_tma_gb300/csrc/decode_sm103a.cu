@@ -439,13 +439,13 @@ static cudaError_t launch_t(const void *q, const void *Kc, const void *Vc, void 
 }  // namespace dec
 
 cudaError_t launch_decode_combine(const float *ws_o, const float *ws_lse, void *O, int BH, int d,
-                                  cudaStream_t stream) {
+                                  int nsplit, cudaStream_t stream) {
   if (d == 128)
     dec::attn_decode_combine_kernel<128><<<(BH + 3) / 4, 128, 0, stream>>>(
-        ws_o, ws_lse, static_cast<__nv_bfloat16 *>(O), BH, kDecodeSplits);
+        ws_o, ws_lse, static_cast<__nv_bfloat16 *>(O), BH, nsplit);
   else
     dec::attn_decode_combine_kernel<64><<<(BH + 3) / 4, 128, 0, stream>>>(
-        ws_o, ws_lse, static_cast<__nv_bfloat16 *>(O), BH, kDecodeSplits);
+        ws_o, ws_lse, static_cast<__nv_bfloat16 *>(O), BH, nsplit);
   return cudaGetLastError();
 }
 

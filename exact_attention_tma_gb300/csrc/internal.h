@@ -49,9 +49,10 @@ cudaError_t launch_decode(const void *q, const void *Kc, const void *Vc, void *O
 cudaError_t launch_decode_gqa(const void *q, const void *Kc, const void *Vc, void *O, int B, int H,
                               int H_kv, int L, int d, float scale, void *ws, unsigned *status,
                               cudaStream_t stream);
-// The combine launch of the split-KV decode (one warp per query head).
+// The combine launch of the split-KV decode (one warp per query head):
+// partials [BH][nsplit][d] and log-sum-exps [BH][nsplit] (nsplit <= 32).
 cudaError_t launch_decode_combine(const float *ws_o, const float *ws_lse, void *O, int BH, int d,
-                                  cudaStream_t stream);
+                                  int nsplit, cudaStream_t stream);
 // Grouped-query decode on the tensor cores (mma.sync, query heads of a group
 // as the M dimension); same workspace layout.
 cudaError_t launch_decode_gqa_mma(const void *q, const void *Kc, const void *Vc, void *O, int B,

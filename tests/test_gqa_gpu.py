@@ -127,6 +127,23 @@ def test_decode_gqa_run_to_run_identical(H, H_kv):
     torch.cuda.synchronize()
 
 
+@pytest.mark.parametrize("B,H,H_kv,L,d", [(1, 16, 1, 5000, 64), (2, 8, 2, 70000, 128),
+                                          (3, 24, 1, 999, 128), (1, 64, 8, 300, 64)])
+def test_decode_gqa_writes_only_its_workspace(B, H, H_kv, L, d):
+    # The caller's workspace is exactly attn_decode_workspace_bytes long and
+    # followed by a guard region that must come back untouched.
+    q, K, V = decode_inputs(B, H, L, d, seed=L + H, device="cuda", H_kv=H_kv)
+    need = ea.attn_decode_workspace_bytes(B, H, L, d)
+    guard = 1 << 16
+    buf = torch.full((need + guard,), 0x5A, dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(q)
+    ea.attn_decode_gqa_ws(q, K, V, o, d ** -0.5, buf[:need])
+    torch.cuda.synchronize()
+    assert bool((buf[need:] == 0x5A).all())
+    O_ref, _ = oracle.decode_gqa(to_f64(q), to_f64(K), to_f64(V), d ** -0.5)
+    _assert_close(o, O_ref)
+
+
 def test_decode_gqa_with_caller_workspace_matches():
     q, K, V = decode_inputs(2, 16, 700, 128, seed=3, device="cuda", H_kv=4)
     o1 = _dec(q, K, V, 0.1)
