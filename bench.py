@@ -472,7 +472,7 @@ def per_config(ea, peaks, dev, stream, reps=10):
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     out = {}
     for name in ("causal_fwd", "noncausal_fwd", "long_causal_fwd", "decode", "gqa_fwd",
-                 "gqa_decode", "paged_decode", "causal_bwd", "fp8_causal_fwd",
+                 "gqa_decode", "paged_decode", "paged_gqa_decode", "causal_bwd", "fp8_causal_fwd",
                  "fp8_long_causal_fwd"):
         w = WORKLOADS[name]
         ins = workload_inputs(w, dev)

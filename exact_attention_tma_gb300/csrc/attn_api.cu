@@ -315,6 +315,8 @@ attn_status attn_decode_paged(const void *q, const void *K_pages, const void *V_
       (page_size & (page_size - 1)) != 0)
     return ATTN_ERR_SHAPE;
   if (static_cast<long long>(max_blocks) * page_size > kMaxLen) return ATTN_ERR_SHAPE;
+  if (static_cast<long long>(num_pages) * (H_kv > 0 ? H_kv : 1) >= (1LL << 31))
+    return ATTN_ERR_SHAPE;
   attn_status st = check_common(B, H, max_blocks * page_size, d, scale);
   if (st != ATTN_OK) return st;
   if (H_kv < 1 || H % H_kv != 0) return ATTN_ERR_SHAPE;

@@ -66,13 +66,23 @@ struct Cfg {
   static_assert(MERGE_BYTES <= OFF_BAR, "merge buffer fits in the K/V stages");
 };
 
-template <int D>
+// Paged caches: K/V pages [num_pages, H_kv, page_size, d] seen by the tensor
+// maps as [num_pages * H_kv, page_size, d] (boxes of min(64, page_size) rows);
+// key t of sequence b is row t mod page_size of page
+// block_table[b][t / page_size]; seq_lens[b] keys are visible.
+struct PagedArgs {
+  const int *block_table;
+  const int *seq_lens;
+  int max_blocks, num_pages, log2_page;
+};
+
+template <int D, bool PAGED>
 __global__ void __launch_bounds__(kThreads)
     attn_decode_gqa_mma_kernel(const __grid_constant__ CUtensorMap tmK,
                                const __grid_constant__ CUtensorMap tmV,
                                const __nv_bfloat16 *__restrict__ q, float *__restrict__ ws_o,
                                float *__restrict__ ws_lse, int H, int H_kv, int L, int chunk,
-                               int nsplit, float scale_log2, unsigned *status) {
+                               int nsplit, float scale_log2, unsigned *status, PagedArgs pg) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -93,9 +103,23 @@ __global__ void __launch_bounds__(kThreads)
   const int nh = min(kRows, group - hc * kRows);     // query heads of this CTA
   const size_t qh0 = static_cast<size_t>(b) * H + h0;
   const int kv_head = b * H_kv + hk;                 // z coordinate of the K/V maps
-  const int lo = split * chunk;
-  const int hi = min(L, lo + chunk);
+  int Lb = L;                                        // keys of this sequence
+  if constexpr (PAGED) Lb = min(max(pg.seq_lens[b], 0), pg.max_blocks << pg.log2_page);
+  const int lo = split * chunk;                      // a multiple of kTile when PAGED
+  const int hi = min(Lb, lo + chunk);
   const int n_tiles = hi > lo ? (hi - lo + kTile - 1) / kTile : 0;
+  // Page of key `key` (a valid id, or page 0 for keys past the sequence and
+  // for ids outside [0, num_pages), which also raise the bad-input bit when
+  // the key is visible).
+  auto page_of = [&](int key, bool flag) {
+    if (key >= Lb) return 0;
+    const int p = pg.block_table[static_cast<size_t>(b) * pg.max_blocks + (key >> pg.log2_page)];
+    if (p < 0 || p >= pg.num_pages) {
+      if (flag) atomicOr(status, kStatusBadInputBit);
+      return 0;
+    }
+    return p;
+  };
 
   auto B_FULL = [&](int s) { return sb + C::OFF_BAR + 8u * s; };
   auto B_EMPTY = [&](int s) { return sb + C::OFF_BAR + 8u * (kStages + s); };
@@ -125,12 +149,30 @@ __global__ void __launch_bounds__(kThreads)
         break;
       if (leader) {
         mbar_arrive_expect_tx(B_FULL(s), 2 * C::TILE_BYTES);
+        if constexpr (PAGED) {
+          // 64 / rows sub-boxes of `rows` keys, each inside one page; a sub-box
+          // of r rows lands r x 128 bytes into the 128-byte-swizzled box, a
+          // multiple of the 1024-byte swizzle atom (rows >= 8).
+          const int rows = min(kTile, 1 << pg.log2_page);
+          for (int sub = 0; sub < kTile / rows; ++sub) {
+            const int key = lo + t * kTile + sub * rows;
+            const int z = page_of(key, false) * H_kv + hk;
+            const int y = key & ((1 << pg.log2_page) - 1);
 #pragma unroll
-        for (int kb = 0; kb < C::KB; ++kb) {
-          tma_load_3d(sb + C::OFF_K + s * C::TILE_BYTES + kb * C::BOX_BYTES, &tmK, kb * 64,
-                      lo + t * kTile, kv_head, B_FULL(s));
-          tma_load_3d(sb + C::OFF_V + s * C::TILE_BYTES + kb * C::BOX_BYTES, &tmV, kb * 64,
-                      lo + t * kTile, kv_head, B_FULL(s));
+            for (int kb = 0; kb < C::KB; ++kb) {
+              const uint32_t off = s * C::TILE_BYTES + kb * C::BOX_BYTES + sub * rows * 128;
+              tma_load_3d(sb + C::OFF_K + off, &tmK, kb * 64, y, z, B_FULL(s));
+              tma_load_3d(sb + C::OFF_V + off, &tmV, kb * 64, y, z, B_FULL(s));
+            }
+          }
+        } else {
+#pragma unroll
+          for (int kb = 0; kb < C::KB; ++kb) {
+            tma_load_3d(sb + C::OFF_K + s * C::TILE_BYTES + kb * C::BOX_BYTES, &tmK, kb * 64,
+                        lo + t * kTile, kv_head, B_FULL(s));
+            tma_load_3d(sb + C::OFF_V + s * C::TILE_BYTES + kb * C::BOX_BYTES, &tmV, kb * 64,
+                        lo + t * kTile, kv_head, B_FULL(s));
+          }
         }
       }
       issued = t + 1;
@@ -187,13 +229,26 @@ __global__ void __launch_bounds__(kThreads)
       // Online softmax on the fragments: keys past the split (or the cache)
       // are masked; each row's max over the quad of lanes holding it.
       const int key0 = lo + t * kTile + warp * 16;
+      int lim = hi;
+      if constexpr (PAGED) {
+        // This warp's 16 keys share one page (page_size >= 16): skip them all
+        // if its id is invalid (the producer loaded page 0 in its place).
+        if (key0 < hi) {
+          const int p = pg.block_table[static_cast<size_t>(b) * pg.max_blocks +
+                                       (key0 >> pg.log2_page)];
+          if (p < 0 || p >= pg.num_pages) {
+            if (lane == 0) atomicOr(status, kStatusBadInputBit);
+            lim = key0;
+          }
+        }
+      }
       float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
       for (int j = 0; j < 2; ++j)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int key = key0 + 8 * j + 2 * t4 + (e & 1);
-          c[j][e] = key < hi ? c[j][e] * scale_log2 : -INFINITY;
+          c[j][e] = key < lim ? c[j][e] * scale_log2 : -INFINITY;
           mx[e >> 1] = fmaxf(mx[e >> 1], c[j][e]);
         }
       uint32_t pa[4];
@@ -308,15 +363,24 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-template <int D>
+template <int D, bool PAGED>
 static cudaError_t launch_t(const void *q, const void *Kc, const void *Vc, void *O, int B, int H,
                             int H_kv, int L, float scale_log2, void *ws, unsigned *status,
-                            cudaStream_t stream) {
+                            const PagedArgs &pg, cudaStream_t stream) {
   using C = Cfg<D>;
   CUtensorMap mk, mv;
-  if (!make_bhnd_map(&mk, Kc, B * H_kv, L, D, kTile) || !make_bhnd_map(&mv, Vc, B * H_kv, L, D, kTile))
-    return cudaErrorInvalidValue;
-  auto kern = attn_decode_gqa_mma_kernel<D>;
+  if constexpr (PAGED) {
+    const int ps = 1 << pg.log2_page;
+    const int rows = ps < kTile ? ps : kTile;
+    if (!make_bhnd_map(&mk, Kc, pg.num_pages * H_kv, ps, D, rows) ||
+        !make_bhnd_map(&mv, Vc, pg.num_pages * H_kv, ps, D, rows))
+      return cudaErrorInvalidValue;
+  } else {
+    if (!make_bhnd_map(&mk, Kc, B * H_kv, L, D, kTile) ||
+        !make_bhnd_map(&mv, Vc, B * H_kv, L, D, kTile))
+      return cudaErrorInvalidValue;
+  }
+  auto kern = attn_decode_gqa_mma_kernel<D, PAGED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(C::SMEM_ALLOC));
   if (e != cudaSuccess) return e;
@@ -328,13 +392,14 @@ static cudaError_t launch_t(const void *q, const void *Kc, const void *Vc, void 
   const long long units = static_cast<long long>(B) * H_kv * ((group + kRows - 1) / kRows);
   const int nsplit = choose_splits(units, L, n_sm);
   if (nsplit < 1 || nsplit > kDecodeSplits) return cudaErrorInvalidValue;
-  const int chunk = (L + nsplit - 1) / nsplit;
+  int chunk = (L + nsplit - 1) / nsplit;
+  if (PAGED) chunk = (chunk + kTile - 1) / kTile * kTile;   // tiles start on 64-key rows
   float *ws_o = static_cast<float *>(ws);
   float *ws_lse = ws_o + static_cast<size_t>(BH) * nsplit * D;
   const long long grid = units * nsplit;
   kern<<<static_cast<unsigned>(grid), kThreads, C::SMEM_ALLOC, stream>>>(
       mk, mv, static_cast<const __nv_bfloat16 *>(q), ws_o, ws_lse, H, H_kv, L, chunk, nsplit,
-      scale_log2, status);
+      scale_log2, status, pg);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_decode_combine(ws_o, ws_lse, O, BH, D, nsplit, stream);
@@ -346,9 +411,27 @@ cudaError_t launch_decode_gqa_mma(const void *q, const void *Kc, const void *Vc,
                                   int H, int H_kv, int L, int d, float scale, void *ws,
                                   unsigned *status, cudaStream_t stream) {
   const float scale_log2 = scale * 1.44269504088896340736f;
+  const decm::PagedArgs none{};
   if (d == 128)
-    return decm::launch_t<128>(q, Kc, Vc, O, B, H, H_kv, L, scale_log2, ws, status, stream);
-  return decm::launch_t<64>(q, Kc, Vc, O, B, H, H_kv, L, scale_log2, ws, status, stream);
+    return decm::launch_t<128, false>(q, Kc, Vc, O, B, H, H_kv, L, scale_log2, ws, status, none,
+                                      stream);
+  return decm::launch_t<64, false>(q, Kc, Vc, O, B, H, H_kv, L, scale_log2, ws, status, none,
+                                   stream);
+}
+
+cudaError_t launch_decode_paged_mma(const void *q, const void *K_pages, const void *V_pages,
+                                    const int *block_table, const int *seq_lens, void *O, int B,
+                                    int H, int H_kv, int num_pages, int log2_page, int max_blocks,
+                                    int d, float scale, void *ws, unsigned *status,
+                                    cudaStream_t stream) {
+  const float scale_log2 = scale * 1.44269504088896340736f;
+  const decm::PagedArgs pg{block_table, seq_lens, max_blocks, num_pages, log2_page};
+  const int L = max_blocks << log2_page;
+  if (d == 128)
+    return decm::launch_t<128, true>(q, K_pages, V_pages, O, B, H, H_kv, L, scale_log2, ws, status,
+                                     pg, stream);
+  return decm::launch_t<64, true>(q, K_pages, V_pages, O, B, H, H_kv, L, scale_log2, ws, status,
+                                  pg, stream);
 }
 
 }  // namespace ea

@@ -503,6 +503,10 @@ cudaError_t launch_decode_paged(const void *q, const void *K_pages, const void *
   const float scale_log2 = scale * 1.44269504088896340736f;
   int log2_page = 0;
   while ((1 << log2_page) < page_size) ++log2_page;
+  // Grouped heads on pages of at least 16 tokens: the tensor-core kernel.
+  if (H_kv < H && page_size >= 16)
+    return launch_decode_paged_mma(q, K_pages, V_pages, block_table, seq_lens, O, B, H, H_kv,
+                                   num_pages, log2_page, max_blocks, d, scale, ws, status, stream);
   const dec::Paging pg{block_table, seq_lens, max_blocks, num_pages, log2_page, status};
   // L bounds the split size only for the host's grid; each CTA recomputes it
   // from its sequence's length.

@@ -58,6 +58,12 @@ cudaError_t launch_decode_combine(const float *ws_o, const float *ws_lse, void *
 cudaError_t launch_decode_gqa_mma(const void *q, const void *Kc, const void *Vc, void *O, int B,
                                   int H, int H_kv, int L, int d, float scale, void *ws,
                                   unsigned *status, cudaStream_t stream);
+// The same kernel on a paged cache (page_size = 2^log2_page >= 16).
+cudaError_t launch_decode_paged_mma(const void *q, const void *K_pages, const void *V_pages,
+                                    const int *block_table, const int *seq_lens, void *O, int B,
+                                    int H, int H_kv, int num_pages, int log2_page, int max_blocks,
+                                    int d, float scale, void *ws, unsigned *status,
+                                    cudaStream_t stream);
 
 // Backward: row statistics (2 fp32 per padded query row) in `ws`, then the
 // dK/dV and dQ kernels, all on `stream`.

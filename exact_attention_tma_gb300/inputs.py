@@ -60,6 +60,9 @@ WORKLOADS = {
     # page pool (one block table per sequence, all sequences full length).
     "paged_decode": Workload("paged_decode", "paged", 16, 32, 8192, 128, False, 7, nsplit=32,
                              page_size=64),
+    # The grouped-query decode shape on a paged cache (64-token pages).
+    "paged_gqa_decode": Workload("paged_gqa_decode", "paged", 16, 64, 8192, 128, False, 12,
+                                 nsplit=32, H_kv=8, page_size=64),
     # Backward of the causal forward shape: Q, K, V as the forward draws them,
     # then the upstream gradient dO ~ N(0, 1).
     "causal_bwd": Workload("causal_bwd", "bwd", 4, 16, 2048, 128, True, 8),

@@ -41,7 +41,7 @@ def _assert_close(o, O_ref):
 
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("H,H_kv", [(4, 4), (8, 2), (8, 1)])
-@pytest.mark.parametrize("page_size", [1, 16, 64, 256])
+@pytest.mark.parametrize("page_size", [1, 16, 32, 64, 256])
 def test_paged_small_full(page_size, H, H_kv, d):
     B, L = 3, 700
     lens = [700, 1, 333]
@@ -92,6 +92,43 @@ def test_bad_page_id_is_reported_not_dereferenced():
     table[0, 0] = 1
     ea.attn_decode_paged(q, Kp, Vp, table, sl, o, 0.125)
     assert ea.attn_get_device_status() == 0
+
+
+@pytest.mark.parametrize("page_size", [16, 64])
+def test_grouped_bad_page_is_skipped_and_reported(page_size):
+    # Grouped heads take the tensor-core path: a bad id in sequence 0's first
+    # block drops that block's tokens there, sequence 1 is untouched, and the
+    # call reports ATTN_ERR_ARG.
+    B, H, H_kv, L, d = 2, 8, 2, 300, 128
+    q, Kp, Vp, table, sl = paged_decode_inputs(B, H, L, d, page_size, seed=13, device="cuda",
+                                               H_kv=H_kv)
+    tab = table.cpu().numpy().copy()
+    table[0, 0] = -3
+    o = torch.empty_like(q)
+    ea.attn_decode_paged(q, Kp, Vp, table, sl, o, 0.1)
+    assert ea.attn_get_device_status() == ea.ATTN_ERR_ARG
+    O1, _ = oracle.decode_paged(to_f64(q[1:]), to_f64(Kp), to_f64(Vp), tab[1:], np.array([L]), 0.1)
+    _assert_close(o[1:], O1)
+    rows = np.concatenate([np.arange(page_size * blk, min(L, page_size * (blk + 1)))
+                           for blk in range(1, tab.shape[1])])
+    K0 = np.stack([oracle.paged_rows(to_f64(Kp), tab[0], L, kh)[rows] for kh in range(H_kv)])
+    V0 = np.stack([oracle.paged_rows(to_f64(Vp), tab[0], L, kh)[rows] for kh in range(H_kv)])
+    O0, _ = oracle.decode_gqa(to_f64(q[:1]), K0[None], V0[None], 0.1)
+    _assert_close(o[:1], O0)
+
+
+def test_paged_gqa_workload_sampled():
+    w = WORKLOADS["paged_gqa_decode"]
+    q, Kp, Vp, table, sl = workload_inputs(w, device="cuda")
+    o = _run(q, Kp, Vp, table, sl, w.scale)
+    tab = table.cpu().numpy()
+    for flat in [0, 7, 8, 63, 64 * 5 + 33, w.B * w.H - 1]:
+        b, h = divmod(flat, w.H)
+        kh = oracle.kv_head_of(h, w.H, w.H_kv)
+        O_ref, _ = oracle.decode_paged(to_f64(q[b:b + 1, h:h + 1]), to_f64(Kp[:, kh:kh + 1]),
+                                       to_f64(Vp[:, kh:kh + 1]), tab[b:b + 1],
+                                       np.array([int(sl[b])]), w.scale)
+        _assert_close(o[b:b + 1, h:h + 1], O_ref)
 
 
 def test_paged_workload_sampled():
