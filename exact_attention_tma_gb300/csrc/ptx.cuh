@@ -288,14 +288,6 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t (&r)[4
                : "r"(addr)
                : "memory");
 }
-// Four 8x8 b16 matrices to shared memory: lane i supplies the address of row
-// i % 8 of matrix i / 8; lane l's register m holds row l / 4, columns 2 (l % 4)
-// and 2 (l % 4) + 1 of matrix m (the ldmatrix fragment layout).
-__device__ __forceinline__ void stmatrix_x4(uint32_t addr, const uint32_t (&r)[4]) {
-  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
-               : "memory");
-}
 // C[16x8] (+)= A[16x16] B[16x8], bf16 inputs, fp32 accumulate (A row-major,
 // B column-major fragments; lane l holds rows l/4 and l/4 + 8 of A and C).
 __device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
