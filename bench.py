@@ -591,8 +591,10 @@ def main(argv=None):
     ap.add_argument("--cpu-baseline-fwd-heads", type=int, default=64)
     ap.add_argument("--cpu-baseline-dec-heads", type=int, default=128)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--per-config", action="store_true",
-                    help="also time every performance workload on its own")
+    ap.add_argument("--per-config", dest="per_config", action="store_true", default=True,
+                    help="also time every workload alone (forward, decode, grouped, paged, "
+                         "backward, FP8) with an L2 flush between launches (default)")
+    ap.add_argument("--no-per-config", dest="per_config", action="store_false")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
