@@ -776,11 +776,10 @@ static cudaError_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const 
   const float scale_log2 = scale * kLog2e;
   auto kkv = attn_bwd_dkdv_kernel<D, CAUSAL>;
   auto kq = attn_bwd_dq_kernel<D, CAUSAL>;
-  cudaError_t e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(CfgKV<D>::SMEM_ALLOC));
+  static std::atomic<unsigned long long> set_kv{0}, set_q{0};
+  cudaError_t e = smem_limit_once(kkv, static_cast<int>(CfgKV<D>::SMEM_ALLOC), set_kv);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(CfgQ<D>::SMEM_ALLOC));
+  e = smem_limit_once(kq, static_cast<int>(CfgQ<D>::SMEM_ALLOC), set_q);
   if (e != cudaSuccess) return e;
   kkv<<<static_cast<unsigned>(B * H_kv * n_blk), kThreads, CfgKV<D>::SMEM_ALLOC, stream>>>(
       mq, mk, mv, mdo, lse2, delta, static_cast<__nv_bfloat16 *>(dK),

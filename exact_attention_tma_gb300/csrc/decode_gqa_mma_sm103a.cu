@@ -381,13 +381,11 @@ static cudaError_t launch_t(const void *q, const void *Kc, const void *Vc, void 
       return cudaErrorInvalidValue;
   }
   auto kern = attn_decode_gqa_mma_kernel<D, PAGED>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(C::SMEM_ALLOC));
+  static std::atomic<unsigned long long> smem_set{0};
+  cudaError_t e = smem_limit_once(kern, static_cast<int>(C::SMEM_ALLOC), smem_set);
   if (e != cudaSuccess) return e;
   const int BH = B * H;
-  int dev = 0, n_sm = 152;
-  if (cudaGetDevice(&dev) == cudaSuccess)
-    cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+  const int n_sm = sm_count();
   const int group = H / H_kv;
   const long long units = static_cast<long long>(B) * H_kv * ((group + kRows - 1) / kRows);
   const int nsplit = choose_splits(units, L, n_sm);

@@ -460,8 +460,8 @@ static cudaError_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const 
                             void *O, float *LSE, int N, int BH, int n_blk, float scale_log2,
                             float out_mul, unsigned *status, cudaStream_t stream) {
   auto kern = attn_fwd_fp8_kernel<CAUSAL>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(SMEM_ALLOC));
+  static std::atomic<unsigned long long> smem_set{0};
+  cudaError_t e = smem_limit_once(kern, static_cast<int>(SMEM_ALLOC), smem_set);
   if (e != cudaSuccess) return e;
   kern<<<static_cast<unsigned>(BH) * n_blk, kThreads, SMEM_ALLOC, stream>>>(
       mq, mk, mvt, static_cast<__nv_bfloat16 *>(O), LSE, N, BH, n_blk, scale_log2, out_mul,

@@ -1,10 +1,38 @@
 // internal.h — launchers shared between the C-ABI layer and the kernel files.
 #pragma once
+#include <atomic>
 #include <cstddef>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace ea {
+
+// Raises `kern`'s dynamic shared-memory limit to `bytes` once per device:
+// `done` is the call site's static flag word, one bit per device ordinal.
+template <typename Kernel>
+inline cudaError_t smem_limit_once(Kernel kern, int bytes, std::atomic<unsigned long long> &done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (done.load() & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.fetch_or(bit);
+  return e;
+}
+
+// Streaming multiprocessors of the current device (looked up once per device).
+inline int sm_count() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  int n = cache[dev].load();
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+    n = 152;
+  cache[dev].store(n);
+  return n;
+}
 
 // Bits of the device status word (see attn_get_device_status).
 constexpr unsigned kStatusTimeoutBit = 1u;
