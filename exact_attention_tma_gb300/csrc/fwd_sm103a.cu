@@ -39,6 +39,15 @@
 // per key half, each half keeps its own maximum and sum, and the two are
 // merged once in the epilogue.
 //
+// FP8 instance (d = 128): Q, K and V arrive as E4M3 (V transposed, [d][keys],
+// so that P V reads a K-major B as kind::f8f6f4 requires); both products run
+// at the 8-bit rate with 32-byte k-steps, P is written to TMEM as E4M3
+// quadruples (keys 0-63 of a half in 16 columns), scaled by 2^2 so that the
+// smallest P kept (2^-8) is a normal E4M3 number, and the lazy-rescale
+// threshold drops to a half-row sum of 64 (every P <= 64, so P * 4 stays
+// below E4M3's 448).  Q_i holds half as many bytes, so O is staged in a
+// buffer of its own; the epilogue multiplies by V's descale over 2^2.
+//
 // Registers are re-balanced with setmaxnreg: 160 per softmax thread, 128 for
 // warps 8-11 and 32 for the idle warps 12-15 (256*160 + 128*128 + 128*32 =
 // 61440 of the block's launch allocation of 512 threads x 128).
@@ -87,14 +96,21 @@ constexpr float kMInit = -1.0e30f;
 #define EA_FWD_SV64 3
 #endif
 
-template <int D>
+// F8: Q, K and V are E4M3 (one byte per element) and V arrives transposed
+// (V^T tiles [d][keys], so P V reads a K-major B); P is E4M3 in TMEM.
+template <int D, bool F8 = false>
 struct Cfg {
   static_assert(D == 64 || D == 128, "head dimension");
-  static constexpr int KB = D / 64;                 // 128-byte swizzle column blocks
-  static constexpr int SK = (D == 128) ? EA_FWD_SK128 : EA_FWD_SK64;   // K ring stages
-  static constexpr int SV = (D == 128) ? EA_FWD_SV128 : EA_FWD_SV64;   // V ring stages
-  static constexpr uint32_t Q_BYTES = BM * D * 2;   // one query tile
-  static constexpr uint32_t KV_BYTES = BN * D * 2;  // one K or V tile
+  static_assert(!F8 || D == 128, "FP8 forward: d = 128");
+  static constexpr int ESZ = F8 ? 1 : 2;            // bytes per element
+  static constexpr int KB = D * ESZ / 128;          // 128-byte swizzle column blocks
+  static constexpr int BOX_COLS = 128 / ESZ;        // elements per 128-byte box row
+  static constexpr int KSTEPS = D * ESZ / 32;       // 32-byte k-steps of Q K^T
+  static constexpr int PSTEPS = BN * ESZ / 32;      // 32-byte k-steps of P V (keys)
+  static constexpr int SK = F8 ? 3 : (D == 128) ? EA_FWD_SK128 : EA_FWD_SK64;   // K ring stages
+  static constexpr int SV = F8 ? 3 : (D == 128) ? EA_FWD_SV128 : EA_FWD_SV64;   // V ring stages
+  static constexpr uint32_t Q_BYTES = BM * D * ESZ;   // one query tile
+  static constexpr uint32_t KV_BYTES = BN * D * ESZ;  // one K or V tile
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = OFF_Q + QT * Q_BYTES;
   static constexpr uint32_t OFF_V = OFF_K + SK * KV_BYTES;
@@ -104,7 +120,11 @@ struct Cfg {
   static constexpr bool kIndep = (D == 64);
   static constexpr int NPB = kIndep ? 2 : 1;        // P hand-off barriers per query tile
   static constexpr uint32_t OFF_XCH = OFF_V + SV * KV_BYTES;   // float[2][QT][2][BM]
-  static constexpr uint32_t OFF_BAR = OFF_XCH + 2 * QT * 2 * BM * 4;
+  // The epilogue stages O (bf16) in the free Q_i buffer, or with 1-byte Q in
+  // a buffer of its own.
+  static constexpr uint32_t O_TILE = BM * D * 2;
+  static constexpr uint32_t OFF_OST = OFF_XCH + 2 * QT * 2 * BM * 4;
+  static constexpr uint32_t OFF_BAR = OFF_OST + (F8 ? QT * O_TILE : 0);
   // q[QT], kf[SK], ke[SK], vf[SV], ve[SV], s[QT], p[QT][NPB], o[QT], drain
   static constexpr int NBAR = QT + 2 * SK + 2 * SV + QT + QT * NPB + QT + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
@@ -140,6 +160,29 @@ __device__ __forceinline__ void exp_chunk(const uint32_t (&sr)[32], float2 sc2, 
   }
 }
 
+// FP8 variant: P is rounded to E4M3 as P * 2^2 (nm2 = 2 - m); the lazy
+// rescale keeps every P <= 64 (a 64-key half's sum <= 64), so P * 4 <= 256
+// stays below E4M3's 448 and P >= 2^-8 stays a normal number.  Packs four
+// scores per word (key order, low byte first); adds the P * 4 to rs2.
+constexpr float kPScale8 = 4.0f;
+constexpr float kLog2PScale8 = 2.0f;
+constexpr float kRescaleSum8 = 64.0f;
+__device__ __forceinline__ void exp_chunk_f8(const uint32_t (&sr)[32], float2 sc2, float2 nm2,
+                                             uint32_t *pk, float2 (&rs2)[2]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const float2 x0 = ffma2(make_float2(__uint_as_float(sr[4 * c]), __uint_as_float(sr[4 * c + 1])),
+                            sc2, nm2);
+    const float2 x1 = ffma2(
+        make_float2(__uint_as_float(sr[4 * c + 2]), __uint_as_float(sr[4 * c + 3])), sc2, nm2);
+    const float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
+    const float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
+    rs2[0] = fadd2(rs2[0], p0);
+    rs2[1] = fadd2(rs2[1], p1);
+    pk[c] = pack_e4m3x4(p0.x, p0.y, p1.x, p1.y);
+  }
+}
+
 // Scores of keys kv0 + col0 .. kv0 + col0 + 31 that lie past the last visible
 // key lim become -inf (so p = 0).
 __device__ __forceinline__ void mask_chunk(uint32_t (&sr)[32], int first_key, int lim) {
@@ -150,14 +193,13 @@ __device__ __forceinline__ void mask_chunk(uint32_t (&sr)[32], int first_key, in
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                    __nv_bfloat16 *__restrict__ O,
                     float *__restrict__ LSE, int N, int BH, int n_blk, int H, int group,
-                    float scale_log2, unsigned *status) {
-  using C = Cfg<D>;
+                    float scale_log2, float out_mul, unsigned *status) {
+  using C = Cfg<D, F8>;
   constexpr int SK = C::SK;
   constexpr int SV = C::SV;
   extern __shared__ uint8_t smem_raw[];
@@ -204,6 +246,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Set by a softmax warp whose wait gave up, read by it and its partner warp
   // after their shared barrier (so both take the same exit).
   volatile int *pair_abort = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 16);
+  // K_j and V_j into ring stages sk / sv: 128-byte-wide column boxes of the
+  // [keys][d] tiles, or with FP8 one box of K and one box of the V^T tile
+  // [d][keys] (keys contiguous).
+  auto load_k = [&](int j, int sk) {
+#pragma unroll
+    for (int kb = 0; kb < C::KB; ++kb)
+      tma_load_3d(sb + C::OFF_K + sk * C::KV_BYTES + kb * kBoxBytes, &tmK, kb * C::BOX_COLS,
+                  j * BN, kvh, B_KF(sk));
+  };
+  auto load_v = [&](int j, int sv) {
+    const uint32_t dst = sb + C::OFF_V + sv * C::KV_BYTES;
+    if constexpr (F8) {
+      tma_load_3d(dst, &tmV, j * BN, 0, kvh, B_VF(sv));
+    } else {
+#pragma unroll
+      for (int kb = 0; kb < C::KB; ++kb)
+        tma_load_3d(dst + kb * kBoxBytes, &tmV, kb * 64, j * BN, kvh, B_VF(sv));
+    }
+  };
 
   // One thread of the TMA warp sets up the barriers and at once starts the
   // first loads, in the order the first MMAs need them (Q_0 and K_0, then Q_1
@@ -234,17 +295,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto load_q = [&](int i) {
       mbar_arrive_expect_tx(B_Q(i), C::Q_BYTES);
       for (int kb = 0; kb < C::KB; ++kb)
-        tma_load_3d(sb + C::OFF_Q + i * C::Q_BYTES + kb * kBoxBytes, &tmQ, kb * 64, q0 + i * BM,
-                    bh, B_Q(i));
+        tma_load_3d(sb + C::OFF_Q + i * C::Q_BYTES + kb * kBoxBytes, &tmQ, kb * C::BOX_COLS,
+                    q0 + i * BM, bh, B_Q(i));
     };
     load_q(0);
     mbar_arrive_expect_tx(B_KF(0), C::KV_BYTES);
-    for (int kb = 0; kb < C::KB; ++kb)
-      tma_load_3d(sb + C::OFF_K + kb * kBoxBytes, &tmK, kb * 64, 0, kvh, B_KF(0));
+    load_k(0, 0);
     for (int i = 1; i < QT; ++i) load_q(i);
     mbar_arrive_expect_tx(B_VF(0), C::KV_BYTES);
-    for (int kb = 0; kb < C::KB; ++kb)
-      tma_load_3d(sb + C::OFF_V + kb * kBoxBytes, &tmV, kb * 64, 0, kvh, B_VF(0));
+    load_v(0, 0);
   }
   if (warp == kWarpMMA) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -284,19 +343,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // their sum.  Keys 32-63 are read from TMEM while keys 0-31 are
     // exponentiated.
     auto pass = [&](uint32_t s_addr, int k0, int lm, float m_use, uint32_t (&pk)[32], float &rs) {
-      const float2 nm2 = make_float2(-m_use, -m_use);
+      const float nm = (F8 ? kLog2PScale8 : 0.f) - m_use;
+      const float2 nm2 = make_float2(nm, nm);
       float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       uint32_t a[32], b[32];
       tmem_ld_32cols(s_addr, a);
       tmem_ld_wait_regs(a);
       tmem_ld_32cols(s_addr + 32, b);
       mask_chunk(a, k0, lm);
-      exp_chunk(a, sc2, nm2, &pk[0], rs2);
+      if constexpr (F8) exp_chunk_f8(a, sc2, nm2, &pk[0], rs2);
+      else exp_chunk(a, sc2, nm2, &pk[0], rs2);
       __syncwarp();
       tmem_ld_wait_regs(b);
       mask_chunk(b, k0 + 32, lm);
-      exp_chunk(b, sc2, nm2, &pk[16], rs2);
+      if constexpr (F8) exp_chunk_f8(b, sc2, nm2, &pk[8], rs2);
+      else exp_chunk(b, sc2, nm2, &pk[16], rs2);
       rs = (rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y);
+      if constexpr (F8) rs *= 1.0f / kPScale8;
     };
     // Maximum of this thread's 64 (masked) raw scores of S_i.
     auto half_max = [&](uint32_t s_addr, int k0, int lm) {
@@ -359,10 +422,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // grew, and the tile is redone with the new one (by both halves when
         // they share the accumulator).
         bool redo;
+        constexpr float kRedo = F8 ? kRescaleSum8 : kRescaleSum;
         if (kIndep) {
-          redo = __any_sync(0xffffffffu, !(rs <= kRescaleSum));
+          redo = __any_sync(0xffffffffu, !(rs <= kRedo));
         } else {
-          redo = named_bar_any(pair_bar, 64, !okw || !(rs <= kRescaleSum));
+          redo = named_bar_any(pair_bar, 64, !okw || !(rs <= kRedo));
           if (redo && pair_abort[q]) {
             ok = false;
             break;
@@ -397,16 +461,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         l[i] = l[i] * alpha + rs;
-        // P for keys 64h .. 64h+63 (bf16 pairs) over the first 32 of this
-        // thread's own S columns, which it has already read.
-        tmem_st_32cols(s_addr, pk);
+        // P for keys 64h .. 64h+63 (bf16 pairs, or E4M3 quadruples) over the
+        // first 32 (16) of this thread's own S columns, which it has already read.
+        if constexpr (F8) tmem_st_16cols(s_addr, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
+        else tmem_st_32cols(s_addr, pk);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(B_P(i, h));
       }
     }
     // Epilogue per tile: each warp stages its half of the columns of O_i as
-    // bf16 in the (no longer needed) Q_i buffer, in the 128-byte-swizzled box
+    // bf16 in the (no longer needed) Q_i buffer (with FP8, whose Q_i is half
+    // the size, in a staging buffer of its own), in the 128-byte-swizzled box
     // layout of the O tensor map, and one thread stores the tile with TMA
     // (rows past N are dropped by the tensor map); the warp of the low half
     // writes the LSE.  Independent halves are merged with weights
@@ -432,10 +498,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         w1 = ex2_approx(xm[BM + r] - mrow);
       }
       const float lt = w0 * xl[r] + w1 * xl[BM + r];
-      const float inv_l = 1.f / lt;
+      const float inv_l = out_mul / lt;
       const float a0 = w0 * inv_l, a1 = w1 * inv_l;
       const int qrow = q0 + i * BM + r;
-      const uint32_t stage = sb + C::OFF_Q + i * C::Q_BYTES + static_cast<uint32_t>(r) * 128;
+      const uint32_t stage_base = F8 ? sb + C::OFF_OST + i * C::O_TILE : sb + C::OFF_Q + i * C::Q_BYTES;
+      const uint32_t stage = stage_base + static_cast<uint32_t>(r) * 128;
       const uint32_t o_addr = tmem + lane_addr + C::TMEM_O + (kIndep ? 2 * i * D : i * D) + h * (D / 2);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
@@ -468,8 +535,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar_sync(kEpiBar, 2 * BM);
       if (threadIdx.x == 0) {
 #pragma unroll
-        for (int kb = 0; kb < C::KB; ++kb)
-          tma_store_3d(&tmO, kb * 64, q0 + i * BM, bh, sb + C::OFF_Q + i * C::Q_BYTES + kb * kBoxBytes);
+        for (int kb = 0; kb < D / 64; ++kb)
+          tma_store_3d(&tmO, kb * 64, q0 + i * BM, bh, stage_base + kb * kBoxBytes);
         bulk_commit_group();
       }
       if (h == 0 && qrow < N) {
@@ -496,10 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         if (leader) {
           mbar_arrive_expect_tx(B_KF(sk), C::KV_BYTES);
-#pragma unroll
-          for (int kb = 0; kb < C::KB; ++kb)
-            tma_load_3d(sb + C::OFF_K + sk * C::KV_BYTES + kb * kBoxBytes, &tmK, kb * 64, j * BN,
-                        kvh, B_KF(sk));
+          load_k(j, sk);
         }
         issued_k = j + 1;
         const int sv = j % SV;
@@ -507,10 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         if (leader) {
           mbar_arrive_expect_tx(B_VF(sv), C::KV_BYTES);
-#pragma unroll
-          for (int kb = 0; kb < C::KB; ++kb)
-            tma_load_3d(sb + C::OFF_V + sv * C::KV_BYTES + kb * kBoxBytes, &tmV, kb * 64, j * BN,
-                        kvh, B_VF(sv));
+          load_v(j, sv);
         }
         issued_v = j + 1;
       }
@@ -526,15 +587,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kWarpMMA) {
       // ------------------------------------------------------- MMA issuer
       const bool leader = elect_one();
-      constexpr uint32_t kIdescQK = make_idesc_bf16(BM, BN, 0, 0);
-      constexpr uint32_t kIdescPV = make_idesc_bf16(BM, D, 0, 1);
+      // bf16: V is MN-major (head dim contiguous); FP8: V^T is K-major.
+      constexpr uint32_t kIdescQK = F8 ? make_idesc_e4m3(BM, BN, 0, 0) : make_idesc_bf16(BM, BN, 0, 0);
+      constexpr uint32_t kIdescPV = F8 ? make_idesc_e4m3(BM, D, 0, 0) : make_idesc_bf16(BM, D, 0, 1);
       // Shared-memory descriptors as low words over one common high word; a
       // k-step or stage moves only the start-address field (byte offset / 16
       // added to the low word).  The issue loops are unrolled so that each MMA
       // costs two integer adds besides the tcgen05.mma itself.
       const uint64_t dQ = make_sdesc_sw128(sb + C::OFF_Q, 16, 1024);
       const uint64_t dK = make_sdesc_sw128(sb + C::OFF_K, 16, 1024);
-      const uint64_t dV = make_sdesc_sw128(sb + C::OFF_V, kBoxBytes, 1024);
+      const uint64_t dV = F8 ? make_sdesc_sw128(sb + C::OFF_V, 16, 1024)
+                             : make_sdesc_sw128(sb + C::OFF_V, kBoxBytes, 1024);
       const uint32_t hi = static_cast<uint32_t>(dQ >> 32);   // identical for dK and dV
       const uint32_t q_lo = static_cast<uint32_t>(dQ);
       const uint32_t k_lo = static_cast<uint32_t>(dK);
@@ -547,22 +610,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a0 = q_lo + ((i * C::Q_BYTES) >> 4);
         const uint32_t b0 = k_lo + ((sk * C::KV_BYTES) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < C::KSTEPS; ++kk) {   // 32-byte k-steps, 4 per 128-byte box
           const uint32_t koff = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-          mma_bf16_ss_lo(tmem + C::TMEM_S + i * BN, a0 + koff, b0 + koff, hi, kIdescQK,
+          if constexpr (F8)
+            mma_f8_ss_lo(tmem + C::TMEM_S + i * BN, a0 + koff, b0 + koff, hi, kIdescQK,
                          kk > 0 ? 1u : 0u);
+          else
+            mma_bf16_ss_lo(tmem + C::TMEM_S + i * BN, a0 + koff, b0 + koff, hi, kIdescQK,
+                           kk > 0 ? 1u : 0u);
         }
       };
       // O += P_i V: P_i from TMEM (8 columns = 16 keys per step; keys 0-63 in
       // columns 0-31 of S_i, keys 64-127 in columns 64-95); V is MN-major
       // (head dim contiguous), 64-column blocks kBoxBytes apart, 8-key groups 1024 B apart.
       // Key steps kb..ke-1 into the accumulator at column o_col.
+      // FP8: 32 keys per step, P_i's keys 0-63 in columns 0-15 and keys
+      // 64-127 in columns 64-79 (four E4M3 per column); the V^T tile is
+      // K-major, 32-byte k-steps along its 128-byte rows.
       auto issue_pv = [&](int i, int sv, bool acc, int kb, int ke, uint32_t o_col) {
         const uint32_t b0 = v_lo + ((sv * C::KV_BYTES) >> 4);
 #pragma unroll
-        for (int kk = kb; kk < ke; ++kk)
-          mma_bf16_ts_lo(tmem + o_col, tmem + C::TMEM_S + i * BN + (kk >> 2) * 64 + (kk & 3) * 8,
-                         b0 + ((kk * 16 * 128) >> 4), hi, kIdescPV, (acc || kk > kb) ? 1u : 0u);
+        for (int kk = kb; kk < ke; ++kk) {
+          if constexpr (F8)
+            mma_f8_ts_lo(tmem + o_col, tmem + C::TMEM_S + i * BN + (kk >> 1) * 64 + (kk & 1) * 8,
+                         b0 + ((kk * 32) >> 4), hi, kIdescPV, (acc || kk > kb) ? 1u : 0u);
+          else
+            mma_bf16_ts_lo(tmem + o_col, tmem + C::TMEM_S + i * BN + (kk >> 2) * 64 + (kk & 3) * 8,
+                           b0 + ((kk * 16 * 128) >> 4), hi, kIdescPV, (acc || kk > kb) ? 1u : 0u);
+        }
       };
       // P_i V_j: one run over all 128 keys into O_i, or (independent halves)
       // keys 0-63 into O_i^0 as soon as that half's P is in, then keys 64-127
@@ -571,16 +646,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (C::kIndep) {
           if (!wait_all(B_P(i, 0), j & 1)) return false;
           tc_fence_after();
-          if (leader) issue_pv(i, sv, j > 0, 0, BN / 32, C::TMEM_O + 2 * i * D);
+          if (leader) issue_pv(i, sv, j > 0, 0, C::PSTEPS / 2, C::TMEM_O + 2 * i * D);
           __syncwarp();
           if (!wait_all(B_P(i, 1), j & 1)) return false;
           tc_fence_after();
-          if (leader) issue_pv(i, sv, j > 0, BN / 32, BN / 16, C::TMEM_O + (2 * i + 1) * D);
+          if (leader) issue_pv(i, sv, j > 0, C::PSTEPS / 2, C::PSTEPS, C::TMEM_O + (2 * i + 1) * D);
           __syncwarp();
         } else {
           if (!wait_all(B_P(i, 0), j & 1)) return false;
           tc_fence_after();
-          if (leader) issue_pv(i, sv, j > 0, 0, BN / 16, C::TMEM_O + i * D);
+          if (leader) issue_pv(i, sv, j > 0, 0, C::PSTEPS, C::TMEM_O + i * D);
           __syncwarp();
         }
         return true;
@@ -685,12 +760,13 @@ static bool make_map(CUtensorMap *m, const void *base, int BH, int N, int d, int
   return r == CUDA_SUCCESS;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool F8 = false>
 static cudaError_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                            const CUtensorMap &mo, void *O, float *LSE, int BH, int N, int H,
-                            int group, float scale_log2, unsigned *status, cudaStream_t stream) {
-  using C = Cfg<D>;
-  auto kern = attn_fwd_kernel<D, CAUSAL>;
+                            const CUtensorMap &mo, float *LSE, int BH, int N, int H, int group,
+                            float scale_log2, float out_mul, unsigned *status,
+                            cudaStream_t stream) {
+  using C = Cfg<D, F8>;
+  auto kern = attn_fwd_kernel<D, CAUSAL, F8>;
   static std::atomic<unsigned long long> configured{0};   // one bit per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -705,8 +781,7 @@ static cudaError_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const 
   const int n_blk = (N + QT * BM - 1) / (QT * BM);
   const long long grid = static_cast<long long>(BH) * n_blk;
   kern<<<static_cast<unsigned>(grid), kThreads, C::SMEM_ALLOC, stream>>>(
-      mq, mk, mv, mo, static_cast<__nv_bfloat16 *>(O), LSE, N, BH, n_blk, H, group, scale_log2,
-      status);
+      mq, mk, mv, mo, LSE, N, BH, n_blk, H, group, scale_log2, out_mul, status);
   return cudaGetLastError();
 }
 
@@ -742,12 +817,33 @@ cudaError_t launch_fwd(const void *Q, const void *K, const void *V, void *O, flo
   if (!make_map(&mq, Q, BH, N, d) || !make_map(&mk, K, B * H_kv, N, d) ||
       !make_map(&mv, V, B * H_kv, N, d) || !make_map(&mo, O, BH, N, d))
     return cudaErrorInvalidValue;
-  const float scale_log2 = scale * 1.44269504088896340736f;
+  const float sl = scale * 1.44269504088896340736f;
   if (d == 128)
-    return causal ? launch_t<128, true>(mq, mk, mv, mo, O, LSE, BH, N, H, group, scale_log2, status, stream)
-                  : launch_t<128, false>(mq, mk, mv, mo, O, LSE, BH, N, H, group, scale_log2, status, stream);
-  return causal ? launch_t<64, true>(mq, mk, mv, mo, O, LSE, BH, N, H, group, scale_log2, status, stream)
-                : launch_t<64, false>(mq, mk, mv, mo, O, LSE, BH, N, H, group, scale_log2, status, stream);
+    return causal ? launch_t<128, true>(mq, mk, mv, mo, LSE, BH, N, H, group, sl, 1.f, status, stream)
+                  : launch_t<128, false>(mq, mk, mv, mo, LSE, BH, N, H, group, sl, 1.f, status, stream);
+  return causal ? launch_t<64, true>(mq, mk, mv, mo, LSE, BH, N, H, group, sl, 1.f, status, stream)
+                : launch_t<64, false>(mq, mk, mv, mo, LSE, BH, N, H, group, sl, 1.f, status, stream);
+}
+
+cudaError_t launch_fwd_f8_tiles(const void *Q8, const void *K8, const void *VT8, int N_pad,
+                                void *O, float *LSE, int B, int H, int N, float scale_log2,
+                                float descale_v, int causal, unsigned *status,
+                                cudaStream_t stream) {
+  using namespace fwd;
+  constexpr int D = 128;
+  const int BH = B * H;
+  CUtensorMap mq, mk, mvt, mo;
+  if (!make_bytes_map(&mq, Q8, BH, N, D, D, 128, 128) ||
+      !make_bytes_map(&mk, K8, BH, N, D, D, 128, 128) ||
+      !make_bytes_map(&mvt, VT8, BH, D, N, N_pad, 128, 128) || !make_map(&mo, O, BH, N, D))
+    return cudaErrorInvalidValue;
+  // P reaches the P V product scaled by 2^2; the epilogue takes it back out
+  // together with V's descale.
+  const float out_mul = descale_v / kPScale8;
+  return causal ? launch_t<D, true, true>(mq, mk, mvt, mo, LSE, BH, N, H, 1, scale_log2, out_mul,
+                                          status, stream)
+                : launch_t<D, false, true>(mq, mk, mvt, mo, LSE, BH, N, H, 1, scale_log2, out_mul,
+                                           status, stream);
 }
 
 }  // namespace ea

@@ -62,6 +62,13 @@ cudaError_t launch_fwd_fp8(const void *Q8, const void *K8, const void *V8, void 
                            int B, int H, int N, float scale, float descale_q, float descale_k,
                            float descale_v, int causal, void *ws, unsigned *status,
                            cudaStream_t stream);
+// The FP8 instance of the two-query-tile forward kernel: E4M3 Q and K
+// [B*H, N, 128], V^T [B*H, 128, N_pad] (N_pad a multiple of 16), scale_log2 =
+// scale * descale_q * descale_k * log2(e); O bf16, LSE fp32.
+cudaError_t launch_fwd_f8_tiles(const void *Q8, const void *K8, const void *VT8, int N_pad,
+                                void *O, float *LSE, int B, int H, int N, float scale_log2,
+                                float descale_v, int causal, unsigned *status,
+                                cudaStream_t stream);
 
 // Device address of the current device's status word (looked up once per device).
 cudaError_t device_status_word(unsigned **out);
