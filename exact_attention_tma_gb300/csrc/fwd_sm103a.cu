@@ -11,20 +11,21 @@
 // blocks entirely above the diagonal are never loaded or multiplied.
 //
 // GB300 mapping: one CTA owns two 128-row query tiles of one head (256 rows)
-// and streams that head's K/V tiles once for both.  16 warps:
-//   warps 0-7   softmax: warps q and q+4 share TMEM lanes 32q..32q+31, i.e.
-//               rows 32q..32q+31 of both query tiles; warp q takes keys 0-63
-//               of every K/V tile, warp q+4 keys 64-127 (thread = row)
-//   warp 8      MMA issuer (one elected lane): tcgen05.mma S_i = Q_i K_j^T into
+// and streams that head's K/V tiles once for both.  18 warps:
+//   warps 0-7   softmax of query tile 0, warps 8-15 of query tile 1: warps
+//               8i+q and 8i+q+4 share TMEM lanes 32q..32q+31, i.e. rows
+//               32q..32q+31 of tile i; warp 8i+q takes keys 0-63 of every K/V
+//               tile, warp 8i+q+4 keys 64-127 (thread = row)
+//   warp 16     MMA issuer (one elected lane): tcgen05.mma S_i = Q_i K_j^T into
 //               TMEM (both operands from swizzled shared memory), then
 //               O += P_i V_j with P_i read straight from TMEM (each key half
 //               overwrites the first 32 of its own 64 S columns as packed bf16)
-//   warp 9      TMA producer: Q tiles once, K_j and V_j into separate rings
+//   warp 17     TMA producer: Q tiles once, K_j and V_j into separate rings
 //               guarded by full/empty mbarriers
-//   warps 10-15 idle
-// The softmax warps work through S_0(j), S_1(j), S_0(j+1), ... while the tensor
-// core runs the other query tile's MMAs, and a tile's P is ready after half a
-// row's exponentials.
+// Each sub-partition runs four softmax warps, two per query tile: while one
+// tile's warps wait for their scores or hand P over, the other tile's warps
+// keep the MUFU and FMA pipes busy, and the tensor core runs one tile's MMAs
+// while the other tile's softmax works.
 //
 // Softmax per K/V tile, in the exp2 domain (x = s * scale * log2 e): the
 // exponentials are computed against the running maximum m straight away (no
@@ -48,9 +49,9 @@
 // below E4M3's 448).  Q_i holds half as many bytes, so O is staged in a
 // buffer of its own; the epilogue multiplies by V's descale over 2^2.
 //
-// Registers are re-balanced with setmaxnreg: 160 per softmax thread, 128 for
-// warps 8-11 and 32 for the idle warps 12-15 (256*160 + 128*128 + 128*32 =
-// 61440 of the block's launch allocation of 512 threads x 128).
+// Registers: 18 warps leave 96 per thread (a sub-partition holds five warps);
+// the softmax reads its 64 scores as two 32-column loads in turn so that it
+// fits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -67,9 +68,9 @@ namespace fwd {
 constexpr int BM = 128;                  // query rows per tile (B_r)
 constexpr int BN = 128;                  // keys per K/V tile (B_c)
 constexpr int QT = 2;                    // query tiles per CTA
-constexpr int kThreads = 512;
-constexpr int kWarpMMA = 8;
-constexpr int kWarpTMA = 9;
+constexpr int kThreads = 576;
+constexpr int kWarpMMA = 16;
+constexpr int kWarpTMA = 17;
 constexpr uint32_t kTmemCols = 512;      // S0 | S1 | O0 | O1
 constexpr uint32_t kBoxBytes = 64 * 128 * 2;   // one TMA box: 64 columns x 128 rows bf16
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -128,7 +129,7 @@ struct Cfg {
   // q[QT], kf[SK], ke[SK], vf[SV], ve[SV], s[QT], p[QT][NPB], o[QT], drain
   static constexpr int NBAR = QT + 2 * SK + 2 * SV + QT + QT * NPB + QT + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 32;   // tmem slot, abort flag, pair_abort[4]
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 48;   // tmem slot, abort flag, pair_abort[8]
   static constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;   // 1024-byte alignment slack
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
   static constexpr uint32_t TMEM_S = 0;               // S_i at column 128 * i
@@ -138,12 +139,6 @@ struct Cfg {
   static_assert(TMEM_O + QT * NPB * D <= kTmemCols, "tensor memory budget");
 };
 
-__device__ __forceinline__ void setmaxnreg_inc160() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 160;" ::: "memory");
-}
-__device__ __forceinline__ void setmaxnreg_dec32() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 32;" ::: "memory");
-}
 
 // exp2 of 32 consecutive scores of one row against the maximum m (-nm = m):
 // p = 2^(s * scale_log2 - m), packed as bf16 pairs into pk; adds the p to the
@@ -286,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(B_DRAIN, 1);
     *abort_flag = 0;
-    for (int p = 0; p < 4; ++p) pair_abort[p] = 0;
+    for (int p = 0; p < 8; ++p) pair_abort[p] = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
@@ -314,82 +309,78 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (wg < QT) {
-    setmaxnreg_inc160();
+  if (warp < 8 * QT) {
     // ------------------------------------------------------------ softmax
-    // Warps q and q + 4 share TMEM lanes 32q..32q+31 (rows 32q..32q+31 of
-    // both query tiles): warp q takes keys 0-63 of every K/V tile, warp q + 4
-    // keys 64-127, and both run through S_0, S_1, S_0, ... in the MMA's order.
+    // Warps 8i + q and 8i + q + 4 share TMEM lanes 32q..32q+31 (rows
+    // 32q..32q+31 of query tile i): the first takes keys 0-63 of every K/V
+    // tile, the second keys 64-127.
     // With one O accumulator per row (d = 128) the pair agrees through its own
     // named barrier on each rescale (and on an abort); with one per key half
     // (d = 64) the halves run independently.  Either way the pair combines its
     // partial sums (and maxima) once at the end.
     constexpr bool kIndep = C::kIndep;
-    const int h = wg;                        // key half
+    const int i = warp >> 3;                 // query tile of this group of 8 warps
+    const int h = wg & 1;                    // key half
     const int q = warp & 3;
     const int r = q * 32 + lane;             // row within a tile == TMEM lane
-    const uint32_t pair_bar = 1 + q;
+    const uint32_t pair_bar = 1 + 4 * i + q;
+    const int pa = 4 * i + q;
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     float *xch = reinterpret_cast<float *>(smem + C::OFF_XCH);   // [2][QT][2][BM]
     const float2 sc2 = make_float2(scale_log2, scale_log2);
-    int lim[QT];                             // last visible key of the row in tile i
-#pragma unroll
-    for (int i = 0; i < QT; ++i) lim[i] = CAUSAL ? min(q0 + i * BM + r, N - 1) : N - 1;
+    const int lim_i = CAUSAL ? min(q0 + i * BM + r, N - 1) : N - 1;   // last visible key of the row
     // O accumulator columns this thread rescales and, at the end, reads.
     auto o_block = [&](int i) {
       return tmem + lane_addr + C::TMEM_O + (kIndep ? (2 * i + h) * D : i * D + h * (D / 2));
     };
     // This thread's 64 scores of S_i: P = 2^(x - m_use) packed into pk and
-    // their sum.  Keys 32-63 are read from TMEM while keys 0-31 are
-    // exponentiated.
+    // their sum, 32 scores at a time.
     auto pass = [&](uint32_t s_addr, int k0, int lm, float m_use, uint32_t (&pk)[32], float &rs) {
       const float nm = (F8 ? kLog2PScale8 : 0.f) - m_use;
       const float2 nm2 = make_float2(nm, nm);
       float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      uint32_t a[32], b[32];
-      tmem_ld_32cols(s_addr, a);
-      tmem_ld_wait_regs(a);
-      tmem_ld_32cols(s_addr + 32, b);
-      mask_chunk(a, k0, lm);
-      if constexpr (F8) exp_chunk_f8(a, sc2, nm2, &pk[0], rs2);
-      else exp_chunk(a, sc2, nm2, &pk[0], rs2);
+      {
+        uint32_t a[32];
+        tmem_ld_32cols(s_addr, a);
+        tmem_ld_wait_regs(a);
+        mask_chunk(a, k0, lm);
+        if constexpr (F8) exp_chunk_f8(a, sc2, nm2, &pk[0], rs2);
+        else exp_chunk(a, sc2, nm2, &pk[0], rs2);
+      }
       __syncwarp();
-      tmem_ld_wait_regs(b);
-      mask_chunk(b, k0 + 32, lm);
-      if constexpr (F8) exp_chunk_f8(b, sc2, nm2, &pk[8], rs2);
-      else exp_chunk(b, sc2, nm2, &pk[16], rs2);
+      {
+        uint32_t b[32];
+        tmem_ld_32cols(s_addr + 32, b);
+        tmem_ld_wait_regs(b);
+        mask_chunk(b, k0 + 32, lm);
+        if constexpr (F8) exp_chunk_f8(b, sc2, nm2, &pk[8], rs2);
+        else exp_chunk(b, sc2, nm2, &pk[16], rs2);
+      }
       rs = (rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y);
       if constexpr (F8) rs *= 1.0f / kPScale8;
     };
     // Maximum of this thread's 64 (masked) raw scores of S_i.
     auto half_max = [&](uint32_t s_addr, int k0, int lm) {
-      uint32_t a[32], b[32];
-      tmem_ld_32cols(s_addr, a);
-      tmem_ld_32cols(s_addr + 32, b);
-      tmem_ld_wait_regs(a);
-      reg_fence32(b);
-      mask_chunk(a, k0, lm);
-      mask_chunk(b, k0 + 32, lm);
-      float ma = __uint_as_float(a[0]), mb = __uint_as_float(b[0]);
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int u = 0; u < 2; ++u) {
+        uint32_t a[32];
+        tmem_ld_32cols(s_addr + 32 * u, a);
+        tmem_ld_wait_regs(a);
+        mask_chunk(a, k0 + 32 * u, lm);
 #pragma unroll
-      for (int c = 1; c + 1 < 32; c += 2) {
-        ma = fmax3(ma, __uint_as_float(a[c]), __uint_as_float(a[c + 1]));
-        mb = fmax3(mb, __uint_as_float(b[c]), __uint_as_float(b[c + 1]));
+        for (int c = 0; c + 1 < 32; c += 2)
+          mx = fmax3(mx, __uint_as_float(a[c]), __uint_as_float(a[c + 1]));
       }
       __syncwarp();
-      return fmaxf(fmaxf(ma, __uint_as_float(a[31])), fmaxf(mb, __uint_as_float(b[31])));
+      return mx;
     };
-    float m[QT], l[QT];                      // per tile: max used for P (base 2), partial row sum
-#pragma unroll
-    for (int i = 0; i < QT; ++i) {
-      m[i] = kIndep ? kMInit : 0.f;
-      l[i] = 0.f;
-    }
+    float m_i = kIndep ? kMInit : 0.f;        // max used for P (base 2)
+    float l_i = 0.f;                          // partial row sum
     bool ok = true;
-    for (int j = 0; ok && j < n1; ++j) {
-#pragma unroll
-      for (int i = 0; i < QT; ++i) {
-        if (j >= (i == 0 ? n0 : n1)) continue;
+    const int n_i = (i == 0) ? n0 : n1;
+    for (int j = 0; ok && j < n_i; ++j) {
+      {
         // With a shared accumulator, a warp whose wait gave up still takes
         // part in the pair's barriers below; the vote after the pass then
         // ends the loop for both.
@@ -406,18 +397,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           // First tile: the maximum first (of the half, or of the whole row,
           // which always contains key 0).
           if (kIndep) {
-            const float hm = half_max(s_addr, k0, lim[i]);
-            m[i] = (hm == -INFINITY) ? kMInit : hm * scale_log2;
+            const float hm = half_max(s_addr, k0, lim_i);
+            m_i = (hm == -INFINITY) ? kMInit : hm * scale_log2;
           } else {
-            xi[h * BM + r] = okw ? half_max(s_addr, k0, lim[i]) : 0.f;
+            xi[h * BM + r] = okw ? half_max(s_addr, k0, lim_i) : 0.f;
             named_bar_sync(pair_bar, 64);
-            m[i] = fmaxf(xi[r], xi[BM + r]) * scale_log2;
+            m_i = fmaxf(xi[r], xi[BM + r]) * scale_log2;
           }
         }
         uint32_t pk[32];
         float rs = 0.f;
-        if (okw) pass(s_addr, k0, lim[i], m[i], pk, rs);
-        else pair_abort[q] = 1;
+        if (okw) pass(s_addr, k0, lim_i, m_i, pk, rs);
+        else pair_abort[pa] = 1;
         // rs > 2^15 (or not finite) means some P exceeded 2^9: the maximum
         // grew, and the tile is redone with the new one (by both halves when
         // they share the accumulator).
@@ -427,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           redo = __any_sync(0xffffffffu, !(rs <= kRedo));
         } else {
           redo = named_bar_any(pair_bar, 64, !okw || !(rs <= kRedo));
-          if (redo && pair_abort[q]) {
+          if (redo && pair_abort[pa]) {
             ok = false;
             break;
           }
@@ -436,16 +427,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (redo) {
           float tmax;
           if (kIndep) {
-            tmax = half_max(s_addr, k0, lim[i]);
+            tmax = half_max(s_addr, k0, lim_i);
           } else {
-            xi[h * BM + r] = half_max(s_addr, k0, lim[i]);
+            xi[h * BM + r] = half_max(s_addr, k0, lim_i);
             named_bar_sync(pair_bar, 64);
             tmax = fmaxf(xi[r], xi[BM + r]);
           }
-          const float m_new = fmaxf(m[i], tmax * scale_log2);
-          alpha = ex2_approx(m[i] - m_new);
-          m[i] = m_new;
-          pass(s_addr, k0, lim[i], m[i], pk, rs);
+          const float m_new = fmaxf(m_i, tmax * scale_log2);
+          alpha = ex2_approx(m_i - m_new);
+          m_i = m_new;
+          pass(s_addr, k0, lim_i, m_i, pk, rs);
           if (j > 0) {
             // This thread's accumulator columns scaled by 2^(m_old - m_new).
             const uint32_t o_addr = o_block(i);
@@ -460,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        l[i] = l[i] * alpha + rs;
+        l_i = l_i * alpha + rs;
         // P for keys 64h .. 64h+63 (bf16 pairs, or E4M3 quadruples) over the
         // first 32 (16) of this thread's own S columns, which it has already read.
         if constexpr (F8) tmem_st_16cols(s_addr, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
@@ -478,20 +469,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // writes the LSE.  Independent halves are merged with weights
     // 2^(m_h - max(m_0, m_1)).  Every MMA reading Q_i finished before the last
     // P_i V_j, whose completion the epilogue waits for.
-    constexpr uint32_t kEpiBar = 5;          // named barrier of all 256 softmax threads
-#pragma unroll
-    for (int i = 0; i < QT; ++i) {
+    const uint32_t kEpiBar = 9 + i;          // named barrier of the group's 256 threads
+    do {
       const bool okw = ok && __all_sync(0xffffffffu, mbar_wait(B_O(i), 0, status, abort_flag));
       float *xm = xch + i * 2 * BM;                 // maxima (independent halves)
       float *xl = xch + (QT + i) * 2 * BM;          // partial sums
-      if (kIndep) xm[h * BM + r] = m[i];   // (the shared-max exchange above uses xm otherwise)
-      xl[h * BM + r] = l[i];
+      if (kIndep) xm[h * BM + r] = m_i;   // (the shared-max exchange above uses xm otherwise)
+      xl[h * BM + r] = l_i;
       if (named_bar_any(kEpiBar, 2 * BM, !okw)) {
         ok = false;
-        continue;
+        break;
       }
       tc_fence_after();
-      float mrow = m[i], w0 = 1.f, w1 = 1.f;
+      float mrow = m_i, w0 = 1.f, w1 = 1.f;
       if (kIndep) {
         mrow = fmaxf(xm[r], xm[BM + r]);
         w0 = ex2_approx(xm[r] - mrow);
@@ -533,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async_smem();
       named_bar_sync(kEpiBar, 2 * BM);
-      if (threadIdx.x == 0) {
+      if (threadIdx.x == i * 256) {
 #pragma unroll
         for (int kb = 0; kb < D / 64; ++kb)
           tma_store_3d(&tmO, kb * 64, q0 + i * BM, bh, stage_base + kb * kBoxBytes);
@@ -544,12 +534,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm("lg2.approx.f32 %0, %1;" : "=f"(lg) : "f"(lt));
         LSE[static_cast<size_t>(bh) * N + qrow] = (mrow + lg) * kLn2;
       }
-    }
-    // The staged tiles must have been read before the CTA's shared memory goes.
-    if (threadIdx.x == 0) bulk_wait_group_read0();
+    } while (false);
+    // The staged tile must have been read before the CTA's shared memory goes.
+    if (threadIdx.x == i * 256) bulk_wait_group_read0();
     tc_fence_before();
-  } else if (wg == QT) {
-    // Warps 8 and 9 run their schedules warp-uniformly (every lane waits on the
+  } else {
+    // Warps 16 and 17 run their schedules warp-uniformly (every lane waits on the
     // barriers) and one elected lane issues the TMA copies / MMAs, so addresses
     // and descriptors stay in the warp-uniform datapath.
     if (warp == kWarpTMA) {
@@ -719,8 +709,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     }
-  } else {
-    setmaxnreg_dec32();   // warps 12-15: nothing to do
   }
   __syncthreads();
   if (warp == kWarpMMA) {
