@@ -10,8 +10,10 @@
 // note "causal masking is not an optimisation here" on the same page: K/V
 // blocks entirely above the diagonal are never loaded or multiplied.
 //
-// GB300 mapping: one CTA owns two 128-row query tiles of one head (256 rows)
-// and streams that head's K/V tiles once for both.  18 warps:
+// GB300 mapping: a work item is two 128-row query tiles of one head (256
+// rows), whose K/V tiles stream once for both.  One persistent CTA per SM
+// (18 warps) takes items one after another from a global counter, longest
+// causal items first:
 //   warps 0-7   softmax of query tile 0, warps 8-15 of query tile 1: warps
 //               8i+q and 8i+q+4 share TMEM lanes 32q..32q+31, i.e. rows
 //               32q..32q+31 of tile i; warp 8i+q takes keys 0-63 of every K/V
@@ -20,8 +22,13 @@
 //               TMEM (both operands from swizzled shared memory), then
 //               O += P_i V_j with P_i read straight from TMEM (each key half
 //               overwrites the first 32 of its own 64 S columns as packed bf16)
-//   warp 17     TMA producer: Q tiles once, K_j and V_j into separate rings
-//               guarded by full/empty mbarriers
+//   warp 17     TMA producer: the item's Q tiles, K_j and V_j into separate
+//               rings guarded by full/empty mbarriers; it claims the next
+//               item and passes its index to the other warps
+// Item boundaries overlap: the next item's first K/V tiles load while the
+// current one finishes, and its Q tiles as soon as their buffers are free
+// (after the last Q K^T where O has a staging buffer of its own, after the
+// epilogue's store where O is staged in the Q buffer).
 // Each sub-partition runs four softmax warps, two per query tile: while one
 // tile's warps wait for their scores or hand P over, the other tile's warps
 // keep the MUFU and FMA pipes busy, and the tensor core runs one tile's MMAs
@@ -72,6 +79,7 @@ constexpr int kThreads = 576;
 constexpr int kWarpMMA = 16;
 constexpr int kWarpTMA = 17;
 constexpr uint32_t kTmemCols = 512;      // S0 | S1 | O0 | O1
+constexpr int kRing = 4;                 // item indices in flight from the TMA warp to the others
 constexpr uint32_t kBoxBytes = 64 * 128 * 2;   // one TMA box: 64 columns x 128 rows bf16
 constexpr float kLn2 = 0.69314718055994530942f;
 // A half row (64 keys) whose P sum exceeds 2^15 has some P above 2^9: its
@@ -125,11 +133,15 @@ struct Cfg {
   // a buffer of its own.
   static constexpr uint32_t O_TILE = BM * D * 2;
   static constexpr uint32_t OFF_OST = OFF_XCH + 2 * QT * 2 * BM * 4;
-  static constexpr uint32_t OFF_BAR = OFF_OST + (F8 ? QT * O_TILE : 0);
-  // q[QT], kf[SK], ke[SK], vf[SV], ve[SV], s[QT], p[QT][NPB], o[QT], drain
-  static constexpr int NBAR = QT + 2 * SK + 2 * SV + QT + QT * NPB + QT + 1;
+  // O is staged in a buffer of its own where shared memory allows (then
+  // the Q buffers are released as soon as the last Q K^T has read them).
+  static constexpr bool kOwnStage = F8 || D == 64;
+  static constexpr uint32_t OFF_BAR = OFF_OST + (kOwnStage ? QT * O_TILE : 0);
+  // q[QT], qe[QT], kf[SK], ke[SK], vf[SV], ve[SV], s[QT], p[QT][NPB], o[QT], drain
+  static constexpr int NBAR = 2 * QT + 2 * SK + 2 * SV + QT + QT * NPB + QT + 1 + 2 * kRing;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 48;   // tmem slot, abort flag, pair_abort[8]
+  // tmem slot, abort flag, pair_abort[8], item ring
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 48 + 4 * kRing;
   static constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;   // 1024-byte alignment slack
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
   static constexpr uint32_t TMEM_S = 0;               // S_i at column 128 * i
@@ -193,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                     float *__restrict__ LSE, int N, int BH, int n_blk, int H, int group,
-                    float scale_log2, float out_mul, unsigned *status) {
+                    float scale_log2, float out_mul, unsigned *status, unsigned *sched) {
   using C = Cfg<D, F8>;
   constexpr int SK = C::SK;
   constexpr int SV = C::SV;
@@ -205,52 +217,86 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int wg = warp >> 2;
 
-  // Causal: heads vary fastest and the longest query blocks go first, so the
-  // hardware scheduler balances the unequal blocks.  Non-causal: all blocks
-  // cost the same, so query blocks vary fastest and the co-resident CTAs share
-  // a few heads' K/V through L2 instead of each streaming its own head.
-  const int bh = CAUSAL ? static_cast<int>(blockIdx.x % BH) : static_cast<int>(blockIdx.x / n_blk);
-  // K/V head read by query head bh: H query heads per batch share H / group
-  // K/V heads in contiguous groups ("Why Fast GPUs Still Wait for Memory",
-  // Attention III: GQA with group size g; g = 1 is multi-head attention).
-  const int kvh = (bh / H) * (H / group) + (bh % H) / group;
-  const int blk = CAUSAL ? n_blk - 1 - static_cast<int>(blockIdx.x / BH)
-                         : static_cast<int>(blockIdx.x % n_blk);
-  const int q0 = blk * (QT * BM);
+  // Work items are (head, 256-row query block) pairs.  Causal: heads vary
+  // fastest and the longest query blocks come first; non-causal: query blocks
+  // vary fastest, so the CTAs working at the same time share a few heads' K/V
+  // through L2.  The CTA is persistent: it starts with item blockIdx and
+  // claims each further item from a global counter (sched[0]) once it has
+  // issued the loads of the current one, so the items go out in order to
+  // whichever CTA frees up first.  The TMA warp claims them and hands each
+  // item index to the MMA and softmax warps through a small ring in shared
+  // memory; the last CTA to finish resets the counter for the next launch.
+  const int n_items = BH * n_blk;
+  const int G = static_cast<int>(gridDim.x);
   const int n_kv_total = (N + BN - 1) / BN;
-  // K/V tiles each query tile needs (query tile 0 can stop one tile earlier when causal).
-  const int n0 = CAUSAL ? min(QT * blk + 1, n_kv_total) : n_kv_total;
-  const int n1 = CAUSAL ? min(QT * blk + 2, n_kv_total) : n_kv_total;
+  struct Item {
+    int bh, kvh, q0, n0, n1;   // head, K/V head, first query row, K/V tiles of query tiles 0, 1
+  };
+  auto item_at = [&](int k, Item &it) {
+    if (k >= n_items) return false;
+    const int blk = CAUSAL ? n_blk - 1 - k / BH : k % n_blk;
+    it.bh = CAUSAL ? k % BH : k / n_blk;
+    // K/V head read by query head bh: H query heads per batch share H / group
+    // K/V heads in contiguous groups ("Why Fast GPUs Still Wait for Memory",
+    // Attention III: GQA with group size g; g = 1 is multi-head attention).
+    it.kvh = (it.bh / H) * (H / group) + (it.bh % H) / group;
+    it.q0 = blk * (QT * BM);
+    // K/V tiles each query tile needs (query tile 0 can stop one tile earlier when causal).
+    it.n0 = CAUSAL ? min(QT * blk + 1, n_kv_total) : n_kv_total;
+    it.n1 = CAUSAL ? min(QT * blk + 2, n_kv_total) : n_kv_total;
+    return true;
+  };
 
+  // Barrier phases run on across items: the K/V rings count K/V tiles over
+  // the CTA's whole sequence, S_i / P_i count tile i's K/V steps, and the Q_i
+  // and O_i barriers complete once per item.
   const uint32_t bar0 = sb + C::OFF_BAR;
   auto B_Q = [&](int i) { return bar0 + 8u * i; };                    // Q_i loaded
-  auto B_KF = [&](int s) { return bar0 + 8u * (QT + s); };
-  auto B_KE = [&](int s) { return bar0 + 8u * (QT + SK + s); };
-  auto B_VF = [&](int s) { return bar0 + 8u * (QT + 2 * SK + s); };
-  auto B_VE = [&](int s) { return bar0 + 8u * (QT + 2 * SK + SV + s); };
-  constexpr int kB5 = QT + 2 * SK + 2 * SV;
+  auto B_QE = [&](int i) { return bar0 + 8u * (QT + i); };            // Q_i buffer and O_i free
+  auto B_KF = [&](int s) { return bar0 + 8u * (2 * QT + s); };
+  auto B_KE = [&](int s) { return bar0 + 8u * (2 * QT + SK + s); };
+  auto B_VF = [&](int s) { return bar0 + 8u * (2 * QT + 2 * SK + s); };
+  auto B_VE = [&](int s) { return bar0 + 8u * (2 * QT + 2 * SK + SV + s); };
+  constexpr int kB5 = 2 * QT + 2 * SK + 2 * SV;
   auto B_S = [&](int i) { return bar0 + 8u * (kB5 + i); };            // S_i ready (MMA)
   constexpr int NPB = C::NPB;
   // P_i written by the softmax (per key half when the halves are independent)
   auto B_P = [&](int i, int hh) { return bar0 + 8u * (kB5 + QT + i * NPB + (NPB > 1 ? hh : 0)); };
-  auto B_O = [&](int i) { return bar0 + 8u * (kB5 + QT + QT * NPB + i); };   // last P_i V_j done
+  auto B_O = [&](int i) { return bar0 + 8u * (kB5 + QT + QT * NPB + i); };   // item's last P_i V_j done
   const uint32_t B_DRAIN = bar0 + 8u * (kB5 + 2 * QT + QT * NPB);
-  static_assert(kB5 + 2 * QT + QT * NPB + 1 == C::NBAR, "barrier count");
+  constexpr int kB6 = kB5 + 2 * QT + QT * NPB + 1;
+  auto B_IF = [&](int s) { return bar0 + 8u * (kB6 + s); };           // item slot s written
+  auto B_IE = [&](int s) { return bar0 + 8u * (kB6 + kRing + s); };   // item slot s read by all
+  static_assert(kB6 + 2 * kRing == C::NBAR, "barrier count");
+  volatile int *item_ring = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 48);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
   // Set by a softmax warp whose wait gave up, read by it and its partner warp
   // after their shared barrier (so both take the same exit).
   volatile int *pair_abort = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 16);
+  // The t-th item of this CTA as the TMA warp published it (warp-uniform):
+  // false past the last item, or when the wait gave up (then ok = false).
+  auto take_item = [&](int t, Item &it, bool &ok) {
+    const int s = t % kRing;
+    if (!__all_sync(0xffffffffu, mbar_wait(B_IF(s), (t / kRing) & 1, status, abort_flag))) {
+      ok = false;
+      return false;
+    }
+    const int k = item_ring[s];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(B_IE(s));
+    return item_at(k, it);
+  };
   // K_j and V_j into ring stages sk / sv: 128-byte-wide column boxes of the
   // [keys][d] tiles, or with FP8 one box of K and one box of the V^T tile
   // [d][keys] (keys contiguous).
-  auto load_k = [&](int j, int sk) {
+  auto load_k = [&](int kvh, int j, int sk) {
 #pragma unroll
     for (int kb = 0; kb < C::KB; ++kb)
       tma_load_3d(sb + C::OFF_K + sk * C::KV_BYTES + kb * kBoxBytes, &tmK, kb * C::BOX_COLS,
                   j * BN, kvh, B_KF(sk));
   };
-  auto load_v = [&](int j, int sv) {
+  auto load_v = [&](int kvh, int j, int sv) {
     const uint32_t dst = sb + C::OFF_V + sv * C::KV_BYTES;
     if constexpr (F8) {
       tma_load_3d(dst, &tmV, j * BN, 0, kvh, B_VF(sv));
@@ -260,12 +306,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(dst + kb * kBoxBytes, &tmV, kb * 64, j * BN, kvh, B_VF(sv));
     }
   };
-
+  auto load_q = [&](const Item &it, int i) {
+    mbar_arrive_expect_tx(B_Q(i), C::Q_BYTES);
+#pragma unroll
+    for (int kb = 0; kb < C::KB; ++kb)
+      tma_load_3d(sb + C::OFF_Q + i * C::Q_BYTES + kb * kBoxBytes, &tmQ, kb * C::BOX_COLS,
+                  it.q0 + i * BM, it.bh, B_Q(i));
+  };
   // One thread of the TMA warp sets up the barriers and at once starts the
-  // first loads, in the order the first MMAs need them (Q_0 and K_0, then Q_1
-  // and V_0), while the MMA warp allocates TMEM.
+  // first item's loads, in the order the first MMAs need them (Q_0 and K_0,
+  // then Q_1 and V_0), while the MMA warp allocates TMEM.
   if (threadIdx.x == kWarpTMA * 32) {
-    for (int i = 0; i < QT; ++i) mbar_init(B_Q(i), 1);
+    for (int i = 0; i < QT; ++i) {
+      mbar_init(B_Q(i), 1);
+      mbar_init(B_QE(i), 1);
+    }
     for (int s = 0; s < SK; ++s) {
       mbar_init(B_KF(s), 1);
       mbar_init(B_KE(s), 1);
@@ -276,10 +331,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < QT; ++i) {
       mbar_init(B_S(i), 1);
-      for (int hh = 0; hh < NPB; ++hh) mbar_init(B_P(i, hh), 2 * BM / NPB);   // 256 threads, 2 per row
+      for (int hh = 0; hh < NPB; ++hh) mbar_init(B_P(i, hh), 2 * BM / NPB / 32);   // one arrival per warp
       mbar_init(B_O(i), 1);
     }
     mbar_init(B_DRAIN, 1);
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(B_IF(s), 1);
+      mbar_init(B_IE(s), 1 + 8 * QT);   // the MMA warp and every softmax warp
+    }
     *abort_flag = 0;
     for (int p = 0; p < 8; ++p) pair_abort[p] = 0;
     fence_mbar_init();
@@ -287,18 +346,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmO);
-    auto load_q = [&](int i) {
-      mbar_arrive_expect_tx(B_Q(i), C::Q_BYTES);
-      for (int kb = 0; kb < C::KB; ++kb)
-        tma_load_3d(sb + C::OFF_Q + i * C::Q_BYTES + kb * kBoxBytes, &tmQ, kb * C::BOX_COLS,
-                    q0 + i * BM, bh, B_Q(i));
-    };
-    load_q(0);
-    mbar_arrive_expect_tx(B_KF(0), C::KV_BYTES);
-    load_k(0, 0);
-    for (int i = 1; i < QT; ++i) load_q(i);
-    mbar_arrive_expect_tx(B_VF(0), C::KV_BYTES);
-    load_v(0, 0);
+    Item it0;
+    if (item_at(static_cast<int>(blockIdx.x), it0)) {   // (always true: the grid is no larger than the item count)
+      load_q(it0, 0);
+      mbar_arrive_expect_tx(B_KF(0), C::KV_BYTES);
+      load_k(it0.kvh, 0, 0);
+      for (int i = 1; i < QT; ++i) load_q(it0, i);
+      mbar_arrive_expect_tx(B_VF(0), C::KV_BYTES);
+      load_v(it0.kvh, 0, 0);
+    }
   }
   if (warp == kWarpMMA) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -317,25 +373,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     // With one O accumulator per row (d = 128) the pair agrees through its own
     // named barrier on each rescale (and on an abort); with one per key half
     // (d = 64) the halves run independently.  Either way the pair combines its
-    // partial sums (and maxima) once at the end.
+    // partial sums (and maxima) once at the end of each item.
     constexpr bool kIndep = C::kIndep;
     const int i = warp >> 3;                 // query tile of this group of 8 warps
     const int h = wg & 1;                    // key half
     const int q = warp & 3;
     const int r = q * 32 + lane;             // row within a tile == TMEM lane
     const uint32_t pair_bar = 1 + 4 * i + q;
+    const uint32_t kEpiBar = 9 + i;          // named barrier of the group's 256 threads
     const int pa = 4 * i + q;
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     float *xch = reinterpret_cast<float *>(smem + C::OFF_XCH);   // [2][QT][2][BM]
+    float *xi = xch + i * 2 * BM;            // maxima of the two halves
+    float *xl = xch + (QT + i) * 2 * BM;     // partial sums of the two halves
     const float2 sc2 = make_float2(scale_log2, scale_log2);
-    const int lim_i = CAUSAL ? min(q0 + i * BM + r, N - 1) : N - 1;   // last visible key of the row
-    // O accumulator columns this thread rescales and, at the end, reads.
-    auto o_block = [&](int i) {
-      return tmem + lane_addr + C::TMEM_O + (kIndep ? (2 * i + h) * D : i * D + h * (D / 2));
-    };
+    const uint32_t s_addr = tmem + lane_addr + C::TMEM_S + i * BN + h * 64;
+    // O accumulator columns this thread rescales.
+    const uint32_t o_blk =
+        tmem + lane_addr + C::TMEM_O + (kIndep ? (2 * i + h) * D : i * D + h * (D / 2));
     // This thread's 64 scores of S_i: P = 2^(x - m_use) packed into pk and
     // their sum, 32 scores at a time.
-    auto pass = [&](uint32_t s_addr, int k0, int lm, float m_use, uint32_t (&pk)[32], float &rs) {
+    auto pass = [&](int k0, int lm, float m_use, uint32_t (&pk)[32], float &rs) {
       const float nm = (F8 ? kLog2PScale8 : 0.f) - m_use;
       const float2 nm2 = make_float2(nm, nm);
       float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
@@ -360,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (F8) rs *= 1.0f / kPScale8;
     };
     // Maximum of this thread's 64 (masked) raw scores of S_i.
-    auto half_max = [&](uint32_t s_addr, int k0, int lm) {
+    auto half_max = [&](int k0, int lm) {
       float mx = -INFINITY;
 #pragma unroll 1
       for (int u = 0; u < 2; ++u) {
@@ -375,43 +433,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       return mx;
     };
-    float m_i = kIndep ? kMInit : 0.f;        // max used for P (base 2)
-    float l_i = 0.f;                          // partial row sum
     bool ok = true;
-    const int n_i = (i == 0) ? n0 : n1;
-    for (int j = 0; ok && j < n_i; ++j) {
-      {
+    int base = 0;                            // steps of tile i in earlier items
+    for (int t = 0; ok; ++t) {
+      Item it;
+      if (!take_item(t, it, ok)) break;
+      const int n_i = (i == 0) ? it.n0 : it.n1;
+      const int lim = CAUSAL ? min(it.q0 + i * BM + r, N - 1) : N - 1;   // last visible key of the row
+      float m_i = kIndep ? kMInit : 0.f;     // max used for P (base 2)
+      float l_i = 0.f;                       // partial row sum
+      for (int j = 0; j < n_i; ++j) {
         // With a shared accumulator, a warp whose wait gave up still takes
         // part in the pair's barriers below; the vote after the pass then
         // ends the loop for both.
-        const bool okw = __all_sync(0xffffffffu, mbar_wait(B_S(i), j & 1, status, abort_flag));
+        const bool okw =
+            __all_sync(0xffffffffu, mbar_wait(B_S(i), (base + j) & 1, status, abort_flag));
         if (kIndep && !okw) {
           ok = false;
           break;
         }
         if (okw) tc_fence_after();
-        const uint32_t s_addr = tmem + lane_addr + C::TMEM_S + i * BN + h * 64;
         const int k0 = j * BN + h * 64;
-        float *xi = xch + i * 2 * BM;
         if (j == 0) {
           // First tile: the maximum first (of the half, or of the whole row,
           // which always contains key 0).
           if (kIndep) {
-            const float hm = half_max(s_addr, k0, lim_i);
+            const float hm = half_max(k0, lim);
             m_i = (hm == -INFINITY) ? kMInit : hm * scale_log2;
           } else {
-            xi[h * BM + r] = okw ? half_max(s_addr, k0, lim_i) : 0.f;
+            xi[h * BM + r] = okw ? half_max(k0, lim) : 0.f;
             named_bar_sync(pair_bar, 64);
             m_i = fmaxf(xi[r], xi[BM + r]) * scale_log2;
           }
         }
         uint32_t pk[32];
         float rs = 0.f;
-        if (okw) pass(s_addr, k0, lim_i, m_i, pk, rs);
+        if (okw) pass(k0, lim, m_i, pk, rs);
         else pair_abort[pa] = 1;
-        // rs > 2^15 (or not finite) means some P exceeded 2^9: the maximum
-        // grew, and the tile is redone with the new one (by both halves when
-        // they share the accumulator).
+        // rs above the threshold (or not finite) means some P exceeded it:
+        // the maximum grew, and the tile is redone with the new one (by both
+        // halves when they share the accumulator).
         bool redo;
         constexpr float kRedo = F8 ? kRescaleSum8 : kRescaleSum;
         if (kIndep) {
@@ -427,27 +488,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (redo) {
           float tmax;
           if (kIndep) {
-            tmax = half_max(s_addr, k0, lim_i);
+            tmax = half_max(k0, lim);
           } else {
-            xi[h * BM + r] = half_max(s_addr, k0, lim_i);
+            xi[h * BM + r] = half_max(k0, lim);
             named_bar_sync(pair_bar, 64);
             tmax = fmaxf(xi[r], xi[BM + r]);
           }
           const float m_new = fmaxf(m_i, tmax * scale_log2);
           alpha = ex2_approx(m_i - m_new);
           m_i = m_new;
-          pass(s_addr, k0, lim_i, m_i, pk, rs);
+          pass(k0, lim, m_i, pk, rs);
           if (j > 0) {
             // This thread's accumulator columns scaled by 2^(m_old - m_new).
-            const uint32_t o_addr = o_block(i);
+            // O_i is quiescent: the MMA that wrote it last was committed
+            // before S_i was.
 #pragma unroll 1
             for (int c = 0; c < (kIndep ? D / 32 : D / 64); ++c) {
               uint32_t o[32];
-              tmem_ld_32cols(o_addr + c * 32, o);
+              tmem_ld_32cols(o_blk + c * 32, o);
               tmem_ld_wait_regs(o);
 #pragma unroll
               for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-              tmem_st_32cols(o_addr + c * 32, o);
+              tmem_st_32cols(o_blk + c * 32, o);
             }
           }
         }
@@ -458,24 +520,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         else tmem_st_32cols(s_addr, pk);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(B_P(i, h));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(B_P(i, h));
       }
-    }
-    // Epilogue per tile: each warp stages its half of the columns of O_i as
-    // bf16 in the (no longer needed) Q_i buffer (with FP8, whose Q_i is half
-    // the size, in a staging buffer of its own), in the 128-byte-swizzled box
-    // layout of the O tensor map, and one thread stores the tile with TMA
-    // (rows past N are dropped by the tensor map); the warp of the low half
-    // writes the LSE.  Independent halves are merged with weights
-    // 2^(m_h - max(m_0, m_1)).  Every MMA reading Q_i finished before the last
-    // P_i V_j, whose completion the epilogue waits for.
-    const uint32_t kEpiBar = 9 + i;          // named barrier of the group's 256 threads
-    do {
-      const bool okw = ok && __all_sync(0xffffffffu, mbar_wait(B_O(i), 0, status, abort_flag));
-      float *xm = xch + i * 2 * BM;                 // maxima (independent halves)
-      float *xl = xch + (QT + i) * 2 * BM;          // partial sums
-      if (kIndep) xm[h * BM + r] = m_i;   // (the shared-max exchange above uses xm otherwise)
+      // Epilogue of tile i: each warp stages its half of the columns of O_i
+      // as bf16 in the (no longer needed) Q_i buffer (with FP8, whose Q_i is
+      // half the size, in a staging buffer of its own), in the
+      // 128-byte-swizzled box layout of the O tensor map, and one thread
+      // stores the tile with TMA (rows past N are dropped by the tensor map);
+      // the warp of the low half writes the LSE.  Independent halves are
+      // merged with weights 2^(m_h - max(m_0, m_1)).  Every MMA reading Q_i
+      // finished before the item's last P_i V_j, whose completion the
+      // epilogue waits for.  Once the store has read the staging buffer, the
+      // storing thread releases Q_i (and O_i) to the next item.
+      const bool okw = ok && __all_sync(0xffffffffu, mbar_wait(B_O(i), t & 1, status, abort_flag));
+      if (kIndep) xi[h * BM + r] = m_i;
       xl[h * BM + r] = l_i;
+      // (FP8: the previous item's store must have read the staging buffer.)
+      if (C::kOwnStage && threadIdx.x == i * 256) bulk_wait_group_read0();
       if (named_bar_any(kEpiBar, 2 * BM, !okw)) {
         ok = false;
         break;
@@ -483,15 +545,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       float mrow = m_i, w0 = 1.f, w1 = 1.f;
       if (kIndep) {
-        mrow = fmaxf(xm[r], xm[BM + r]);
-        w0 = ex2_approx(xm[r] - mrow);
-        w1 = ex2_approx(xm[BM + r] - mrow);
+        mrow = fmaxf(xi[r], xi[BM + r]);
+        w0 = ex2_approx(xi[r] - mrow);
+        w1 = ex2_approx(xi[BM + r] - mrow);
       }
       const float lt = w0 * xl[r] + w1 * xl[BM + r];
       const float inv_l = out_mul / lt;
       const float a0 = w0 * inv_l, a1 = w1 * inv_l;
-      const int qrow = q0 + i * BM + r;
-      const uint32_t stage_base = F8 ? sb + C::OFF_OST + i * C::O_TILE : sb + C::OFF_Q + i * C::Q_BYTES;
+      const int qrow = it.q0 + i * BM + r;
+      const uint32_t stage_base =
+          C::kOwnStage ? sb + C::OFF_OST + i * C::O_TILE : sb + C::OFF_Q + i * C::Q_BYTES;
       const uint32_t stage = stage_base + static_cast<uint32_t>(r) * 128;
       const uint32_t o_addr = tmem + lane_addr + C::TMEM_O + (kIndep ? 2 * i * D : i * D) + h * (D / 2);
 #pragma unroll
@@ -522,56 +585,103 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
       fence_proxy_async_smem();
+      tc_fence_before();
       named_bar_sync(kEpiBar, 2 * BM);
       if (threadIdx.x == i * 256) {
 #pragma unroll
         for (int kb = 0; kb < D / 64; ++kb)
-          tma_store_3d(&tmO, kb * 64, q0 + i * BM, bh, stage_base + kb * kBoxBytes);
+          tma_store_3d(&tmO, kb * 64, it.q0 + i * BM, it.bh, stage_base + kb * kBoxBytes);
         bulk_commit_group();
+        if constexpr (!C::kOwnStage) {
+          bulk_wait_group_read0();
+          mbar_arrive(B_QE(i));
+        }
       }
       if (h == 0 && qrow < N) {
         float lg;
         asm("lg2.approx.f32 %0, %1;" : "=f"(lg) : "f"(lt));
-        LSE[static_cast<size_t>(bh) * N + qrow] = (mrow + lg) * kLn2;
+        LSE[static_cast<size_t>(it.bh) * N + qrow] = (mrow + lg) * kLn2;
       }
-    } while (false);
-    // The staged tile must have been read before the CTA's shared memory goes.
+      base += n_i;
+    }
+    // The last stores must have finished reading shared memory before the CTA exits.
     if (threadIdx.x == i * 256) bulk_wait_group_read0();
     tc_fence_before();
   } else {
     // Warps 16 and 17 run their schedules warp-uniformly (every lane waits on the
     // barriers) and one elected lane issues the TMA copies / MMAs, so addresses
     // and descriptors stay in the warp-uniform datapath.
+    auto wait_all = [&](uint32_t bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, abort_flag));
+    };
     if (warp == kWarpTMA) {
       // ------------------------------------------------------ TMA producer
-      // (Q and the first K/V tile were issued before the CTA-wide barrier.)
+      // (The first item's Q tiles and first K/V tile were issued before the
+      // CTA-wide barrier.)  Q_i of a later item waits until the previous
+      // item's epilogue of tile i has released the buffer.
       const bool leader = elect_one();
-      int issued_k = 1, issued_v = 1;
-      for (int j = 1; j < n1; ++j) {
-        const int sk = j % SK;
-        if (!__all_sync(0xffffffffu, mbar_wait(B_KE(sk), ((j / SK) & 1) ^ 1u, status, abort_flag)))
-          break;
+      int gk = 0, gv = 0;                    // K / V tiles issued so far
+      int q_items[QT];                       // per Q buffer: items whose Q tile was issued
+#pragma unroll
+      for (int i = 0; i < QT; ++i) q_items[i] = 1;
+      bool ok = true;
+      auto load_k_next = [&](int kvh, int j) {
+        const int sk = gk % SK;
+        if (!wait_all(B_KE(sk), ((gk / SK) & 1) ^ 1u)) return false;
         if (leader) {
           mbar_arrive_expect_tx(B_KF(sk), C::KV_BYTES);
-          load_k(j, sk);
+          load_k(kvh, j, sk);
         }
-        issued_k = j + 1;
-        const int sv = j % SV;
-        if (!__all_sync(0xffffffffu, mbar_wait(B_VE(sv), ((j / SV) & 1) ^ 1u, status, abort_flag)))
-          break;
+        ++gk;
+        return true;
+      };
+      auto load_v_next = [&](int kvh, int j) {
+        const int sv = gv % SV;
+        if (!wait_all(B_VE(sv), ((gv / SV) & 1) ^ 1u)) return false;
         if (leader) {
           mbar_arrive_expect_tx(B_VF(sv), C::KV_BYTES);
-          load_v(j, sv);
+          load_v(kvh, j, sv);
         }
-        issued_v = j + 1;
+        ++gv;
+        return true;
+      };
+      int k = static_cast<int>(blockIdx.x);
+      for (int t = 0; ok; ++t) {
+        // Publish item k (or the end of the sequence) to the other warps.
+        const int s = t % kRing;
+        if (!(ok = wait_all(B_IE(s), ((t / kRing) & 1) ^ 1u))) break;
+        if (leader) {
+          item_ring[s] = k;
+          mbar_arrive(B_IF(s));
+        }
+        __syncwarp();
+        Item it;
+        if (!item_at(k, it)) break;
+        if (t == 0) {
+          gk = gv = 1;
+        } else {
+          // K_0 and V_0 go first: their stages are free well before the
+          // previous item's epilogues release the Q buffers.
+          ok = load_k_next(it.kvh, 0) && load_v_next(it.kvh, 0);
+          for (int i = 0; ok && i < QT; ++i) {
+            if (!(ok = wait_all(B_QE(i), (t - 1) & 1))) break;
+            if (leader) load_q(it, i);
+            q_items[i] = t + 1;
+          }
+        }
+        for (int j = 1; ok && j < it.n1; ++j) ok = load_k_next(it.kvh, j) && load_v_next(it.kvh, j);
+        // This item's loads are all issued: claim the next one.
+        int kn = 0;
+        if (lane == 0) kn = G + static_cast<int>(atomicAdd(sched, 1u));
+        k = __shfl_sync(0xffffffffu, kn, 0);
       }
       if (leader && *abort_flag) {
         // Let every copy this warp started land before the CTA exits.
-        for (int i = 0; i < QT; ++i) mbar_wait_drain(B_Q(i), 0, 100000000ull);
-        for (int s = 0; s < SK && s < issued_k; ++s)
-          mbar_wait_drain(B_KF(s), (((issued_k - 1 - s) / SK)) & 1, 100000000ull);
-        for (int s = 0; s < SV && s < issued_v; ++s)
-          mbar_wait_drain(B_VF(s), (((issued_v - 1 - s) / SV)) & 1, 100000000ull);
+        for (int i = 0; i < QT; ++i) mbar_wait_drain(B_Q(i), (q_items[i] - 1) & 1, 100000000ull);
+        for (int s = 0; s < SK && s < gk; ++s)
+          mbar_wait_drain(B_KF(s), ((gk - 1 - s) / SK) & 1, 100000000ull);
+        for (int s = 0; s < SV && s < gv; ++s)
+          mbar_wait_drain(B_VF(s), ((gv - 1 - s) / SV) & 1, 100000000ull);
       }
       __syncwarp();
     } else if (warp == kWarpMMA) {
@@ -592,9 +702,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q_lo = static_cast<uint32_t>(dQ);
       const uint32_t k_lo = static_cast<uint32_t>(dK);
       const uint32_t v_lo = static_cast<uint32_t>(dV);
-      auto wait_all = [&](uint32_t bar, uint32_t parity) {
-        return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, abort_flag));
-      };
       // S_i = Q_i K^T: both operands K-major (head dim contiguous), 128-B swizzle.
       auto issue_qk = [&](int i, int sk) {
         const uint32_t a0 = q_lo + ((i * C::Q_BYTES) >> 4);
@@ -613,7 +720,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O += P_i V: P_i from TMEM (8 columns = 16 keys per step; keys 0-63 in
       // columns 0-31 of S_i, keys 64-127 in columns 64-95); V is MN-major
       // (head dim contiguous), 64-column blocks kBoxBytes apart, 8-key groups 1024 B apart.
-      // Key steps kb..ke-1 into the accumulator at column o_col.
       // FP8: 32 keys per step, P_i's keys 0-63 in columns 0-15 and keys
       // 64-127 in columns 64-79 (four E4M3 per column); the V^T tile is
       // K-major, 32-byte k-steps along its 128-byte rows.
@@ -631,76 +737,98 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // P_i V_j: one run over all 128 keys into O_i, or (independent halves)
       // keys 0-63 into O_i^0 as soon as that half's P is in, then keys 64-127
-      // into O_i^1.
-      auto pv = [&](int i, int sv, int j) {
+      // into O_i^1.  ph: parity of tile i's step.
+      auto pv = [&](int i, int sv, int j, uint32_t ph) {
         if constexpr (C::kIndep) {
-          if (!wait_all(B_P(i, 0), j & 1)) return false;
+          if (!wait_all(B_P(i, 0), ph)) return false;
           tc_fence_after();
           if (leader) issue_pv(i, sv, j > 0, 0, C::PSTEPS / 2, C::TMEM_O + 2 * i * D);
           __syncwarp();
-          if (!wait_all(B_P(i, 1), j & 1)) return false;
+          if (!wait_all(B_P(i, 1), ph)) return false;
           tc_fence_after();
           if (leader) issue_pv(i, sv, j > 0, C::PSTEPS / 2, C::PSTEPS, C::TMEM_O + (2 * i + 1) * D);
           __syncwarp();
         } else {
-          if (!wait_all(B_P(i, 0), j & 1)) return false;
+          if (!wait_all(B_P(i, 0), ph)) return false;
           tc_fence_after();
           if (leader) issue_pv(i, sv, j > 0, 0, C::PSTEPS, C::TMEM_O + i * D);
           __syncwarp();
         }
         return true;
       };
-      bool ok = wait_all(B_Q(0), 0) && wait_all(B_KF(0), 0);
-      if (ok) {
-        tc_fence_after();
-        if (leader) {
-          issue_qk(0, 0);
-          mma_commit(B_S(0));
-        }
-        __syncwarp();
-      }
-      ok = ok && wait_all(B_Q(1), 0);
-      if (ok) {
-        tc_fence_after();
-        if (leader) {
-          issue_qk(1, 0);
-          mma_commit(B_S(1));
-          if (SK < n1) mma_commit(B_KE(0));
-        }
-        __syncwarp();
-      }
-      // Per K/V tile j: the V_j and K_{j+1} stages are checked first (they are
-      // normally resident long before), so that each softmax hand-off is
-      // followed by one wait and an uninterrupted run of MMAs:
-      // P_0 V_j, Q_0 K_{j+1}^T, then P_1 V_j, Q_1 K_{j+1}^T.
-      for (int j = 0; ok && j < n1; ++j) {
-        const int sv = j % SV;
-        const bool more = j + 1 < n1;
-        const int sk1 = (j + 1) % SK;
-        if (!(ok = wait_all(B_VF(sv), (j / SV) & 1))) break;
-        if (more && !(ok = wait_all(B_KF(sk1), ((j + 1) / SK) & 1))) break;
-        if (j < n0) {
-          if (!(ok = pv(0, sv, j))) break;
-          if (leader) {
-            if (j + 1 == n0) mma_commit(B_O(0));
-            if (j + 1 < n0) {
-              issue_qk(0, sk1);   // overwrites S_0/P_0 after the P_0 V_j MMAs above read it
+      bool ok = true;
+      int gk = 0, gv = 0;                    // K / V tiles consumed so far
+      int base0 = 0, base1 = 0;              // steps of tiles 0 / 1 in earlier items
+      for (int t = 0; ok; ++t) {
+        Item it;
+        if (!take_item(t, it, ok)) break;
+        const int n0 = it.n0, n1 = it.n1;
+        // S_0 = Q_0 K_0^T, S_1 = Q_1 K_0^T.  Q_i of this item arrives only
+        // after the previous item's epilogue of tile i has read O_i, so the
+        // first P_i V_0 below may overwrite O_i.
+        {
+          const int sk = gk % SK;
+          ok = wait_all(B_Q(0), t & 1) && wait_all(B_KF(sk), (gk / SK) & 1);
+          if (ok) {
+            tc_fence_after();
+            if (leader) {
+              issue_qk(0, sk);
               mma_commit(B_S(0));
+              if (C::kOwnStage && n0 == 1) mma_commit(B_QE(0));
+            }
+            __syncwarp();
+          }
+          ok = ok && wait_all(B_Q(1), t & 1);
+          if (ok) {
+            tc_fence_after();
+            if (leader) {
+              issue_qk(1, sk);
+              mma_commit(B_S(1));
+              mma_commit(B_KE(sk));
+              if (C::kOwnStage && n1 == 1) mma_commit(B_QE(1));
+            }
+            __syncwarp();
+          }
+        }
+        // Per K/V tile j: the V_j and K_{j+1} stages are checked first (they are
+        // normally resident long before), so that each softmax hand-off is
+        // followed by one wait and an uninterrupted run of MMAs:
+        // P_0 V_j, Q_0 K_{j+1}^T, then P_1 V_j, Q_1 K_{j+1}^T.
+        for (int j = 0; ok && j < n1; ++j) {
+          const int vp = gv + j, sv = vp % SV;
+          const bool more = j + 1 < n1;
+          const int kp = gk + j + 1, sk1 = kp % SK;
+          if (!(ok = wait_all(B_VF(sv), (vp / SV) & 1))) break;
+          if (more && !(ok = wait_all(B_KF(sk1), (kp / SK) & 1))) break;
+          if (j < n0) {
+            if (!(ok = pv(0, sv, j, (base0 + j) & 1))) break;
+            if (leader) {
+              if (j + 1 == n0) mma_commit(B_O(0));
+              if (j + 1 < n0) {
+                issue_qk(0, sk1);   // overwrites S_0/P_0 after the P_0 V_j MMAs above read it
+                mma_commit(B_S(0));
+                if (C::kOwnStage && j + 2 == n0) mma_commit(B_QE(0));
+              }
+            }
+            __syncwarp();
+          }
+          if (!(ok = pv(1, sv, j, (base1 + j) & 1))) break;
+          if (leader) {
+            if (j + 1 == n1) mma_commit(B_O(1));
+            mma_commit(B_VE(sv));
+            if (more) {
+              issue_qk(1, sk1);
+              mma_commit(B_S(1));
+              mma_commit(B_KE(sk1));
+              if (C::kOwnStage && j + 2 == n1) mma_commit(B_QE(1));
             }
           }
           __syncwarp();
         }
-        if (!(ok = pv(1, sv, j))) break;
-        if (leader) {
-          if (j + 1 == n1) mma_commit(B_O(1));
-          if (j + SV < n1) mma_commit(B_VE(sv));
-          if (more) {
-            issue_qk(1, sk1);
-            mma_commit(B_S(1));
-            if (j + 1 + SK < n1) mma_commit(B_KE(sk1));
-          }
-        }
-        __syncwarp();
+        gk += n1;
+        gv += n1;
+        base0 += n0;
+        base1 += n1;
       }
       // Every MMA issued so far must finish before TMEM is released.
       if (leader) {
@@ -714,6 +842,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpMMA) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  }
+  // Every claim of this CTA is behind it: the last CTA to get here resets
+  // the item counter (sched[0]) and this count (sched[1]) for the next launch.
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(sched + 1, 1u) == gridDim.x - 1) {
+      atomicExch(sched, 0u);
+      atomicExch(sched + 1, 0u);
+    }
   }
 }
 
@@ -748,6 +885,30 @@ static bool make_map(CUtensorMap *m, const void *base, int BH, int N, int d, int
   return r == CUDA_SUCCESS;
 }
 
+// Item counters of the persistent forward, [slot][counter, finished CTAs];
+// each launch takes the next slot and leaves it at zero when it completes, so
+// launches in flight at the same time (up to kSchedSlots, on any streams) do
+// not share one.
+constexpr int kSchedSlots = 256;
+__device__ unsigned g_fwd_sched[kSchedSlots][2];
+
+static cudaError_t sched_slot(unsigned **out) {
+  static unsigned *base[64] = {};
+  static std::atomic<unsigned> next{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!base[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_fwd_sched);
+    if (e != cudaSuccess) return e;
+    base[dev] = static_cast<unsigned *>(p);
+  }
+  *out = base[dev] + 2 * (next.fetch_add(1u) % kSchedSlots);
+  return cudaSuccess;
+}
+
 template <int D, bool CAUSAL, bool F8 = false>
 static cudaError_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                             const CUtensorMap &mo, float *LSE, int BH, int N, int H, int group,
@@ -767,9 +928,14 @@ static cudaError_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const 
     configured.fetch_or(bit);
   }
   const int n_blk = (N + QT * BM - 1) / (QT * BM);
-  const long long grid = static_cast<long long>(BH) * n_blk;
+  // Persistent: one CTA per SM (at most one per work item).
+  const long long n_items = static_cast<long long>(BH) * n_blk;
+  const long long grid = n_items < sm_count() ? n_items : sm_count();
+  unsigned *sched = nullptr;
+  e = sched_slot(&sched);
+  if (e != cudaSuccess) return e;
   kern<<<static_cast<unsigned>(grid), kThreads, C::SMEM_ALLOC, stream>>>(
-      mq, mk, mv, mo, LSE, N, BH, n_blk, H, group, scale_log2, out_mul, status);
+      mq, mk, mv, mo, LSE, N, BH, n_blk, H, group, scale_log2, out_mul, status, sched);
   return cudaGetLastError();
 }
 
