@@ -464,12 +464,15 @@ def run_ours(args, rank, world, local_rank):
 
 def per_config(ea, peaks, dev, stream, reps=10):
     """Each performance workload on its own: median over `reps` launches with an
-    L2 flush (256 MB write) between launches."""
+    L2 flush between launches: a 256 MB write, then a read of the same buffer,
+    so that the dirty lines the write leaves in L2 are written back before the
+    timed call rather than during it."""
     import torch
 
     from exact_attention_tma_gb300.inputs import WORKLOADS, workload_inputs
 
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush_words = flush.view(torch.int32)
     out = {}
     for name in ("causal_fwd", "noncausal_fwd", "long_causal_fwd", "decode", "gqa_fwd",
                  "gqa_decode", "paged_decode", "paged_gqa_decode", "causal_bwd", "fp8_causal_fwd",
@@ -515,6 +518,7 @@ def per_config(ea, peaks, dev, stream, reps=10):
         times = []
         for _ in range(reps):
             flush.zero_()
+            flush_words.max()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             call()
