@@ -28,11 +28,20 @@ namespace f8 {
 constexpr int D = 128;                     // head dimension (bytes per row)
 
 // ------------------------------------------------------------ V transpose
-// V [BH, N, 128] bytes -> V^T [BH, 128, N_pad] bytes, 128 x 128 blocks
-// through shared memory (row stride 132 so column reads spread over banks).
+// V [BH, N, 128] bytes -> V^T [BH, 128, N_pad] bytes, one 128-key x 128-byte
+// block per CTA.  The block is staged in shared memory as 32-bit words, 32
+// per key row, with the word column XOR-swizzled by bits of the key (so that
+// the column reads below hit 32 distinct banks); each thread then reads 4 x 4
+// byte blocks (4 keys x 4 head-dim bytes) as words, transposes them with byte
+// permutes, and writes 16 keys of 4 head-dim rows of V^T (8 threads cover
+// one 128-byte output row, so the stores are coalesced).
+__device__ __forceinline__ int vt_swz(int k) {   // word-column swizzle of key row k (bits 2-4)
+  return (((k >> 5) & 3) << 2) | (((k >> 4) & 1) << 4);
+}
+
 __global__ void __launch_bounds__(256)
     attn_fp8_vt_kernel(const uint8_t *__restrict__ V, uint8_t *__restrict__ VT, int N, int N_pad) {
-  __shared__ uint8_t tile[128 * 132];
+  __shared__ uint4 tile[128 * 8];      // [key][8 quads of 4 words], quad index swizzled
   const size_t bh = blockIdx.y;
   const int k0 = blockIdx.x * 128;
   const uint8_t *src = V + (bh * N + k0) * D;
@@ -42,30 +51,35 @@ __global__ void __launch_bounds__(256)
     const int row = idx >> 3, c = idx & 7;
     uint4 x = make_uint4(0, 0, 0, 0);
     if (k0 + row < N) x = *reinterpret_cast<const uint4 *>(src + row * D + c * 16);
-    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      *reinterpret_cast<uint32_t *>(&tile[row * 132 + c * 16 + 4 * e]) = w[e];
+    tile[row * 8 + (c ^ (vt_swz(row) >> 2))] = x;
   }
   __syncthreads();
-  uint8_t *dst = VT + bh * D * static_cast<size_t>(N_pad) + k0;
+  const uint32_t *words = reinterpret_cast<const uint32_t *>(tile);
+  const int kg = threadIdx.x & 7;      // keys 16 kg .. 16 kg + 15
+  const int dg = threadIdx.x >> 3;     // head-dim bytes 4 dg .. 4 dg + 3
+  if (k0 + kg * 16 >= N_pad) return;
+  uint32_t out[4][4];                  // [head-dim byte j][4-key group g]
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int idx = threadIdx.x + u * 256;           // 1024 chunks of 16 keys
-    const int d = idx >> 3, c = idx & 7;
-    if (k0 + c * 16 >= N_pad) continue;
-    uint32_t w[4];
+  for (int g = 0; g < 4; ++g) {
+    uint32_t r[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int k = c * 16 + 4 * e;
-      w[e] = static_cast<uint32_t>(tile[k * 132 + d]) |
-             (static_cast<uint32_t>(tile[(k + 1) * 132 + d]) << 8) |
-             (static_cast<uint32_t>(tile[(k + 2) * 132 + d]) << 16) |
-             (static_cast<uint32_t>(tile[(k + 3) * 132 + d]) << 24);
+    for (int i = 0; i < 4; ++i) {
+      const int k = kg * 16 + g * 4 + i;
+      r[i] = words[k * 32 + (dg ^ vt_swz(k))];
     }
-    *reinterpret_cast<uint4 *>(dst + static_cast<size_t>(d) * N_pad + c * 16) =
-        make_uint4(w[0], w[1], w[2], w[3]);
+    // 4 x 4 byte transpose: out[j][g] byte i = r[i] byte j.
+    const uint32_t t0 = __byte_perm(r[0], r[1], 0x5140), t1 = __byte_perm(r[0], r[1], 0x7362);
+    const uint32_t t2 = __byte_perm(r[2], r[3], 0x5140), t3 = __byte_perm(r[2], r[3], 0x7362);
+    out[0][g] = __byte_perm(t0, t2, 0x5410);
+    out[1][g] = __byte_perm(t0, t2, 0x7632);
+    out[2][g] = __byte_perm(t1, t3, 0x5410);
+    out[3][g] = __byte_perm(t1, t3, 0x7632);
   }
+  uint8_t *dst = VT + bh * D * static_cast<size_t>(N_pad) + k0 + kg * 16;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    *reinterpret_cast<uint4 *>(dst + static_cast<size_t>(4 * dg + j) * N_pad) =
+        make_uint4(out[j][0], out[j][1], out[j][2], out[j][3]);
 }
 
 }  // namespace f8
