@@ -157,15 +157,6 @@ __device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
-// 3-D tiled TMA prefetch of one box into L2 (no shared memory, no barrier);
-// boxes that reach past the tensor's bounds fetch only what lies inside.
-__device__ __forceinline__ void tma_prefetch_l2_3d(const void *tmap, int x, int y, int z) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                   reinterpret_cast<uint64_t>(tmap)),
-               "r"(x), "r"(y), "r"(z)
-               : "memory");
-}
-
 // 3-D tiled TMA load of one box into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int x, int y, int z,
                                             uint32_t bar) {
@@ -437,26 +428,6 @@ __device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&r)[32]) {
 __device__ __forceinline__ void reg_fence32(uint32_t (&r)[32]) {
   asm volatile("" : EA_RW32(r) : : "memory");
 }
-#define EA_R16(r)                                                                              \
-  "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),           \
-      "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),   \
-      "=r"(r[14]), "=r"(r[15])
-#define EA_RW16(r)                                                                             \
-  "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),           \
-      "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),   \
-      "+r"(r[14]), "+r"(r[15])
-// 16 consecutive columns of this thread's TMEM lane, and its wait.
-__device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-      : EA_R16(r)
-      : "r"(taddr)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_ld_wait_regs16(uint32_t (&r)[16]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" : EA_RW16(r) : : "memory");
-}
 __device__ __forceinline__ void tmem_st_32cols(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -476,13 +447,6 @@ __device__ __forceinline__ void tmem_st_16cols(uint32_t taddr, const uint32_t (&
       "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
       EA_W16(r)
       : "memory");
-}
-// Each thread writes 8 consecutive 32-bit columns of its own TMEM lane.
-__device__ __forceinline__ void tmem_st_8cols(uint32_t taddr, const uint32_t (&r)[8]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
-                   taddr),
-               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-               : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
