@@ -887,9 +887,11 @@ static bool make_map(CUtensorMap *m, const void *base, int BH, int N, int d, int
 
 // Item counters of the persistent forward, [slot][counter, finished CTAs];
 // each launch takes the next slot and leaves it at zero when it completes, so
-// launches in flight at the same time (up to kSchedSlots, on any streams) do
-// not share one.
-constexpr int kSchedSlots = 256;
+// launches in flight at the same time on any streams do not share one unless
+// kSchedSlots launches were issued in between.  A captured CUDA graph keeps
+// the slot of its capture: one graph must not be replayed on two streams at
+// once (as with any workspace it holds).
+constexpr int kSchedSlots = 65536;
 __device__ unsigned g_fwd_sched[kSchedSlots][2];
 
 static cudaError_t sched_slot(unsigned **out) {

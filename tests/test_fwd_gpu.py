@@ -153,3 +153,30 @@ def test_runs_on_a_side_stream():
     s.synchronize()
     O_ref, L_ref = oracle_fwd(q, k, v, 0.125, False)
     assert_within(compare_fwd(o, lse, O_ref, L_ref, range(B * H), None))
+
+
+def test_concurrent_launches_on_several_streams():
+    """The persistent forward hands out work items from a counter that each
+    launch takes for itself: launches running at the same time on different
+    streams (and more launches than there are counters) each compute their own
+    result, equal to the same call made alone."""
+    B, H, N, d = 2, 8, 1024, 128
+    streams = [torch.cuda.Stream() for _ in range(4)]
+    ins = [fwd_inputs(B, H, N, d, 40 + n, device="cuda") for n in range(4)]
+    refs = []
+    for q, k, v in ins:
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+        ea.attn_fwd(q, k, v, o, lse, True, d ** -0.5)
+        refs.append((o, lse))
+    torch.cuda.synchronize()
+    outs = [(torch.empty_like(q), torch.empty((B, H, N), dtype=torch.float32, device="cuda"))
+            for q, _, _ in ins]
+    for rep in range(80):   # 320 launches in flight in groups of four
+        for s, (q, k, v), (o, lse) in zip(streams, ins, outs):
+            with torch.cuda.stream(s):
+                ea.attn_fwd(q, k, v, o, lse, True, d ** -0.5, stream=s)
+    torch.cuda.synchronize()
+    for (o, lse), (o_ref, l_ref) in zip(outs, refs):
+        assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
+    assert ea.attn_get_device_status() == 0
