@@ -176,16 +176,26 @@ __global__ void __launch_bounds__(kPrepThreads)
   }
 }
 
-// Writes 32 fp32 accumulator columns of one row as bf16 (times `mul`).
-__device__ __forceinline__ void store_row32(__nv_bfloat16 *dst, const uint32_t (&r)[32], float mul) {
-  uint32_t pk[16];
+// Stages 32 fp32 accumulator columns (times `mul`) of tile row `row` as bf16
+// at columns col0.. of a [128 rows][D] tile laid out as the 128-byte-swizzled
+// 64-column boxes of a TMA map (box b at stage + b * kBoxBytes), for a TMA
+// store of the whole tile (rows past N are dropped by the map).
+__device__ __forceinline__ void stage_row32(uint32_t stage, int row, int col0,
+                                            const uint32_t (&r)[32], float mul) {
 #pragma unroll
-  for (int k = 0; k < 16; ++k)
-    pk[k] = pack_bf16x2(__uint_as_float(r[2 * k]) * mul, __uint_as_float(r[2 * k + 1]) * mul);
+  for (int v = 0; v < 4; ++v) {
+    uint32_t w[4];
 #pragma unroll
-  for (int v = 0; v < 4; ++v)
-    st_global_v4(dst + 8 * v, pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+    for (int e = 0; e < 4; ++e)
+      w[e] = pack_bf16x2(__uint_as_float(r[8 * v + 2 * e]) * mul,
+                         __uint_as_float(r[8 * v + 2 * e + 1]) * mul);
+    const int col = col0 + 8 * v;
+    const uint32_t chunk = static_cast<uint32_t>((col & 63) >> 3) ^ static_cast<uint32_t>(row & 7);
+    st_shared_v4(stage + (col >> 6) * kBoxBytes + static_cast<uint32_t>(row) * 128 + (chunk << 4),
+                 w[0], w[1], w[2], w[3]);
+  }
 }
+constexpr uint32_t kEpiBar = 1;   // named barrier of the compute warps (epilogue)
 
 // Both kernels run two independent pipelines, one per half of the 128-wide
 // score tile (query columns 0-63 / 64-127 in the dK/dV kernel, key columns
@@ -200,9 +210,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV,
-                         const __grid_constant__ CUtensorMap tmdO, const float *__restrict__ lse2,
-                         const float *__restrict__ delta, __nv_bfloat16 *__restrict__ dK,
-                         __nv_bfloat16 *__restrict__ dV, int N, int N_pad, int H, int H_kv,
+                         const __grid_constant__ CUtensorMap tmdO,
+                         const __grid_constant__ CUtensorMap tmdK,
+                         const __grid_constant__ CUtensorMap tmdV, const float *__restrict__ lse2,
+                         const float *__restrict__ delta, int N, int N_pad, int H, int H_kv,
                          int n_blk, float scale_log2, float scale, unsigned *status) {
   using C = CfgKV<D>;
   constexpr int NST = C::NST;
@@ -475,19 +486,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(B_P(h));
     }
-    if (ok && __all_sync(0xffffffffu, mbar_wait(B_DONE, 0, status, abort_flag))) {
+    // Epilogue: dV and dK staged as bf16 in stage 0's Q and dO slots (every
+    // load into the ring has been consumed once the last products are done)
+    // and stored by TMA; the compute warps agree first, so that they all
+    // take part in the barrier or all skip it.
+    const bool okd = ok && __all_sync(0xffffffffu, mbar_wait(B_DONE, 0, status, abort_flag));
+    if (!named_bar_any(kEpiBar, 32 * kComputeWarps, !okd)) {
       tc_fence_after();
-      const int key = jt * BT + row;
-      const size_t out = (static_cast<size_t>(bkv) * N + key) * D + h * (D / 2);
+      const uint32_t st_dv = sb + C::OFF_STAGE + C::ST_Q;
+      const uint32_t st_dk = sb + C::OFF_STAGE + C::ST_DO;
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         uint32_t r[32];
         tmem_ld_32cols(tmem + lane_base + C::TM_DV + h * (D / 2) + 32 * c, r);
         tmem_ld_wait_regs(r);
-        if (key < N) store_row32(dV + out + 32 * c, r, 1.f);
+        stage_row32(st_dv, row, h * (D / 2) + 32 * c, r, 1.f);
         tmem_ld_32cols(tmem + lane_base + C::TM_DK + h * (D / 2) + 32 * c, r);
         tmem_ld_wait_regs(r);
-        if (key < N) store_row32(dK + out + 32 * c, r, scale);
+        stage_row32(st_dk, row, h * (D / 2) + 32 * c, r, scale);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(kEpiBar, 32 * kComputeWarps);
+      if (threadIdx.x == 0) {
+#pragma unroll
+        for (int kb = 0; kb < C::KB; ++kb) {
+          tma_store_3d(&tmdV, kb * 64, jt * BT, bkv, st_dv + kb * kBoxBytes);
+          tma_store_3d(&tmdK, kb * 64, jt * BT, bkv, st_dk + kb * kBoxBytes);
+        }
+        bulk_commit_group();
+        bulk_wait_group_read0();
       }
     }
   }
@@ -504,9 +531,10 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ CUtensorMap tmdQ,
                        const __nv_bfloat16 *__restrict__ Q, const __nv_bfloat16 *__restrict__ dO,
                        const float *__restrict__ lse2, const float *__restrict__ delta,
-                       __nv_bfloat16 *__restrict__ dQ, int N, int N_pad, int H, int H_kv,
+                       int N, int N_pad, int H, int H_kv,
                        int n_blk, float scale_log2, float scale, unsigned *status) {
   using C = CfgQ<D>;
   constexpr int NST = C::NST;
@@ -745,16 +773,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(B_P(h));
     }
-    if (ok && __all_sync(0xffffffffu, mbar_wait(B_DONE, 0, status, abort_flag))) {
+    // Epilogue: dQ staged as bf16 in stage 0's K slot (every K/V load has
+    // been consumed once the last products are done) and stored by TMA.
+    const bool okd = ok && __all_sync(0xffffffffu, mbar_wait(B_DONE, 0, status, abort_flag));
+    if (!named_bar_any(kEpiBar, 32 * kComputeWarps, !okd)) {
       tc_fence_after();
-      const int qi = it * BT + row;
-      const size_t out = (static_cast<size_t>(bh) * N + qi) * D + h * (D / 2);
+      const uint32_t st_dq = sb + C::OFF_STAGE + C::ST_K;
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         uint32_t r[32];
         tmem_ld_32cols(tmem + lane_base + C::TM_DQ + h * (D / 2) + 32 * c, r);
         tmem_ld_wait_regs(r);
-        if (qi < N) store_row32(dQ + out + 32 * c, r, scale);
+        stage_row32(st_dq, row, h * (D / 2) + 32 * c, r, scale);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(kEpiBar, 32 * kComputeWarps);
+      if (threadIdx.x == 0) {
+#pragma unroll
+        for (int kb = 0; kb < C::KB; ++kb)
+          tma_store_3d(&tmdQ, kb * 64, it * BT, bh, st_dq + kb * kBoxBytes);
+        bulk_commit_group();
+        bulk_wait_group_read0();
       }
     }
   }
@@ -769,10 +808,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------ host
 template <int D, bool CAUSAL>
 static cudaError_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                            const CUtensorMap &mdo, const void *Q, const void *dO,
-                            const float *lse2, const float *delta,
-                            void *dQ, void *dK, void *dV, int B, int H, int H_kv, int N, int N_pad,
-                            int n_blk, float scale, unsigned *status, cudaStream_t stream) {
+                            const CUtensorMap &mdo, const CUtensorMap &mdq, const CUtensorMap &mdk,
+                            const CUtensorMap &mdv, const void *Q, const void *dO,
+                            const float *lse2, const float *delta, int B, int H, int H_kv, int N,
+                            int N_pad, int n_blk, float scale, unsigned *status,
+                            cudaStream_t stream) {
   const float scale_log2 = scale * kLog2e;
   auto kkv = attn_bwd_dkdv_kernel<D, CAUSAL>;
   auto kq = attn_bwd_dq_kernel<D, CAUSAL>;
@@ -782,13 +822,12 @@ static cudaError_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const 
   e = smem_limit_once(kq, static_cast<int>(CfgQ<D>::SMEM_ALLOC), set_q);
   if (e != cudaSuccess) return e;
   kkv<<<static_cast<unsigned>(B * H_kv * n_blk), kThreads, CfgKV<D>::SMEM_ALLOC, stream>>>(
-      mq, mk, mv, mdo, lse2, delta, static_cast<__nv_bfloat16 *>(dK),
-      static_cast<__nv_bfloat16 *>(dV), N, N_pad, H, H_kv, n_blk, scale_log2, scale, status);
+      mq, mk, mv, mdo, mdk, mdv, lse2, delta, N, N_pad, H, H_kv, n_blk, scale_log2, scale, status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   kq<<<static_cast<unsigned>(B * H * n_blk), kThreads, CfgQ<D>::SMEM_ALLOC, stream>>>(
-      mk, mv, static_cast<const __nv_bfloat16 *>(Q), static_cast<const __nv_bfloat16 *>(dO), lse2,
-      delta, static_cast<__nv_bfloat16 *>(dQ), N, N_pad, H, H_kv, n_blk, scale_log2, scale, status);
+      mk, mv, mdq, static_cast<const __nv_bfloat16 *>(Q), static_cast<const __nv_bfloat16 *>(dO),
+      lse2, delta, N, N_pad, H, H_kv, n_blk, scale_log2, scale, status);
   return cudaGetLastError();
 }
 
@@ -824,18 +863,20 @@ cudaError_t launch_bwd(const void *Q, const void *K, const void *V, const void *
         delta, N, N_pad);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
   if (!make_bhnd_map(&mq, Q, B * H, N, d, BT) || !make_bhnd_map(&mk, K, B * H_kv, N, d, BT) ||
-      !make_bhnd_map(&mv, V, B * H_kv, N, d, BT) || !make_bhnd_map(&mdo, dO, B * H, N, d, BT))
+      !make_bhnd_map(&mv, V, B * H_kv, N, d, BT) || !make_bhnd_map(&mdo, dO, B * H, N, d, BT) ||
+      !make_bhnd_map(&mdq, dQ, B * H, N, d, BT) || !make_bhnd_map(&mdk, dK, B * H_kv, N, d, BT) ||
+      !make_bhnd_map(&mdv, dV, B * H_kv, N, d, BT))
     return cudaErrorInvalidValue;
   if (d == 128)
-    return causal ? launch_t<128, true>(mq, mk, mv, mdo, Q, dO, lse2, delta, dQ, dK, dV, B, H, H_kv, N,
+    return causal ? launch_t<128, true>(mq, mk, mv, mdo, mdq, mdk, mdv, Q, dO, lse2, delta, B, H, H_kv, N,
                                         N_pad, n_blk, scale, status, stream)
-                  : launch_t<128, false>(mq, mk, mv, mdo, Q, dO, lse2, delta, dQ, dK, dV, B, H, H_kv, N,
+                  : launch_t<128, false>(mq, mk, mv, mdo, mdq, mdk, mdv, Q, dO, lse2, delta, B, H, H_kv, N,
                                          N_pad, n_blk, scale, status, stream);
-  return causal ? launch_t<64, true>(mq, mk, mv, mdo, Q, dO, lse2, delta, dQ, dK, dV, B, H, H_kv, N, N_pad,
+  return causal ? launch_t<64, true>(mq, mk, mv, mdo, mdq, mdk, mdv, Q, dO, lse2, delta, B, H, H_kv, N, N_pad,
                                      n_blk, scale, status, stream)
-                : launch_t<64, false>(mq, mk, mv, mdo, Q, dO, lse2, delta, dQ, dK, dV, B, H, H_kv, N,
+                : launch_t<64, false>(mq, mk, mv, mdo, mdq, mdk, mdv, Q, dO, lse2, delta, B, H, H_kv, N,
                                       N_pad, n_blk, scale, status, stream);
 }
 
