@@ -885,32 +885,6 @@ static bool make_map(CUtensorMap *m, const void *base, int BH, int N, int d, int
   return r == CUDA_SUCCESS;
 }
 
-// Item counters of the persistent forward, [slot][counter, finished CTAs];
-// each launch takes the next slot and leaves it at zero when it completes, so
-// launches in flight at the same time on any streams do not share one unless
-// kSchedSlots launches were issued in between.  A captured CUDA graph keeps
-// the slot of its capture: one graph must not be replayed on two streams at
-// once (as with any workspace it holds).
-constexpr int kSchedSlots = 65536;
-__device__ unsigned g_fwd_sched[kSchedSlots][2];
-
-static cudaError_t sched_slot(unsigned **out) {
-  static unsigned *base[64] = {};
-  static std::atomic<unsigned> next{0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!base[dev]) {
-    void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_fwd_sched);
-    if (e != cudaSuccess) return e;
-    base[dev] = static_cast<unsigned *>(p);
-  }
-  *out = base[dev] + 2 * (next.fetch_add(1u) % kSchedSlots);
-  return cudaSuccess;
-}
-
 template <int D, bool CAUSAL, bool F8 = false>
 static cudaError_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                             const CUtensorMap &mo, float *LSE, int BH, int N, int H, int group,
@@ -961,6 +935,34 @@ bool make_bytes_map(CUtensorMap *m, const void *base, int heads, int rows, int c
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// Item counters of the persistent kernels, [slot][counter, finished CTAs];
+// each launch takes the next slot and leaves it at zero when it completes, so
+// launches in flight at the same time on any streams do not share one unless
+// kSchedSlots launches were issued in between.  A captured CUDA graph keeps
+// the slots of its capture: one graph must not be replayed on two streams at
+// once (as with any workspace it holds).
+constexpr int kSchedSlots = 65536;
+__device__ unsigned g_sched[kSchedSlots][2];
+
+cudaError_t sched_slot(unsigned **out) {
+  static std::atomic<unsigned *> base[64] = {};
+  static std::atomic<unsigned> next{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  unsigned *b = base[dev].load();
+  if (!b) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_sched);
+    if (e != cudaSuccess) return e;
+    b = static_cast<unsigned *>(p);
+    base[dev].store(b);
+  }
+  *out = b + 2 * (next.fetch_add(1u) % kSchedSlots);
+  return cudaSuccess;
 }
 
 cudaError_t launch_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,

@@ -70,6 +70,11 @@ cudaError_t launch_fwd_f8_tiles(const void *Q8, const void *K8, const void *VT8,
                                 float descale_v, int causal, unsigned *status,
                                 cudaStream_t stream);
 
+// A zeroed item-counter pair for one launch of a persistent kernel
+// ([0] = items claimed, [1] = CTAs finished; the kernel's last CTA zeroes
+// both again).  Slots rotate over 65,536 per device.
+cudaError_t sched_slot(unsigned **out);
+
 // Device address of the current device's status word (looked up once per device).
 cudaError_t device_status_word(unsigned **out);
 
