@@ -53,6 +53,7 @@ constexpr int kThreads = 320;
 constexpr int kComputeWarps = 8;
 constexpr int kWarpMMA = 8;
 constexpr int kWarpTMA = 9;
+constexpr int kRing = 4;   // item indices in flight from the TMA warp to the others (dK/dV)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kBoxBytes = 64 * BT * 2;    // one TMA box: 64 columns x 128 rows bf16
 constexpr float kLog2e = 1.44269504088896340736f;
@@ -75,10 +76,11 @@ struct CfgKV {
   static constexpr uint32_t STAGE_TX = 2 * TILE + 1024;
   static constexpr int NST = (D == 64) ? 4 : 2;          // query-tile ring depth
   static constexpr uint32_t OFF_BAR = OFF_STAGE + NST * STAGE_BYTES;
-  // kv, full[NST], empty[NST], s[2], dp[2], p[2], done, drain
-  static constexpr int NBAR = 1 + 2 * NST + 8;
+  // kv, kv free, full[NST], empty[NST], s[2], dp[2], p[2], done, drain,
+  // item ring full[kRing], empty[kRing]
+  static constexpr int NBAR = 2 + 2 * NST + 8 + 2 * kRing;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;   // tmem slot, abort flag
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 4 * kRing;   // tmem slot, abort flag, item ring
   // At least 116 KB so that one CTA runs per SM: each allocates all 512 TMEM
   // columns, and a second CTA would only wait for them.
   static constexpr uint32_t SMEM_ALLOC =
@@ -214,7 +216,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tmdK,
                          const __grid_constant__ CUtensorMap tmdV, const float *__restrict__ lse2,
                          const float *__restrict__ delta, int N, int N_pad, int H, int H_kv,
-                         int n_blk, float scale_log2, float scale, unsigned *status) {
+                         int BHkv, int n_blk, float scale_log2, float scale, unsigned *status,
+                         unsigned *sched) {
   using C = CfgKV<D>;
   constexpr int NST = C::NST;
   extern __shared__ uint8_t smem_raw[];
@@ -224,37 +227,77 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Causal: K/V heads vary fastest and key tiles go in ascending order (the
-  // first key tiles are seen by the most query tiles: longest first).
-  // Non-causal: key tiles vary fastest, so co-resident CTAs share their
-  // head's Q and dO through L2.
-  const int BHkv = static_cast<int>(gridDim.x) / n_blk;
-  const int bkv = CAUSAL ? static_cast<int>(blockIdx.x % BHkv) : static_cast<int>(blockIdx.x / n_blk);
-  const int jt = CAUSAL ? static_cast<int>(blockIdx.x / BHkv) : static_cast<int>(blockIdx.x % n_blk);
+  // Work items are (K/V head, 128-key tile) pairs.  Causal: K/V heads vary
+  // fastest and key tiles go in ascending order (the first key tiles are
+  // seen by the most query tiles: longest first); non-causal: key tiles vary
+  // fastest, so CTAs working at the same time share their head's Q and dO
+  // through L2.  The CTA is persistent: it starts with item blockIdx and
+  // claims further items from a global counter (sched[0]) once the current
+  // item's loads are issued; the TMA warp passes each index on through a
+  // ring in shared memory, and the last CTA to finish resets the counter.
+  const int n_items = BHkv * n_blk;
+  const int G = static_cast<int>(gridDim.x);
   const int group = H / H_kv;
-  const int b = bkv / H_kv;
-  const int hk = bkv % H_kv;
-  const int it0 = CAUSAL ? jt : 0;
-  const int n_q = n_blk - it0;                 // query tiles per query head
-  const int n_it = group * n_q;                // (query head of the group, query tile) pairs
-  auto q_head = [&](int t) { return b * H + hk * group + t / n_q; };
-  auto q_tile = [&](int t) { return it0 + t % n_q; };
+  struct Item {
+    int bkv, jt, it0, n_q, n_it;   // K/V head, key tile, first query tile, query tiles, steps
+  };
+  auto item_at = [&](int k, Item &it) {
+    if (k >= n_items) return false;
+    it.bkv = CAUSAL ? k % BHkv : k / n_blk;
+    it.jt = CAUSAL ? k / BHkv : k % n_blk;
+    it.it0 = CAUSAL ? it.jt : 0;
+    it.n_q = n_blk - it.it0;                 // query tiles per query head
+    it.n_it = group * it.n_q;                // (query head of the group, query tile) steps
+    return true;
+  };
+  auto q_head = [&](const Item &it, int t) {
+    return (it.bkv / H_kv) * H + (it.bkv % H_kv) * group + t / it.n_q;
+  };
+  auto q_tile = [&](const Item &it, int t) { return it.it0 + t % it.n_q; };
 
+  // Barrier phases run on across items: the stage ring counts stages over
+  // the CTA's whole sequence, S/dP/P count steps, K/V, K/V-free and done
+  // complete once per item.
   const uint32_t bar0 = sb + C::OFF_BAR;
-  const uint32_t B_KV = bar0;
-  auto B_FULL = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto B_EMPTY = [&](int s) { return bar0 + 8u * (1 + NST + s); };
-  const uint32_t bar1 = bar0 + 8u * (1 + 2 * NST);
+  const uint32_t B_KV = bar0;                                  // K, V of the item loaded
+  const uint32_t B_KVE = bar0 + 8u;                            // K, V slots free (epilogue stored)
+  auto B_FULL = [&](int s) { return bar0 + 8u * (2 + s); };
+  auto B_EMPTY = [&](int s) { return bar0 + 8u * (2 + NST + s); };
+  const uint32_t bar1 = bar0 + 8u * (2 + 2 * NST);
   auto B_S = [&](int h) { return bar1 + 8u * h; };          // S^T half h in TMEM
   auto B_DP = [&](int h) { return bar1 + 8u * (2 + h); };   // dP^T half h in TMEM
   auto B_P = [&](int h) { return bar1 + 8u * (4 + h); };    // P^T, dS^T half h written
-  const uint32_t B_DONE = bar1 + 48;
+  const uint32_t B_DONE = bar1 + 48;                           // item's last products done
   const uint32_t B_DRAIN = bar1 + 56;
+  auto B_IF = [&](int s) { return bar1 + 64 + 8u * s; };       // item slot s written
+  auto B_IE = [&](int s) { return bar1 + 64 + 8u * (kRing + s); };   // item slot s read by all
+  static_assert(2 + 2 * NST + 8 + 2 * kRing == C::NBAR, "barrier count");
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+  volatile int *item_ring = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 16);
+  // The t-th item of this CTA as the TMA warp published it (warp-uniform).
+  auto take_item = [&](int t, Item &it, bool &ok) {
+    const int s = t % kRing;
+    if (!__all_sync(0xffffffffu, mbar_wait(B_IF(s), (t / kRing) & 1, status, abort_flag))) {
+      ok = false;
+      return false;
+    }
+    const int k = item_ring[s];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(B_IE(s));
+    return item_at(k, it);
+  };
+  auto load_kv = [&](const Item &it) {
+    mbar_arrive_expect_tx(B_KV, 2 * C::TILE);
+    for (int kb = 0; kb < C::KB; ++kb) {
+      tma_load_3d(sb + C::OFF_K + kb * kBoxBytes, &tmK, kb * 64, it.jt * BT, it.bkv, B_KV);
+      tma_load_3d(sb + C::OFF_V + kb * kBoxBytes, &tmV, kb * 64, it.jt * BT, it.bkv, B_KV);
+    }
+  };
 
   if (threadIdx.x == kWarpTMA * 32) {
     mbar_init(B_KV, 1);
+    mbar_init(B_KVE, 1);
     for (int s = 0; s < NST; ++s) {
       mbar_init(B_FULL(s), 1);
       mbar_init(B_EMPTY(s), 1);
@@ -266,17 +309,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(B_DONE, 1);
     mbar_init(B_DRAIN, 1);
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(B_IF(s), 1);
+      mbar_init(B_IE(s), 1 + kComputeWarps);   // the MMA warp and every compute warp
+    }
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmdO);
-    mbar_arrive_expect_tx(B_KV, 2 * C::TILE);
-    for (int kb = 0; kb < C::KB; ++kb) {
-      tma_load_3d(sb + C::OFF_K + kb * kBoxBytes, &tmK, kb * 64, jt * BT, bkv, B_KV);
-      tma_load_3d(sb + C::OFF_V + kb * kBoxBytes, &tmV, kb * 64, jt * BT, bkv, B_KV);
-    }
+    tma_prefetch_desc(&tmdK);
+    tma_prefetch_desc(&tmdV);
+    Item it0;
+    if (item_at(static_cast<int>(blockIdx.x), it0)) load_kv(it0);   // (the grid is no larger than the item count)
   }
   if (warp == kWarpMMA) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -290,31 +336,66 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpTMA) {
     // ------------------------------------------------------------ TMA
     const bool leader = elect_one();
-    int issued = 0;
-    for (int t = 0; t < n_it; ++t) {
-      const int s = t % NST;
+    int g = 0;                               // stages issued so far
+    int kv_items = 1;                        // items whose K/V load was issued
+    bool ok = true;
+    int k = static_cast<int>(blockIdx.x);
+    auto load_stage = [&](const Item &it, int t) {
+      const int s = g % NST;
       if (!__all_sync(0xffffffffu,
-                      mbar_wait(B_EMPTY(s), ((t / NST) & 1) ^ 1u, status, abort_flag)))
-        break;
+                      mbar_wait(B_EMPTY(s), ((g / NST) & 1) ^ 1u, status, abort_flag)))
+        return false;
       if (leader) {
-        const int bh = q_head(t);
-        const int it = q_tile(t);
+        const int bh = q_head(it, t);
+        const int qt = q_tile(it, t);
         const uint32_t st = sb + C::OFF_STAGE + s * C::STAGE_BYTES;
         mbar_arrive_expect_tx(B_FULL(s), C::STAGE_TX);
         for (int kb = 0; kb < C::KB; ++kb) {
-          tma_load_3d(st + C::ST_Q + kb * kBoxBytes, &tmQ, kb * 64, it * BT, bh, B_FULL(s));
-          tma_load_3d(st + C::ST_DO + kb * kBoxBytes, &tmdO, kb * 64, it * BT, bh, B_FULL(s));
+          tma_load_3d(st + C::ST_Q + kb * kBoxBytes, &tmQ, kb * 64, qt * BT, bh, B_FULL(s));
+          tma_load_3d(st + C::ST_DO + kb * kBoxBytes, &tmdO, kb * 64, qt * BT, bh, B_FULL(s));
         }
-        const size_t row0 = static_cast<size_t>(bh) * N_pad + static_cast<size_t>(it) * BT;
+        const size_t row0 = static_cast<size_t>(bh) * N_pad + static_cast<size_t>(qt) * BT;
         bulk_load_1d(st + C::ST_LSE, lse2 + row0, BT * 4, B_FULL(s));
         bulk_load_1d(st + C::ST_DELTA, delta + row0, BT * 4, B_FULL(s));
       }
-      issued = t + 1;
+      ++g;
+      return true;
+    };
+    for (int t = 0; ok; ++t) {
+      const int s = t % kRing;
+      if (!(ok = __all_sync(0xffffffffu,
+                            mbar_wait(B_IE(s), ((t / kRing) & 1) ^ 1u, status, abort_flag))))
+        break;
+      if (leader) {
+        item_ring[s] = k;
+        mbar_arrive(B_IF(s));
+      }
+      __syncwarp();
+      Item it;
+      if (!item_at(k, it)) break;
+      // The item's first stages go out at once; its K and V once the
+      // previous item's epilogue has stored dK and dV out of their slots.
+      const int first = it.n_it < NST ? it.n_it : NST;
+      int u = 0;
+      for (; ok && u < first; ++u) ok = load_stage(it, u);
+      if (ok && t > 0) {
+        if (!(ok = __all_sync(0xffffffffu,
+                              mbar_wait(B_KVE, (t - 1) & 1, status, abort_flag))))
+          break;
+        if (leader) load_kv(it);
+        kv_items = t + 1;
+      }
+      for (; ok && u < it.n_it; ++u) ok = load_stage(it, u);
+      // This item's loads are all issued: claim the next one.
+      int kn = 0;
+      if (lane == 0) kn = G + static_cast<int>(atomicAdd(sched, 1u));
+      k = __shfl_sync(0xffffffffu, kn, 0);
     }
     if (leader && *abort_flag) {
-      mbar_wait_drain(B_KV, 0, 100000000ull);
-      for (int j = 0; j < NST && j < issued; ++j) {
-        const int tt = issued - 1 - j;
+      // Let every copy this warp started land before the CTA exits.
+      mbar_wait_drain(B_KV, (kv_items - 1) & 1, 100000000ull);
+      for (int j = 0; j < NST && j < g; ++j) {
+        const int tt = g - 1 - j;
         mbar_wait_drain(B_FULL(tt % NST), (tt / NST) & 1, 100000000ull);
       }
     }
@@ -378,36 +459,51 @@ __global__ void __launch_bounds__(kThreads, 1)
                        stm_lo + so + (C::ST_Q >> 4) + boff, hi, kIdescG, (acc || u > 0) ? 1u : 0u);
       }
     };
-    bool ok = wait_all(B_KV, 0) && wait_all(B_FULL(0), 0);
-    if (ok) {
-      tc_fence_after();
-      if (leader) {
-        issue_scores(0, 0);
-        issue_scores(0, 1);
-      }
-      __syncwarp();
-    }
-    for (int t = 0; ok && t < n_it; ++t) {
-      const int s = t % NST;
-      for (int h = 0; h < 2; ++h) {
-        // Half h's warps have read S^T / dP^T and written P^T / dS^T over
-        // them: accumulate, then reuse the half's regions for the next tile
-        // (MMAs from one thread run in issue order).
-        if (!(ok = wait_all(B_P(h), t & 1))) break;
+    bool ok = true;
+    int g = 0;                               // stages consumed so far (= steps before this item)
+    for (int t = 0; ok; ++t) {
+      Item it;
+      if (!take_item(t, it, ok)) break;
+      const int n_it = it.n_it;
+      // The item's K and V, and its first stage.  dV and dK of the previous
+      // item were read out by its epilogue before the compute warps handed
+      // over this item's first P^T / dS^T, so the first gradient products
+      // below may overwrite them.
+      ok = wait_all(B_KV, t & 1) && wait_all(B_FULL(g % NST), (g / NST) & 1);
+      if (ok) {
         tc_fence_after();
         if (leader) {
-          issue_grads(s, h, t > 0 || h > 0);
-          if (h == 1) mma_commit(t + 1 < n_it ? B_EMPTY(s) : B_DONE);
+          issue_scores(g % NST, 0);
+          issue_scores(g % NST, 1);
         }
         __syncwarp();
-        if (t + 1 < n_it) {
-          if (h == 0 && !(ok = wait_all(B_FULL((t + 1) % NST), ((t + 1) / NST) & 1)))
-            break;
+      }
+      for (int u = 0; ok && u < n_it; ++u) {
+        const int gs = g + u, s = gs % NST;
+        for (int h = 0; h < 2; ++h) {
+          // Half h's warps have read S^T / dP^T and written P^T / dS^T over
+          // them: accumulate, then reuse the half's regions for the next step
+          // (MMAs from one thread run in issue order).
+          if (!(ok = wait_all(B_P(h), gs & 1))) break;
           tc_fence_after();
-          if (leader) issue_scores((t + 1) % NST, h);
+          if (leader) {
+            issue_grads(s, h, u > 0 || h > 0);
+            if (h == 1) {
+              mma_commit(B_EMPTY(s));
+              if (u + 1 == n_it) mma_commit(B_DONE);
+            }
+          }
           __syncwarp();
+          if (u + 1 < n_it) {
+            const int g1 = gs + 1;
+            if (h == 0 && !(ok = wait_all(B_FULL(g1 % NST), (g1 / NST) & 1))) break;
+            tc_fence_after();
+            if (leader) issue_scores(g1 % NST, h);
+            __syncwarp();
+          }
         }
       }
+      g += n_it;
     }
     if (leader) {
       mma_commit(B_DRAIN);
@@ -421,80 +517,88 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = 32 * q + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
     bool ok = true;
-    for (int t = 0; t < n_it; ++t) {
-      const int s = t % NST;
-      const int it = q_tile(t);
-      ok = __all_sync(0xffffffffu, mbar_wait(B_FULL(s), (t / NST) & 1, status, abort_flag)) &&
-           __all_sync(0xffffffffu, mbar_wait(B_S(h), t & 1, status, abort_flag));
-      if (!ok) break;
-      tc_fence_after();
-      const float *lse_s =
-          reinterpret_cast<const float *>(smem + C::OFF_STAGE + s * C::STAGE_BYTES + C::ST_LSE);
-      const float *del_s =
-          reinterpret_cast<const float *>(smem + C::OFF_STAGE + s * C::STAGE_BYTES + C::ST_DELTA);
-      const bool diag = CAUSAL && it == jt;
-      // P^T for the half's 64 queries while the dP^T product is still running.
-      float p[64];
+    int g = 0;                               // steps of earlier items
+    for (int t = 0; ok; ++t) {
+      Item itm;
+      if (!take_item(t, itm, ok)) break;
+      for (int u = 0; u < itm.n_it; ++u) {
+        const int gs = g + u, s = gs % NST;
+        const int it = q_tile(itm, u);
+        ok = __all_sync(0xffffffffu, mbar_wait(B_FULL(s), (gs / NST) & 1, status, abort_flag)) &&
+             __all_sync(0xffffffffu, mbar_wait(B_S(h), gs & 1, status, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        const float *lse_s =
+            reinterpret_cast<const float *>(smem + C::OFF_STAGE + s * C::STAGE_BYTES + C::ST_LSE);
+        const float *del_s =
+            reinterpret_cast<const float *>(smem + C::OFF_STAGE + s * C::STAGE_BYTES + C::ST_DELTA);
+        const bool diag = CAUSAL && it == itm.jt;
+        // P^T for the half's 64 queries while the dP^T product is still running.
+        float p[64];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int col0 = 64 * h + 32 * c;
-        uint32_t sr[32];
-        tmem_ld_32cols(tmem + lane_base + C::TM_ST + col0, sr);
-        tmem_ld_wait_regs(sr);
+        for (int c = 0; c < 2; ++c) {
+          const int col0 = 64 * h + 32 * c;
+          uint32_t sr[32];
+          tmem_ld_32cols(tmem + lane_base + C::TM_ST + col0, sr);
+          tmem_ld_wait_regs(sr);
 #pragma unroll
-        for (int k = 0; k < 32; k += 4) {
-          const float4 lv = *reinterpret_cast<const float4 *>(lse_s + col0 + k);
-          const float lsev[4] = {lv.x, lv.y, lv.z, lv.w};
+          for (int k = 0; k < 32; k += 4) {
+            const float4 lv = *reinterpret_cast<const float4 *>(lse_s + col0 + k);
+            const float lsev[4] = {lv.x, lv.y, lv.z, lv.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float pe = ex2_approx(fmaf(__uint_as_float(sr[k + e]), scale_log2, -lsev[e]));
-            if (diag && col0 + k + e < row) pe = 0.f;   // query before key: masked
-            p[32 * c + k + e] = pe;
+            for (int e = 0; e < 4; ++e) {
+              float pe = ex2_approx(fmaf(__uint_as_float(sr[k + e]), scale_log2, -lsev[e]));
+              if (diag && col0 + k + e < row) pe = 0.f;   // query before key: masked
+              p[32 * c + k + e] = pe;
+            }
           }
         }
-      }
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(B_DP(h), t & 1, status, abort_flag)))) break;
-      tc_fence_after();
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(B_DP(h), gs & 1, status, abort_flag)))) break;
+        tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int col0 = 64 * h + 32 * c;
-        uint32_t dp[32];
-        tmem_ld_32cols(tmem + lane_base + C::TM_DPT + col0, dp);
-        tmem_ld_wait_regs(dp);
-        uint32_t pk[16], dk[16];
+        for (int c = 0; c < 2; ++c) {
+          const int col0 = 64 * h + 32 * c;
+          uint32_t dp[32];
+          tmem_ld_32cols(tmem + lane_base + C::TM_DPT + col0, dp);
+          tmem_ld_wait_regs(dp);
+          uint32_t pk[16], dk[16];
 #pragma unroll
-        for (int k = 0; k < 32; k += 4) {
-          const float4 dv = *reinterpret_cast<const float4 *>(del_s + col0 + k);
-          const float delv[4] = {dv.x, dv.y, dv.z, dv.w};
-          float ds[4];
+          for (int k = 0; k < 32; k += 4) {
+            const float4 dv = *reinterpret_cast<const float4 *>(del_s + col0 + k);
+            const float delv[4] = {dv.x, dv.y, dv.z, dv.w};
+            float ds[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            ds[e] = p[32 * c + k + e] * (__uint_as_float(dp[k + e]) - delv[e]);
-          pk[k / 2] = pack_bf16x2(p[32 * c + k], p[32 * c + k + 1]);
-          pk[k / 2 + 1] = pack_bf16x2(p[32 * c + k + 2], p[32 * c + k + 3]);
-          dk[k / 2] = pack_bf16x2(ds[0], ds[1]);
-          dk[k / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+            for (int e = 0; e < 4; ++e)
+              ds[e] = p[32 * c + k + e] * (__uint_as_float(dp[k + e]) - delv[e]);
+            pk[k / 2] = pack_bf16x2(p[32 * c + k], p[32 * c + k + 1]);
+            pk[k / 2 + 1] = pack_bf16x2(p[32 * c + k + 2], p[32 * c + k + 3]);
+            dk[k / 2] = pack_bf16x2(ds[0], ds[1]);
+            dk[k / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+          }
+          tmem_st_16cols(tmem + lane_base + C::TM_ST + 64 * h + 16 * c, pk);
+          tmem_st_16cols(tmem + lane_base + C::TM_DPT + 64 * h + 16 * c, dk);
         }
-        tmem_st_16cols(tmem + lane_base + C::TM_ST + 64 * h + 16 * c, pk);
-        tmem_st_16cols(tmem + lane_base + C::TM_DPT + 64 * h + 16 * c, dk);
+        tmem_st_wait();
+        // The stage's L / delta were read through the generic proxy and the
+        // next TMA refill writes them through the async proxy.
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(B_P(h));
       }
-      tmem_st_wait();
-      // The stage's L / delta were read through the generic proxy and the
-      // next TMA refill writes them through the async proxy.
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(B_P(h));
-    }
-    // Epilogue: dV and dK staged as bf16 in stage 0's Q and dO slots (every
-    // load into the ring has been consumed once the last products are done)
-    // and stored by TMA; the compute warps agree first, so that they all
-    // take part in the barrier or all skip it.
-    const bool okd = ok && __all_sync(0xffffffffu, mbar_wait(B_DONE, 0, status, abort_flag));
-    if (!named_bar_any(kEpiBar, 32 * kComputeWarps, !okd)) {
+      // Epilogue of the item: dV and dK staged as bf16 in the V and K slots
+      // (free once the item's last products are done) and stored by TMA; the
+      // storing thread then frees the slots for the next item's K and V.
+      // The compute warps agree first, so that they all take part in the
+      // barrier or all leave.
+      const bool okd = ok && __all_sync(0xffffffffu, mbar_wait(B_DONE, t & 1, status, abort_flag));
+      if (named_bar_any(kEpiBar, 32 * kComputeWarps, !okd)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
-      const uint32_t st_dv = sb + C::OFF_STAGE + C::ST_Q;
-      const uint32_t st_dk = sb + C::OFF_STAGE + C::ST_DO;
+      const uint32_t st_dv = sb + C::OFF_V;
+      const uint32_t st_dk = sb + C::OFF_K;
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         uint32_t r[32];
@@ -506,16 +610,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         stage_row32(st_dk, row, h * (D / 2) + 32 * c, r, scale);
       }
       fence_proxy_async_smem();
+      tc_fence_before();
       named_bar_sync(kEpiBar, 32 * kComputeWarps);
       if (threadIdx.x == 0) {
 #pragma unroll
         for (int kb = 0; kb < C::KB; ++kb) {
-          tma_store_3d(&tmdV, kb * 64, jt * BT, bkv, st_dv + kb * kBoxBytes);
-          tma_store_3d(&tmdK, kb * 64, jt * BT, bkv, st_dk + kb * kBoxBytes);
+          tma_store_3d(&tmdV, kb * 64, itm.jt * BT, itm.bkv, st_dv + kb * kBoxBytes);
+          tma_store_3d(&tmdK, kb * 64, itm.jt * BT, itm.bkv, st_dk + kb * kBoxBytes);
         }
         bulk_commit_group();
         bulk_wait_group_read0();
+        mbar_arrive(B_KVE);
       }
+      g += itm.n_it;
     }
   }
   tc_fence_before();
@@ -523,6 +630,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpMMA) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  }
+  // Every claim of this CTA is behind it: the last CTA to get here resets
+  // the item counter (sched[0]) and this count (sched[1]) for the next launch.
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(sched + 1, 1u) == gridDim.x - 1) {
+      atomicExch(sched, 0u);
+      atomicExch(sched + 1, 0u);
+    }
   }
 }
 
@@ -821,8 +937,15 @@ static cudaError_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const 
   if (e != cudaSuccess) return e;
   e = smem_limit_once(kq, static_cast<int>(CfgQ<D>::SMEM_ALLOC), set_q);
   if (e != cudaSuccess) return e;
-  kkv<<<static_cast<unsigned>(B * H_kv * n_blk), kThreads, CfgKV<D>::SMEM_ALLOC, stream>>>(
-      mq, mk, mv, mdo, mdk, mdv, lse2, delta, N, N_pad, H, H_kv, n_blk, scale_log2, scale, status);
+  // dK/dV: persistent, one CTA per SM (at most one per item).
+  unsigned *sched = nullptr;
+  e = sched_slot(&sched);
+  if (e != cudaSuccess) return e;
+  const long long kv_items = static_cast<long long>(B) * H_kv * n_blk;
+  const long long kv_grid = kv_items < sm_count() ? kv_items : sm_count();
+  kkv<<<static_cast<unsigned>(kv_grid), kThreads, CfgKV<D>::SMEM_ALLOC, stream>>>(
+      mq, mk, mv, mdo, mdk, mdv, lse2, delta, N, N_pad, H, H_kv, B * H_kv, n_blk, scale_log2,
+      scale, status, sched);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   kq<<<static_cast<unsigned>(B * H * n_blk), kThreads, CfgQ<D>::SMEM_ALLOC, stream>>>(
