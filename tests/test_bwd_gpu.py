@@ -128,3 +128,24 @@ def test_bwd_workload_sampled():
         _assert_grad_close(dq[b, h], rq[t], f"dQ head {flat}")
         _assert_grad_close(dk[b, h], rk[t], f"dK head {flat}")
         _assert_grad_close(dv[b, h], rv[t], f"dV head {flat}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_many_short_items_per_persistent_cta(causal):
+    """The persistent dK/dV kernel over far more (K/V head, key tile) items
+    than SMs, two key tiles per head: each CTA runs many items in a row, with
+    dK/dV leaving through the K/V slots that the next item reloads.  Batches
+    at the start, middle and end of the item order are checked against the
+    oracle in full."""
+    B, H, H_kv, N, d = 96, 4, 2, 200, 128   # 192 K/V heads x 2 key tiles = 384 items
+    q, k, v, do = bwd_inputs(B, H, N, d, seed=77 + causal, device="cuda", H_kv=H_kv)
+    scale = d ** -0.5
+    o, lse = _oracle_fwd(q, k, v, scale, causal)
+    dq, dk, dv = _bwd(q, k, v, o, do, lse, causal, scale)
+    for b in (0, 47, B - 1):
+        rq, rk, rv = oracle.attention_backward(to_f64(q[b:b + 1]), to_f64(k[b:b + 1]),
+                                               to_f64(v[b:b + 1]), to_f64(do[b:b + 1]), scale,
+                                               causal)
+        _assert_grad_close(dq[b:b + 1], rq, "dQ")
+        _assert_grad_close(dk[b:b + 1], rk, "dK")
+        _assert_grad_close(dv[b:b + 1], rv, "dV")

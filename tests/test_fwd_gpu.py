@@ -180,3 +180,20 @@ def test_concurrent_launches_on_several_streams():
     for (o, lse), (o_ref, l_ref) in zip(outs, refs):
         assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
     assert ea.attn_get_device_status() == 0
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_many_short_items_per_persistent_cta(d, causal):
+    """A grid of one CTA per SM over far more (head, query block) items than
+    SMs, each only one or two K/V tiles long: every CTA runs a long sequence
+    of items, so item hand-over, the per-item barrier phases and the reuse of
+    Q, staging and accumulators across items are all exercised.  Heads at the
+    start, middle and end of the item order are checked in full."""
+    B, H, N = 24, 32, 200                # 768 heads, 768 items
+    q, k, v = fwd_inputs(B, H, N, d, 61 + d + causal, device="cuda")
+    scale = d ** -0.5
+    o, lse = _run(q, k, v, causal, scale)
+    heads = [0, 1, 151, 152, 383, 384, 700, B * H - 1]
+    O_ref, L_ref = oracle_fwd(q, k, v, scale, causal, heads=heads)
+    assert_within(compare_fwd(o, lse, O_ref, L_ref, heads, None))
