@@ -503,13 +503,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             // O_i is quiescent: the MMA that wrote it last was committed
             // before S_i was.
 #pragma unroll 1
-            for (int c = 0; c < (kIndep ? D / 32 : D / 64); ++c) {
-              uint32_t o[32];
-              tmem_ld_32cols(o_blk + c * 32, o);
-              tmem_ld_wait_regs(o);
+            for (int c = 0; c < (kIndep ? D / 16 : D / 64); ++c) {
+              if constexpr (kIndep) {   // (16 columns at a time: fewer live registers)
+                uint32_t o[16];
+                tmem_ld_16cols(o_blk + c * 16, o);
+                tmem_ld_wait_regs16(o);
 #pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-              tmem_st_32cols(o_blk + c * 32, o);
+                for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                tmem_st_16cols(o_blk + c * 16, o);
+              } else {
+                uint32_t o[32];
+                tmem_ld_32cols(o_blk + c * 32, o);
+                tmem_ld_wait_regs(o);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                tmem_st_32cols(o_blk + c * 32, o);
+              }
             }
           }
         }
@@ -558,31 +567,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t stage = stage_base + static_cast<uint32_t>(r) * 128;
       const uint32_t o_addr = tmem + lane_addr + C::TMEM_O + (kIndep ? 2 * i * D : i * D) + h * (D / 2);
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        uint32_t o[32], o1[32];
-        tmem_ld_32cols(o_addr + c * 32, o);
-        if (kIndep) tmem_ld_32cols(o_addr + D + c * 32, o1);
-        tmem_ld_wait_regs(o);
-        if (kIndep) {
-          reg_fence32(o1);
+      if constexpr (kIndep) {
+        // 16 columns of each half's accumulator at a time (both are live).
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[16], o1[16];
+          tmem_ld_16cols(o_addr + c * 16, o);
+          tmem_ld_16cols(o_addr + D + c * 16, o1);
+          tmem_ld_wait_regs16(o);
+          reg_fence16(o1);
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
             o[e] = __float_as_uint(__uint_as_float(o[e]) * a0 + __uint_as_float(o1[e]) * a1);
-        } else {
+#pragma unroll
+          for (int v = 0; v < 2; ++v) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w[e] = pack_bf16x2(__uint_as_float(o[8 * v + 2 * e]), __uint_as_float(o[8 * v + 2 * e + 1]));
+            const int col = h * (D / 2) + c * 16 + v * 8;   // first of these 8 columns
+            const uint32_t chunk = static_cast<uint32_t>((col & 63) >> 3) ^ static_cast<uint32_t>(r & 7);
+            st_shared_v4(stage + (col >> 6) * kBoxBytes + (chunk << 4), w[0], w[1], w[2], w[3]);
+          }
+          __syncwarp();
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t o[32];
+          tmem_ld_32cols(o_addr + c * 32, o);
+          tmem_ld_wait_regs(o);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * inv_l);
-        }
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          uint32_t w[4];
+          for (int v = 0; v < 4; ++v) {
+            uint32_t w[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            w[e] = pack_bf16x2(__uint_as_float(o[8 * v + 2 * e]), __uint_as_float(o[8 * v + 2 * e + 1]));
-          const int col = h * (D / 2) + c * 32 + v * 8;   // first of these 8 columns
-          const uint32_t chunk = static_cast<uint32_t>((col & 63) >> 3) ^ static_cast<uint32_t>(r & 7);
-          st_shared_v4(stage + (col >> 6) * kBoxBytes + (chunk << 4), w[0], w[1], w[2], w[3]);
+            for (int e = 0; e < 4; ++e)
+              w[e] = pack_bf16x2(__uint_as_float(o[8 * v + 2 * e]), __uint_as_float(o[8 * v + 2 * e + 1]));
+            const int col = h * (D / 2) + c * 32 + v * 8;   // first of these 8 columns
+            const uint32_t chunk = static_cast<uint32_t>((col & 63) >> 3) ^ static_cast<uint32_t>(r & 7);
+            st_shared_v4(stage + (col >> 6) * kBoxBytes + (chunk << 4), w[0], w[1], w[2], w[3]);
+          }
+          __syncwarp();
         }
-        __syncwarp();
       }
       fence_proxy_async_smem();
       tc_fence_before();
