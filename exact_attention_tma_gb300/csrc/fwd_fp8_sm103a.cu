@@ -42,6 +42,9 @@ __device__ __forceinline__ int vt_swz(int k) {   // word-column swizzle of key r
 __global__ void __launch_bounds__(256)
     attn_fp8_vt_kernel(const uint8_t *__restrict__ V, uint8_t *__restrict__ VT, int N, int N_pad) {
   __shared__ uint4 tile[128 * 8];      // [key][8 quads of 4 words], quad index swizzled
+  // Every block of this pass is running: the forward kernel launched after it
+  // may start (it waits for this pass's results before its first V^T load).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const size_t bh = blockIdx.y;
   const int k0 = blockIdx.x * 128;
   const uint8_t *src = V + (bh * N + k0) * D;

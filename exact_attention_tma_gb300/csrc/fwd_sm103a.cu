@@ -353,6 +353,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       load_k(it0.kvh, 0, 0);
       for (int i = 1; i < QT; ++i) load_q(it0, i);
       mbar_arrive_expect_tx(B_VF(0), C::KV_BYTES);
+      // FP8: V^T comes from the transpose pass launched just before this
+      // kernel, which may still be finishing (programmatic dependent launch).
+      if constexpr (F8) asm volatile("griddepcontrol.wait;" ::: "memory");
       load_v(it0.kvh, 0, 0);
     }
   }
@@ -644,6 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     if (warp == kWarpTMA) {
       // ------------------------------------------------------ TMA producer
+      if constexpr (F8) asm volatile("griddepcontrol.wait;" ::: "memory");
       // (The first item's Q tiles and first K/V tile were issued before the
       // CTA-wide barrier.)  Q_i of a later item waits until the previous
       // item's epilogue of tile i has released the buffer.
@@ -938,6 +942,23 @@ static cudaError_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const 
   unsigned *sched = nullptr;
   e = sched_slot(&sched);
   if (e != cudaSuccess) return e;
+  if constexpr (F8) {
+    // Launched while the V^T pass before it is still running (it signals
+    // once all of its blocks have started): the set-up and the Q and K loads
+    // overlap the pass's end, and the first V^T load waits for its results.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, LSE, N, BH, n_blk, H, group, scale_log2,
+                              out_mul, status, sched);
+  }
   kern<<<static_cast<unsigned>(grid), kThreads, C::SMEM_ALLOC, stream>>>(
       mq, mk, mv, mo, LSE, N, BH, n_blk, H, group, scale_log2, out_mul, status, sched);
   return cudaGetLastError();

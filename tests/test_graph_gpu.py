@@ -99,3 +99,23 @@ def test_graph_replays_backward():
     ea.attn_bwd_ws(q, k, v, o, do, lse, *r, True, 0.09, ws)
     torch.cuda.synchronize()
     assert torch.equal(dq, r[0]) and torch.equal(dk, r[1]) and torch.equal(dv, r[2])
+
+
+def test_graph_replays_fp8_forward():
+    """The FP8 forward is two launches, the second a dependent launch that
+    may start before the V transpose has finished; captured, it replays to
+    the result of a direct call."""
+    from exact_attention_tma_gb300.inputs import fp8_inputs
+
+    (q8, k8, v8), ds = fp8_inputs(2, 4, 700, 128, seed=46, device="cuda")
+    o = torch.empty(q8.shape, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(q8.shape[:3], dtype=torch.float32, device="cuda")
+    g = _capture(lambda s: ea.attn_fwd_fp8(q8, k8, v8, o, lse, True, 0.09, *ds, stream=s))
+    (q2, k2, v2), _ = fp8_inputs(2, 4, 700, 128, seed=47, device="cuda")
+    q8.copy_(q2), k8.copy_(k2), v8.copy_(v2)
+    g.replay()
+    torch.cuda.synchronize()
+    o_ref, l_ref = torch.empty_like(o), torch.empty_like(lse)
+    ea.attn_fwd_fp8(q8, k8, v8, o_ref, l_ref, True, 0.09, *ds)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
