@@ -139,6 +139,10 @@ __global__ void __launch_bounds__(kPrepThreads)
   const size_t bh = blockIdx.x;                       // one head per grid row
   const __nv_bfloat16 *Oh = O + bh * N * D;
   const __nv_bfloat16 *dOh = dO + bh * N * D;
+  // The dK/dV kernel is a programmatic dependent of this one: it may take
+  // the SMs this grid leaves and set up; it waits for this grid's rows
+  // before it loads them.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (int i0 = static_cast<int>(blockIdx.y) * 2 * RPB; i0 < N_pad;
        i0 += static_cast<int>(gridDim.y) * 2 * RPB) {
     int ii[2];
@@ -332,9 +336,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // The dQ kernel may launch as SMs free up; it reads nothing this grid
+  // writes, and it waits for this grid (and so for the row pass) before it
+  // reads L and delta.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == kWarpTMA) {
     // ------------------------------------------------------------ TMA
+    // L and delta come from the row pass launched just before this kernel
+    // (programmatic dependent launch): wait for it before the first load.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const bool leader = elect_one();
     int g = 0;                               // stages issued so far
     int kv_items = 1;                        // items whose K/V load was issued
@@ -821,6 +832,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = 32 * q + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
     const size_t prow = static_cast<size_t>(bh) * N_pad + static_cast<size_t>(it) * BT + row;
+    // This kernel is a programmatic dependent of the dK/dV kernel, which
+    // itself waited for the row pass: once that grid has finished, the
+    // row pass's L and delta are complete too.  Q, dO, K and V are inputs,
+    // so the loads and the first products need not wait.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const float l2 = lse2[prow];
     const float dl = delta[prow];
     {
@@ -943,15 +959,27 @@ static cudaError_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const 
   if (e != cudaSuccess) return e;
   const long long kv_items = static_cast<long long>(B) * H_kv * n_blk;
   const long long kv_grid = kv_items < sm_count() ? kv_items : sm_count();
-  kkv<<<static_cast<unsigned>(kv_grid), kThreads, CfgKV<D>::SMEM_ALLOC, stream>>>(
-      mq, mk, mv, mdo, mdk, mdv, lse2, delta, N, N_pad, H, H_kv, B * H_kv, n_blk, scale_log2,
-      scale, status, sched);
-  e = cudaGetLastError();
+  // Both kernels are programmatic dependents of the launch before them on
+  // the stream (row pass -> dK/dV -> dQ): set-up overlaps the previous
+  // grid's tail, and each waits for its predecessor before using its rows.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(kv_grid));
+  cfg.dynamicSmemBytes = CfgKV<D>::SMEM_ALLOC;
+  e = cudaLaunchKernelEx(&cfg, kkv, mq, mk, mv, mdo, mdk, mdv, lse2, delta, N, N_pad, H, H_kv,
+                         B * H_kv, n_blk, scale_log2, scale, status, sched);
   if (e != cudaSuccess) return e;
-  kq<<<static_cast<unsigned>(B * H * n_blk), kThreads, CfgQ<D>::SMEM_ALLOC, stream>>>(
-      mk, mv, mdq, static_cast<const __nv_bfloat16 *>(Q), static_cast<const __nv_bfloat16 *>(dO),
-      lse2, delta, N, N_pad, H, H_kv, n_blk, scale_log2, scale, status);
-  return cudaGetLastError();
+  cfg.gridDim = dim3(static_cast<unsigned>(B * H * n_blk));
+  cfg.dynamicSmemBytes = CfgQ<D>::SMEM_ALLOC;
+  return cudaLaunchKernelEx(&cfg, kq, mk, mv, mdq, static_cast<const __nv_bfloat16 *>(Q),
+                            static_cast<const __nv_bfloat16 *>(dO), lse2, delta, N, N_pad, H,
+                            H_kv, n_blk, scale_log2, scale, status);
 }
 
 }  // namespace bwd
