@@ -90,6 +90,9 @@ __global__ void __launch_bounds__(kThreads)
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // The combine kernel is a programmatic dependent of this grid: it may
+  // launch once every CTA has started, and waits for this grid's partials.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int group = H / H_kv;
   const int n_hc = (group + kRows - 1) / kRows;      // query-head chunks per K/V head

@@ -45,6 +45,9 @@ __global__ void __launch_bounds__(kWarps * 32)
   constexpr int KPI = 32 / LPK;       // keys per warp-wide load
   constexpr int G = kWarps * KPI;     // lane groups per CTA
   constexpr int BATCH = kWarps * KPI * kUnroll;
+  // The combine kernel is a programmatic dependent of this grid: it may
+  // launch once every CTA has started, and waits for this grid's partials.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // 1-D grid: consecutive CTAs read consecutive chunks of one head.
   const int split = blockIdx.x % nsplit;
   const int bh = blockIdx.x / nsplit;
@@ -173,6 +176,9 @@ __global__ void __launch_bounds__(128)
                                __nv_bfloat16 *__restrict__ O, int BH, int nsplit) {
   const int head = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+  // Launched as a programmatic dependent of the split kernel: wait for its
+  // partials (a no-op when the previous launch did not allow it to start early).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (head >= BH) return;
   const float lse = (lane < nsplit) ? ws_lse[static_cast<size_t>(head) * nsplit + lane] : -INFINITY;
   float mx = lse;
@@ -248,6 +254,9 @@ __global__ void __launch_bounds__(kWarps * 32)
   constexpr int KPI = 32 / LPK;          // keys per warp-wide load
   constexpr int NG = kWarps * KPI;       // lane groups per CTA
   constexpr int BATCH = NG * U;
+  // The combine kernel is a programmatic dependent of this grid: it may
+  // launch once every CTA has started, and waits for this grid's partials.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int group = H / H_kv;
   const int n_hc = group / GQ;           // query-head chunks per K/V head
   const int split = blockIdx.x % nsplit;
@@ -431,22 +440,28 @@ static cudaError_t launch_t(const void *q, const void *Kc, const void *Vc, void 
       static_cast<const __nv_bfloat16 *>(Vc), ws_o, ws_lse, L, chunk, nsplit, scale_log2);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_decode_combine_kernel<D><<<(BH + 3) / 4, 128, 0, stream>>>(
-      ws_o, ws_lse, static_cast<__nv_bfloat16 *>(O), BH, nsplit);
-  return cudaGetLastError();
+  return launch_decode_combine(ws_o, ws_lse, O, BH, D, nsplit, stream);
 }
 
 }  // namespace dec
 
 cudaError_t launch_decode_combine(const float *ws_o, const float *ws_lse, void *O, int BH, int d,
                                   int nsplit, cudaStream_t stream) {
+  // Programmatic dependent launch: the combine grid may be resident before
+  // the split grid ends; the kernel waits for it before reading.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((BH + 3) / 4));
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(O);
   if (d == 128)
-    dec::attn_decode_combine_kernel<128><<<(BH + 3) / 4, 128, 0, stream>>>(
-        ws_o, ws_lse, static_cast<__nv_bfloat16 *>(O), BH, nsplit);
-  else
-    dec::attn_decode_combine_kernel<64><<<(BH + 3) / 4, 128, 0, stream>>>(
-        ws_o, ws_lse, static_cast<__nv_bfloat16 *>(O), BH, nsplit);
-  return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, dec::attn_decode_combine_kernel<128>, ws_o, ws_lse, o, BH, nsplit);
+  return cudaLaunchKernelEx(&cfg, dec::attn_decode_combine_kernel<64>, ws_o, ws_lse, o, BH, nsplit);
 }
 
 size_t decode_ws_bytes(int B, int H, int d) {
@@ -482,9 +497,7 @@ static cudaError_t launch_gqa_d(const void *q, const void *Kc, const void *Vc, v
   else
     e = launch_gqa_t<D, 1, PAGED>(q, Kc, Vc, B, H, H_kv, L, scale_log2, ws_o, ws_lse, pg, stream);
   if (e != cudaSuccess) return e;
-  attn_decode_combine_kernel<D><<<(BH + 3) / 4, 128, 0, stream>>>(
-      ws_o, ws_lse, static_cast<__nv_bfloat16 *>(O), BH, nsplit);
-  return cudaGetLastError();
+  return launch_decode_combine(ws_o, ws_lse, O, BH, D, nsplit, stream);
 }
 }  // namespace dec
 
