@@ -38,14 +38,27 @@ constexpr int kWarpTMA = kComputeWarps;
 constexpr int kThreads = (kComputeWarps + 1) * 32;
 constexpr int kRows = 16;            // query heads per CTA (M of the MMAs)
 
-// Splits per (batch, K/V head, head chunk): about 1024 keys per CTA, more
-// (up to 32, never below 64 keys each) while the grid would not cover every SM
-// once.  Long CTAs amortise the set-up and the merge; measured B16 H64 H_kv8
-// L8192: 8 splits 4.97 TB/s vs 32 splits 4.74; B64 L4096: 5.88 vs 4.17.
-static int choose_splits(long long units, int L, int n_sm) {
-  int s = (L + 1023) / 1024;
+// Splits per (batch, K/V head, head chunk).  The split CTAs of a call run
+// best as one resident wave of about 5/3 CTAs per SM at d = 128 (twice as
+// many at d = 64, whose CTAs are half the size), each as long as possible.
+// Measured on eight shapes (B 1..64, L 2k..64k, g 8 and 16): B16 H64 H_kv8
+// L8192 86 us with 2 splits (256 CTAs) against 94 us with 8; B1 L65536 best
+// at 32 splits (256 CTAs); B32 L2048 best unsplit (256 CTAs).  When the
+// units alone exceed that, one split each while they fit in one wave
+// (slots = SMs x resident CTAs per SM), and ~1024 keys per CTA beyond it
+// (B64 H64 H_kv8 L4096: 4 splits, 2048 CTAs, 6.5 TB/s against 6.0 unsplit).
+static int choose_splits(long long units, int L, int n_sm, int slots, int D) {
+  const long long target = (5LL * n_sm * (128 / D)) / 3;
+  int s;
+  if (units < target) {
+    s = static_cast<int>((target + units / 2) / units);   // nearest
+  } else if (units <= slots) {
+    s = 1;
+  } else {
+    s = (L + 1023) / 1024;
+  }
   s = s < 1 ? 1 : (s > kDecodeSplits ? kDecodeSplits : s);
-  while (units * s < n_sm && 2 * s <= kDecodeSplits && L / (2 * s) >= kTile) s *= 2;
+  while (s > 1 && L / s < kTile) --s;   // at least one whole tile of keys per split
   return s;   // 1 <= s <= kDecodeSplits: the workspace holds kDecodeSplits per head
 }
 
@@ -391,7 +404,16 @@ static cudaError_t launch_t(const void *q, const void *Kc, const void *Vc, void 
   const int n_sm = sm_count();
   const int group = H / H_kv;
   const long long units = static_cast<long long>(B) * H_kv * ((group + kRows - 1) / kRows);
-  const int nsplit = choose_splits(units, L, n_sm);
+  static std::atomic<int> per_sm{0};   // resident CTAs per SM (a property of the kernel)
+  int occ = per_sm.load();
+  if (occ == 0) {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads,
+                                                      static_cast<size_t>(C::SMEM_ALLOC));
+    if (e != cudaSuccess) return e;
+    if (occ < 1) occ = 1;
+    per_sm.store(occ);
+  }
+  const int nsplit = choose_splits(units, L, n_sm, n_sm * occ, D);
   if (nsplit < 1 || nsplit > kDecodeSplits) return cudaErrorInvalidValue;
   int chunk = (L + nsplit - 1) / nsplit;
   if (PAGED) chunk = (chunk + kTile - 1) / kTile * kTile;   // tiles start on 64-key rows
