@@ -413,11 +413,27 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
 }
 
+// Split count for the CUDA-core split kernels: the power of two nearest (in
+// ratio) to target / units CTAs per unit, at least 4 and at most
+// kDecodeSplits, halved while a split would hold fewer than 64 keys.  The
+// targets are measured: the contiguous multi-head kernel runs best with
+// ~108 CTAs per SM in flight over the call (B16 H32 L8192: 32 splits; B64
+// H32 L2048: 8 splits, 7.09 against 6.64 TB/s with 32), the paged kernel with
+// ~13 (B16 H32 L8192, 64-token pages: 4 splits, 5.99 against 5.79 TB/s; B64
+// L2048: 5.97 against 4.70; B4: 16 splits, 5.35 against 5.04).
+static int pow2_splits(long long units, long long target, int L) {
+  int s = 1;
+  while (s < kDecodeSplits && 1.41421356 * static_cast<double>(units) * s < static_cast<double>(target))
+    s *= 2;
+  if (s < 4) s = 4;
+  while (s > 1 && L / s < 64) s /= 2;
+  return s;
+}
+
 template <int D, int GQ, bool PAGED>
 static cudaError_t launch_gqa_t(const void *q, const void *Kc, const void *Vc, int B, int H, int H_kv,
-                                int L, float scale_log2, float *ws_o, float *ws_lse,
+                                int L, float scale_log2, float *ws_o, float *ws_lse, int nsplit,
                                 const Paging &pg, cudaStream_t stream) {
-  const int nsplit = kDecodeSplits;
   const int chunk = (L + nsplit - 1) / nsplit;
   const long long grid = static_cast<long long>(B) * H_kv * (H / H_kv / GQ) * nsplit;
   attn_decode_gqa_split_kernel<D, GQ, PAGED>
@@ -431,7 +447,7 @@ static cudaError_t launch_gqa_t(const void *q, const void *Kc, const void *Vc, i
 template <int D>
 static cudaError_t launch_t(const void *q, const void *Kc, const void *Vc, void *O, int BH, int L,
                             float scale_log2, void *ws, cudaStream_t stream) {
-  const int nsplit = kDecodeSplits;
+  const int nsplit = pow2_splits(BH, 108LL * sm_count(), L);
   const int chunk = (L + nsplit - 1) / nsplit;
   float *ws_o = static_cast<float *>(ws);
   float *ws_lse = ws_o + static_cast<size_t>(BH) * nsplit * D;
@@ -482,20 +498,26 @@ static cudaError_t launch_gqa_d(const void *q, const void *Kc, const void *Vc, v
                                 int H_kv, int L, float scale_log2, void *ws, const Paging &pg,
                                 cudaStream_t stream) {
   const int BH = B * H;
-  const int nsplit = kDecodeSplits;
+  const int group = H / H_kv;
+  const int gq = group % 8 == 0 ? 8 : group % 4 == 0 ? 4 : group % 2 == 0 ? 2 : 1;
+  const int nsplit =
+      PAGED ? pow2_splits(static_cast<long long>(BH) / gq, 13LL * sm_count(), L) : kDecodeSplits;
   float *ws_o = static_cast<float *>(ws);
   float *ws_lse = ws_o + static_cast<size_t>(BH) * nsplit * D;
-  const int group = H / H_kv;
   // Query heads per CTA: the largest of 8, 4, 2 dividing the group size.
   cudaError_t e;
   if (group % 8 == 0)
-    e = launch_gqa_t<D, 8, PAGED>(q, Kc, Vc, B, H, H_kv, L, scale_log2, ws_o, ws_lse, pg, stream);
+    e = launch_gqa_t<D, 8, PAGED>(q, Kc, Vc, B, H, H_kv, L, scale_log2, ws_o, ws_lse, nsplit, pg,
+                                  stream);
   else if (group % 4 == 0)
-    e = launch_gqa_t<D, 4, PAGED>(q, Kc, Vc, B, H, H_kv, L, scale_log2, ws_o, ws_lse, pg, stream);
+    e = launch_gqa_t<D, 4, PAGED>(q, Kc, Vc, B, H, H_kv, L, scale_log2, ws_o, ws_lse, nsplit, pg,
+                                  stream);
   else if (group % 2 == 0)
-    e = launch_gqa_t<D, 2, PAGED>(q, Kc, Vc, B, H, H_kv, L, scale_log2, ws_o, ws_lse, pg, stream);
+    e = launch_gqa_t<D, 2, PAGED>(q, Kc, Vc, B, H, H_kv, L, scale_log2, ws_o, ws_lse, nsplit, pg,
+                                  stream);
   else
-    e = launch_gqa_t<D, 1, PAGED>(q, Kc, Vc, B, H, H_kv, L, scale_log2, ws_o, ws_lse, pg, stream);
+    e = launch_gqa_t<D, 1, PAGED>(q, Kc, Vc, B, H, H_kv, L, scale_log2, ws_o, ws_lse, nsplit, pg,
+                                  stream);
   if (e != cudaSuccess) return e;
   return launch_decode_combine(ws_o, ws_lse, O, BH, D, nsplit, stream);
 }

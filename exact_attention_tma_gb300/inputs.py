@@ -32,7 +32,7 @@ class Workload:
     seed: int
     qk_std: float = 1.0  # Q and K are N(0, qk_std^2)
     v_dist: str = "normal"   # "normal": N(0,1); "uniform": U(-1, 1)
-    nsplit: int = 0      # decode only: KV splits per head
+    nsplit: int = 0      # decode only: KV split slots per head (calls use at most this many)
     scale: float = field(default=0.0)
     H_kv: int = 0        # K/V heads (grouped-query attention); 0 means H_kv = H
     page_size: int = 0   # paged decode only: tokens per page

@@ -299,7 +299,10 @@ attn_status attn_get_device_status(cudaStream_t stream);
 /* Static, NUL-terminated description of a status code. */
 const char *attn_status_string(attn_status status);
 
-/* Number of KV splits attn_decode uses per head (32). */
+/* Most KV splits a decode call uses per head (32): the workspace holds this
+ * many partials per head.  Each call picks its own count from the shape (one
+ * resident wave of split CTAs for the tensor-core grouped kernel; a power of
+ * two from 4 to 32 for the CUDA-core kernels). */
 int attn_decode_num_splits(void);
 
 #ifdef __cplusplus
