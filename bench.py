@@ -462,11 +462,22 @@ def run_ours(args, rank, world, local_rank):
     return record
 
 
-def per_config(ea, peaks, dev, stream, reps=10):
-    """Each performance workload on its own: median over `reps` launches with an
-    L2 flush between launches: a 256 MB write, then a read of the same buffer,
-    so that the dirty lines the write leaves in L2 are written back before the
-    timed call rather than during it."""
+def _pct(xs, q):
+    """q-th percentile (0-100) of xs by linear interpolation between order statistics."""
+    ys = sorted(xs)
+    pos = (len(ys) - 1) * q / 100.0
+    lo = int(pos)
+    hi = min(lo + 1, len(ys) - 1)
+    return ys[lo] + (ys[hi] - ys[lo]) * (pos - lo)
+
+
+def per_config(ea, peaks, dev, stream, reps=20, warmup=20):
+    """Each performance workload on its own: `warmup` untimed launches, then
+    `reps` timed launches (CUDA events on the launching stream) with an L2
+    flush before each: a 256 MB write, then a read of the same buffer, so that
+    the dirty lines the write leaves in L2 are written back before the timed
+    call rather than during it.  Reports the median, p10 and p90 of the
+    launch times, and the roofline fraction of the median."""
     import torch
 
     from exact_attention_tma_gb300.inputs import WORKLOADS, workload_inputs
@@ -513,7 +524,7 @@ def per_config(ea, peaks, dev, stream, reps=10):
             fn = ea.attn_decode_gqa if gqa else ea.attn_decode
             call = lambda: fn(*ins, o, w.scale, stream)  # noqa: E731
             flops, nbytes = dec_work(w)
-        for _ in range(3):
+        for _ in range(warmup):
             call()
         times = []
         for _ in range(reps):
@@ -531,7 +542,9 @@ def per_config(ea, peaks, dev, stream, reps=10):
             roof = max(flops / (2 * peaks["bf16_tflops"] * 1e12), nbytes / (peaks["hbm_gbs"] * 1e9))
         else:
             roof = roof_time(flops, nbytes, peaks)
-        rec = {"median_us": t * 1e6, "roofline_us": roof * 1e6, "frac_of_roofline": roof / t}
+        rec = {"median_us": t * 1e6, "p10_us": _pct(times, 10) * 1e6,
+               "p90_us": _pct(times, 90) * 1e6, "samples": len(times), "warmup": warmup,
+               "roofline_us": roof * 1e6, "frac_of_roofline": roof / t}
         if w.kind in ("fwd", "bwd", "fp8"):
             rec["tflops"] = flops / t / 1e12
         else:

@@ -110,6 +110,11 @@ cudaError_t ea::device_status_word(unsigned **out) {
   return status_ptr(out) == ATTN_OK ? cudaSuccess : cudaErrorUnknown;
 }
 
+int ea::check_decode_args(const void *q, const void *K, const void *V, const void *O, int B, int H,
+                          int L, int d, float scale) {
+  return static_cast<int>(check_decode(q, K, V, O, B, H, L, d, scale));
+}
+
 extern "C" {
 
 attn_status attn_fwd_gqa(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
@@ -364,6 +369,7 @@ attn_status attn_get_device_status(cudaStream_t stream) {
   if (v != 0 && cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
     return ATTN_ERR_CUDA;
   if (v & ea::kStatusTimeoutBit) return ATTN_ERR_TIMEOUT;
+  if (v & ea::kStatusSetupBit) return ATTN_ERR_CUDA;
   return (v & ea::kStatusBadInputBit) ? ATTN_ERR_ARG : ATTN_OK;
 }
 

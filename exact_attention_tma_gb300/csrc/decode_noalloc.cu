@@ -54,18 +54,20 @@ attn_status scratch_for_current_device(void **out) {
 extern "C" attn_status attn_decode_noalloc(const void *q, const void *Kcache, const void *Vcache,
                                            void *O, int B, int H, int L, int d, float scale,
                                            cudaStream_t stream) {
-  const size_t need = attn_decode_workspace_bytes(B, H, L, d);
-  if (need > kNoallocScratchBytes) return ATTN_ERR_NOMEM;   // shape beyond the fixed scratch
+  // attn_decode's own checks first, then the size limit, then the one-time
+  // symbol lookup: an invalid call gets the same code as from attn_decode and
+  // makes no CUDA call.
+  const attn_status st0 =
+      static_cast<attn_status>(ea::check_decode_args(q, Kcache, Vcache, O, B, H, L, d, scale));
+  if (st0 != ATTN_OK) return st0;
+  if (attn_decode_workspace_bytes(B, H, L, d) > kNoallocScratchBytes)
+    return ATTN_ERR_NOMEM;   // shape beyond the fixed scratch
   void *scratch = nullptr;
-  if (need != 0) {
-    // An invalid shape (need == 0) skips the set-up; attn_decode_ws below then
-    // returns its shape / head-dimension error before it looks at the workspace.
-    const attn_status st = scratch_for_current_device(&scratch);
-    if (st != ATTN_OK) return st;
-  }
-  // Same validation and kernels as attn_decode_ws, with the fixed array as the workspace.
-  // The partials are fully written by the split kernel before the combine kernel reads
-  // them, so nothing in the array has to start at zero.
+  const attn_status st = scratch_for_current_device(&scratch);
+  if (st != ATTN_OK) return st;
+  // Same kernels as attn_decode_ws, with the fixed array as the workspace.
+  // The partials are fully written by the split kernel before the combine
+  // kernel reads them, so nothing in the array has to start at zero.
   return attn_decode_ws(q, Kcache, Vcache, O, B, H, L, d, scale, scratch, kNoallocScratchBytes,
                         stream);
 }

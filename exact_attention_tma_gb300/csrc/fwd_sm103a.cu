@@ -120,30 +120,46 @@ struct Cfg {
   static constexpr int SV = F8 ? 3 : (D == 128) ? EA_FWD_SV128 : EA_FWD_SV64;   // V ring stages
   static constexpr uint32_t Q_BYTES = BM * D * ESZ;   // one query tile
   static constexpr uint32_t KV_BYTES = BN * D * ESZ;  // one K or V tile
+  // Q buffers hold the query tiles of QD items (QD = 2 where shared memory
+  // allows: the next item's tiles then load while the current item runs).
+  static constexpr int QD = (D == 64 && !F8) ? 2 : 1;
+  static constexpr int NQB = QT * QD;
   static constexpr uint32_t OFF_Q = 0;
-  static constexpr uint32_t OFF_K = OFF_Q + QT * Q_BYTES;
+  static constexpr uint32_t OFF_K = OFF_Q + NQB * Q_BYTES;
   static constexpr uint32_t OFF_V = OFF_K + SK * KV_BYTES;
   // d = 64: the two key halves of a row keep separate maxima, sums and O
   // accumulators (merged once at the end); d = 128 (no room in TMEM for that):
   // the halves agree on every rescale and share one O accumulator.
   static constexpr bool kIndep = (D == 64);
   static constexpr int NPB = kIndep ? 2 : 1;        // P hand-off barriers per query tile
-  static constexpr uint32_t OFF_XCH = OFF_V + SV * KV_BYTES;   // float[2][QT][2][BM]
-  // The epilogue stages O (bf16) in the free Q_i buffer, or with 1-byte Q in
-  // a buffer of its own.
+  // Pair exchange between the two key-half warps of a row: with independent
+  // halves the maxima and the sums side by side, float[2][QT][2][BM]; with a
+  // shared accumulator one float[QT][2][BM] that carries the maxima during
+  // the K/V steps and the sums in the epilogue.
+  static constexpr uint32_t XCH_BYTES = (kIndep ? 2 : 1) * QT * 2 * BM * 4;
+  static constexpr uint32_t OFF_XCH = OFF_V + SV * KV_BYTES;
+  // The epilogue stages O (bf16) for its TMA store in buffers of its own, so
+  // a Q buffer is free as soon as the item's last Q K^T has read it.  At
+  // d = 128 bf16 (shared memory is full) both query tiles use one staging
+  // buffer in turn; otherwise each tile has its own.
   static constexpr uint32_t O_TILE = BM * D * 2;
-  static constexpr uint32_t OFF_OST = OFF_XCH + 2 * QT * 2 * BM * 4;
-  // O is staged in a buffer of its own where shared memory allows (then
-  // the Q buffers are released as soon as the last Q K^T has read them).
-  static constexpr bool kOwnStage = F8 || D == 64;
-  static constexpr uint32_t OFF_BAR = OFF_OST + (kOwnStage ? QT * O_TILE : 0);
-  // q[QT], qe[QT], kf[SK], ke[SK], vf[SV], ve[SV], s[QT], p[QT][NPB], o[QT], drain
-  static constexpr int NBAR = 2 * QT + 2 * SK + 2 * SV + QT + QT * NPB + QT + 1 + 2 * kRing;
+  static constexpr int NSTG = (D == 128 && !F8) ? 1 : QT;
+  static constexpr uint32_t OFF_OST = OFF_XCH + XCH_BYTES;
+  static_assert(OFF_OST % 1024 == 0, "128-byte-swizzled staging needs 1024-byte alignment");
+  static constexpr uint32_t OFF_BAR = OFF_OST + NSTG * O_TILE;
+  // q[NQB], qe[NQB], kf[SK], ke[SK], vf[SV], ve[SV], s[QT], p[QT][NPB], o[QT],
+  // drain, ostg, item ring full[kRing], empty[kRing]
+  static constexpr int NBAR = 2 * NQB + 2 * SK + 2 * SV + QT + QT * NPB + QT + 2 + 2 * kRing;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   // tmem slot, abort flag, pair_abort[8], item ring
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 48 + 4 * kRing;
-  static constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;   // 1024-byte alignment slack
-  static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+  static constexpr uint32_t kSmemMax = 232448;        // 227 KB per CTA
+  // Slack to align the dynamic shared memory to 1024 bytes where it fits;
+  // without it the kernel checks the alignment it was given (and reports a
+  // set-up error instead of running if it is not 1024-byte aligned).
+  static constexpr uint32_t SMEM_ALLOC =
+      SMEM_BYTES + 1024 <= kSmemMax ? SMEM_BYTES + 1024 : SMEM_BYTES;
+  static_assert(SMEM_ALLOC <= kSmemMax, "shared memory budget");
   static constexpr uint32_t TMEM_S = 0;               // S_i at column 128 * i
   // O accumulators at TMEM_O + D * b: b = i (shared by both halves) or
   // b = 2 i + h (one per key half h).
@@ -152,13 +168,14 @@ struct Cfg {
 };
 
 
-// exp2 of 32 consecutive scores of one row against the maximum m (-nm = m):
-// p = 2^(s * scale_log2 - m), packed as bf16 pairs into pk; adds the p to the
-// two fp32x2 partial sums rs2.
-__device__ __forceinline__ void exp_chunk(const uint32_t (&sr)[32], float2 sc2, float2 nm2,
+// exp2 of W consecutive scores of one row against the maximum m (-nm = m):
+// p = 2^(s * scale_log2 - m), packed as bf16 pairs into pk (W / 2 words);
+// adds the p to the two fp32x2 partial sums rs2.
+template <int W>
+__device__ __forceinline__ void exp_chunk(const uint32_t (&sr)[W], float2 sc2, float2 nm2,
                                           uint32_t *pk, float2 (&rs2)[2]) {
 #pragma unroll
-  for (int c = 0; c < 16; ++c) {
+  for (int c = 0; c < W / 2; ++c) {
     const float2 x = ffma2(make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])),
                            sc2, nm2);
     const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
@@ -170,14 +187,15 @@ __device__ __forceinline__ void exp_chunk(const uint32_t (&sr)[32], float2 sc2, 
 // FP8 variant: P is rounded to E4M3 as P * 2^2 (nm2 = 2 - m); the lazy
 // rescale keeps every P <= 64 (a 64-key half's sum <= 64), so P * 4 <= 256
 // stays below E4M3's 448 and P >= 2^-8 stays a normal number.  Packs four
-// scores per word (key order, low byte first); adds the P * 4 to rs2.
+// scores per word (key order, low byte first; W / 4 words); adds the P * 4 to rs2.
 constexpr float kPScale8 = 4.0f;
 constexpr float kLog2PScale8 = 2.0f;
 constexpr float kRescaleSum8 = 64.0f;
-__device__ __forceinline__ void exp_chunk_f8(const uint32_t (&sr)[32], float2 sc2, float2 nm2,
+template <int W>
+__device__ __forceinline__ void exp_chunk_f8(const uint32_t (&sr)[W], float2 sc2, float2 nm2,
                                              uint32_t *pk, float2 (&rs2)[2]) {
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
+  for (int c = 0; c < W / 4; ++c) {
     const float2 x0 = ffma2(make_float2(__uint_as_float(sr[4 * c]), __uint_as_float(sr[4 * c + 1])),
                             sc2, nm2);
     const float2 x1 = ffma2(
@@ -190,12 +208,13 @@ __device__ __forceinline__ void exp_chunk_f8(const uint32_t (&sr)[32], float2 sc
   }
 }
 
-// Scores of keys kv0 + col0 .. kv0 + col0 + 31 that lie past the last visible
-// key lim become -inf (so p = 0).
-__device__ __forceinline__ void mask_chunk(uint32_t (&sr)[32], int first_key, int lim) {
-  if (first_key + 31 > lim) {
+// Scores of keys first_key .. first_key + W - 1 that lie past the last
+// visible key lim become -inf (so p = 0).
+template <int W>
+__device__ __forceinline__ void mask_chunk(uint32_t (&sr)[W], int first_key, int lim) {
+  if (first_key + W - 1 > lim) {
 #pragma unroll
-    for (int c = 0; c < 32; ++c)
+    for (int c = 0; c < W; ++c)
       if (first_key + c > lim) sr[c] = __float_as_uint(-INFINITY);
   }
 }
@@ -209,7 +228,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = Cfg<D, F8>;
   constexpr int SK = C::SK;
   constexpr int SV = C::SV;
+  constexpr int QD = C::QD;
+  constexpr int NQB = C::NQB;
   extern __shared__ uint8_t smem_raw[];
+  if constexpr (C::SMEM_ALLOC == C::SMEM_BYTES) {
+    // No room for alignment slack: the 128-byte-swizzled buffers need the
+    // dynamic shared memory 1024-byte aligned as given (the same for every
+    // CTA, so the whole grid takes this exit together, before any barrier).
+    if ((smem_u32(smem_raw) & 1023u) != 0) {
+      if (threadIdx.x == 0) atomicOr(status, kStatusSetupBit);
+      return;
+    }
+  }
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sb = smem_u32(smem);
@@ -251,23 +281,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the CTA's whole sequence, S_i / P_i count tile i's K/V steps, and the Q_i
   // and O_i barriers complete once per item.
   const uint32_t bar0 = sb + C::OFF_BAR;
-  auto B_Q = [&](int i) { return bar0 + 8u * i; };                    // Q_i loaded
-  auto B_QE = [&](int i) { return bar0 + 8u * (QT + i); };            // Q_i buffer and O_i free
-  auto B_KF = [&](int s) { return bar0 + 8u * (2 * QT + s); };
-  auto B_KE = [&](int s) { return bar0 + 8u * (2 * QT + SK + s); };
-  auto B_VF = [&](int s) { return bar0 + 8u * (2 * QT + 2 * SK + s); };
-  auto B_VE = [&](int s) { return bar0 + 8u * (2 * QT + 2 * SK + SV + s); };
-  constexpr int kB5 = 2 * QT + 2 * SK + 2 * SV;
+  auto B_Q = [&](int b) { return bar0 + 8u * b; };                    // Q buffer b loaded
+  auto B_QE = [&](int b) { return bar0 + 8u * (NQB + b); };           // Q buffer b free
+  auto B_KF = [&](int s) { return bar0 + 8u * (2 * NQB + s); };
+  auto B_KE = [&](int s) { return bar0 + 8u * (2 * NQB + SK + s); };
+  auto B_VF = [&](int s) { return bar0 + 8u * (2 * NQB + 2 * SK + s); };
+  auto B_VE = [&](int s) { return bar0 + 8u * (2 * NQB + 2 * SK + SV + s); };
+  constexpr int kB5 = 2 * NQB + 2 * SK + 2 * SV;
   auto B_S = [&](int i) { return bar0 + 8u * (kB5 + i); };            // S_i ready (MMA)
   constexpr int NPB = C::NPB;
   // P_i written by the softmax (per key half when the halves are independent)
   auto B_P = [&](int i, int hh) { return bar0 + 8u * (kB5 + QT + i * NPB + (NPB > 1 ? hh : 0)); };
   auto B_O = [&](int i) { return bar0 + 8u * (kB5 + QT + QT * NPB + i); };   // item's last P_i V_j done
   const uint32_t B_DRAIN = bar0 + 8u * (kB5 + 2 * QT + QT * NPB);
-  constexpr int kB6 = kB5 + 2 * QT + QT * NPB + 1;
+  // The shared O staging buffer has been read by its latest TMA store (one
+  // completion per epilogue; used when both query tiles share the buffer).
+  const uint32_t B_OSTG = B_DRAIN + 8u;
+  constexpr int kB6 = kB5 + 2 * QT + QT * NPB + 2;
   auto B_IF = [&](int s) { return bar0 + 8u * (kB6 + s); };           // item slot s written
   auto B_IE = [&](int s) { return bar0 + 8u * (kB6 + kRing + s); };   // item slot s read by all
   static_assert(kB6 + 2 * kRing == C::NBAR, "barrier count");
+  // Query tile i of the CTA's t-th item uses Q buffer qbuf(t, i), for the
+  // quse(t)-th time (the parity of the buffer's barrier phases).
+  auto qbuf = [&](int t, int i) { return (t % QD) * QT + i; };
+  auto quse = [&](int t) { return t / QD; };
   volatile int *item_ring = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 48);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
@@ -306,20 +343,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(dst + kb * kBoxBytes, &tmV, kb * 64, j * BN, kvh, B_VF(sv));
     }
   };
-  auto load_q = [&](const Item &it, int i) {
-    mbar_arrive_expect_tx(B_Q(i), C::Q_BYTES);
+  auto load_q = [&](const Item &it, int i, int qb) {
+    mbar_arrive_expect_tx(B_Q(qb), C::Q_BYTES);
 #pragma unroll
     for (int kb = 0; kb < C::KB; ++kb)
-      tma_load_3d(sb + C::OFF_Q + i * C::Q_BYTES + kb * kBoxBytes, &tmQ, kb * C::BOX_COLS,
-                  it.q0 + i * BM, it.bh, B_Q(i));
+      tma_load_3d(sb + C::OFF_Q + qb * C::Q_BYTES + kb * kBoxBytes, &tmQ, kb * C::BOX_COLS,
+                  it.q0 + i * BM, it.bh, B_Q(qb));
   };
   // One thread of the TMA warp sets up the barriers and at once starts the
   // first item's loads, in the order the first MMAs need them (Q_0 and K_0,
   // then Q_1 and V_0), while the MMA warp allocates TMEM.
   if (threadIdx.x == kWarpTMA * 32) {
-    for (int i = 0; i < QT; ++i) {
-      mbar_init(B_Q(i), 1);
-      mbar_init(B_QE(i), 1);
+    for (int qb = 0; qb < NQB; ++qb) {
+      mbar_init(B_Q(qb), 1);
+      mbar_init(B_QE(qb), 1);
     }
     for (int s = 0; s < SK; ++s) {
       mbar_init(B_KF(s), 1);
@@ -335,6 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(B_O(i), 1);
     }
     mbar_init(B_DRAIN, 1);
+    mbar_init(B_OSTG, 1);
     for (int s = 0; s < kRing; ++s) {
       mbar_init(B_IF(s), 1);
       mbar_init(B_IE(s), 1 + 8 * QT);   // the MMA warp and every softmax warp
@@ -348,10 +386,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmO);
     Item it0;
     if (item_at(static_cast<int>(blockIdx.x), it0)) {   // (always true: the grid is no larger than the item count)
-      load_q(it0, 0);
+      load_q(it0, 0, 0);
       mbar_arrive_expect_tx(B_KF(0), C::KV_BYTES);
       load_k(it0.kvh, 0, 0);
-      for (int i = 1; i < QT; ++i) load_q(it0, i);
+      for (int i = 1; i < QT; ++i) load_q(it0, i, i);
       mbar_arrive_expect_tx(B_VF(0), C::KV_BYTES);
       // FP8: V^T comes from the transpose pass launched just before this
       // kernel, which may still be finishing (programmatic dependent launch).
@@ -386,9 +424,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t kEpiBar = 9 + i;          // named barrier of the group's 256 threads
     const int pa = 4 * i + q;
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
-    float *xch = reinterpret_cast<float *>(smem + C::OFF_XCH);   // [2][QT][2][BM]
+    float *xch = reinterpret_cast<float *>(smem + C::OFF_XCH);
     float *xi = xch + i * 2 * BM;            // maxima of the two halves
-    float *xl = xch + (QT + i) * 2 * BM;     // partial sums of the two halves
+    // Partial sums of the two halves: beside the maxima, or (shared
+    // accumulator) in the same slots once the item's K/V steps are done.
+    float *xl = kIndep ? xch + (QT + i) * 2 * BM : xi;
     const float2 sc2 = make_float2(scale_log2, scale_log2);
     const uint32_t s_addr = tmem + lane_addr + C::TMEM_S + i * BN + h * 64;
     // O accumulator columns this thread rescales.
@@ -400,22 +440,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float nm = (F8 ? kLog2PScale8 : 0.f) - m_use;
       const float2 nm2 = make_float2(nm, nm);
       float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      // (The two warps of a sub-partition that share this tile interleave
+      // their loads and exponentials; loading the next chunk while this one
+      // is exponentiated measured slower.)
       {
         uint32_t a[32];
         tmem_ld_32cols(s_addr, a);
         tmem_ld_wait_regs(a);
-        mask_chunk(a, k0, lm);
-        if constexpr (F8) exp_chunk_f8(a, sc2, nm2, &pk[0], rs2);
-        else exp_chunk(a, sc2, nm2, &pk[0], rs2);
+        mask_chunk<32>(a, k0, lm);
+        if constexpr (F8) exp_chunk_f8<32>(a, sc2, nm2, &pk[0], rs2);
+        else exp_chunk<32>(a, sc2, nm2, &pk[0], rs2);
       }
       __syncwarp();
       {
         uint32_t b[32];
         tmem_ld_32cols(s_addr + 32, b);
         tmem_ld_wait_regs(b);
-        mask_chunk(b, k0 + 32, lm);
-        if constexpr (F8) exp_chunk_f8(b, sc2, nm2, &pk[8], rs2);
-        else exp_chunk(b, sc2, nm2, &pk[16], rs2);
+        mask_chunk<32>(b, k0 + 32, lm);
+        if constexpr (F8) exp_chunk_f8<32>(b, sc2, nm2, &pk[8], rs2);
+        else exp_chunk<32>(b, sc2, nm2, &pk[16], rs2);
       }
       rs = (rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y);
       if constexpr (F8) rs *= 1.0f / kPScale8;
@@ -428,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t a[32];
         tmem_ld_32cols(s_addr + 32 * u, a);
         tmem_ld_wait_regs(a);
-        mask_chunk(a, k0 + 32 * u, lm);
+        mask_chunk<32>(a, k0 + 32 * u, lm);
 #pragma unroll
         for (int c = 0; c + 1 < 32; c += 2)
           mx = fmax3(mx, __uint_as_float(a[c]), __uint_as_float(a[c + 1]));
@@ -536,23 +579,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(B_P(i, h));
       }
       // Epilogue of tile i: each warp stages its half of the columns of O_i
-      // as bf16 in the (no longer needed) Q_i buffer (with FP8, whose Q_i is
-      // half the size, in a staging buffer of its own), in the
-      // 128-byte-swizzled box layout of the O tensor map, and one thread
-      // stores the tile with TMA (rows past N are dropped by the tensor map);
-      // the warp of the low half writes the LSE.  Independent halves are
-      // merged with weights 2^(m_h - max(m_0, m_1)).  Every MMA reading Q_i
-      // finished before the item's last P_i V_j, whose completion the
-      // epilogue waits for.  Once the store has read the staging buffer, the
-      // storing thread releases Q_i (and O_i) to the next item.
+      // as bf16 in the staging buffer, in the 128-byte-swizzled box layout of
+      // the O tensor map, and one thread stores the tile with TMA (rows past
+      // N are dropped by the tensor map); the warp of the low half writes the
+      // LSE.  Independent halves are merged with weights
+      // 2^(m_h - max(m_0, m_1)).  The next item's P_i V_0 overwrites O_i only
+      // after this group has written P_i, i.e. after these TMEM reads.
       const bool okw = ok && __all_sync(0xffffffffu, mbar_wait(B_O(i), t & 1, status, abort_flag));
-      if (kIndep) xi[h * BM + r] = m_i;
-      xl[h * BM + r] = l_i;
-      // (FP8: the previous item's store must have read the staging buffer.)
-      if (C::kOwnStage && threadIdx.x == i * 256) bulk_wait_group_read0();
-      if (named_bar_any(kEpiBar, 2 * BM, !okw)) {
+      if (kIndep) {
+        xi[h * BM + r] = m_i;
+        xl[h * BM + r] = l_i;
+      }
+      // The staging buffer must have been read by its previous store: this
+      // tile's own previous one (a buffer per tile), or the latest one of
+      // either tile (one shared buffer, used by the epilogues in turn: tile
+      // 0 of item t, tile 1 of item t, tile 0 of item t + 1, ...).
+      bool sok = okw;
+      if (threadIdx.x == i * 256) {
+        if constexpr (C::NSTG == 1) {
+          const int e = 2 * t + i;
+          if (e > 0) sok = sok && mbar_wait(B_OSTG, (e - 1) & 1, status, abort_flag);
+        } else {
+          bulk_wait_group_read0();
+        }
+      }
+      if (named_bar_any(kEpiBar, 2 * BM, !sok)) {
         ok = false;
         break;
+      }
+      if constexpr (!kIndep) {
+        // (The partner warp read its last maximum from these slots before
+        // the barrier above.)
+        xl[h * BM + r] = l_i;
+        named_bar_sync(kEpiBar, 2 * BM);
       }
       tc_fence_after();
       float mrow = m_i, w0 = 1.f, w1 = 1.f;
@@ -565,8 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv_l = out_mul / lt;
       const float a0 = w0 * inv_l, a1 = w1 * inv_l;
       const int qrow = it.q0 + i * BM + r;
-      const uint32_t stage_base =
-          C::kOwnStage ? sb + C::OFF_OST + i * C::O_TILE : sb + C::OFF_Q + i * C::Q_BYTES;
+      const uint32_t stage_base = sb + C::OFF_OST + (C::NSTG == 1 ? 0 : i) * C::O_TILE;
       const uint32_t stage = stage_base + static_cast<uint32_t>(r) * 128;
       const uint32_t o_addr = tmem + lane_addr + C::TMEM_O + (kIndep ? 2 * i * D : i * D) + h * (D / 2);
 #pragma unroll
@@ -623,9 +681,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < D / 64; ++kb)
           tma_store_3d(&tmO, kb * 64, it.q0 + i * BM, it.bh, stage_base + kb * kBoxBytes);
         bulk_commit_group();
-        if constexpr (!C::kOwnStage) {
+        if constexpr (C::NSTG == 1) {
+          // Hand the shared buffer to the next epilogue once the store has read it.
           bulk_wait_group_read0();
-          mbar_arrive(B_QE(i));
+          mbar_arrive(B_OSTG);
         }
       }
       if (h == 0 && qrow < N) {
@@ -649,13 +708,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ------------------------------------------------------ TMA producer
       if constexpr (F8) asm volatile("griddepcontrol.wait;" ::: "memory");
       // (The first item's Q tiles and first K/V tile were issued before the
-      // CTA-wide barrier.)  Q_i of a later item waits until the previous
-      // item's epilogue of tile i has released the buffer.
+      // CTA-wide barrier.)  A Q buffer is refilled once the MMA warp has
+      // released it after its previous item's last Q K^T.
       const bool leader = elect_one();
       int gk = 0, gv = 0;                    // K / V tiles issued so far
-      int q_items[QT];                       // per Q buffer: items whose Q tile was issued
-#pragma unroll
-      for (int i = 0; i < QT; ++i) q_items[i] = 1;
+      int gq = QT;                           // Q tiles issued so far (item-major)
       bool ok = true;
       auto load_k_next = [&](int kvh, int j) {
         const int sk = gk % SK;
@@ -677,6 +734,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++gv;
         return true;
       };
+      // Query tile i of the t-th item (t >= 1).
+      auto load_q_next = [&](const Item &it, int t, int i) {
+        const int qb = qbuf(t, i);
+        if (t >= QD && !wait_all(B_QE(qb), (quse(t) - 1) & 1)) return false;
+        if (leader) load_q(it, i, qb);
+        ++gq;
+        return true;
+      };
       int k = static_cast<int>(blockIdx.x);
       for (int t = 0; ok; ++t) {
         // Publish item k (or the end of the sequence) to the other warps.
@@ -691,15 +756,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!item_at(k, it)) break;
         if (t == 0) {
           gk = gv = 1;
+        } else if constexpr (QD > 1) {
+          // The Q buffers of this item were released an item ago: Q first.
+          ok = load_q_next(it, t, 0) && load_q_next(it, t, 1) && load_k_next(it.kvh, 0) &&
+               load_v_next(it.kvh, 0);
         } else {
-          // K_0 and V_0 go first: their stages are free well before the
-          // previous item's epilogues release the Q buffers.
-          ok = load_k_next(it.kvh, 0) && load_v_next(it.kvh, 0);
-          for (int i = 0; ok && i < QT; ++i) {
-            if (!(ok = wait_all(B_QE(i), (t - 1) & 1))) break;
-            if (leader) load_q(it, i);
-            q_items[i] = t + 1;
-          }
+          // In the order the buffers come free near the end of the previous
+          // item (Q_0 of the next item is wanted early, see the MMA warp).
+          ok = load_k_next(it.kvh, 0) && load_q_next(it, t, 0) && load_v_next(it.kvh, 0) &&
+               load_q_next(it, t, 1);
         }
         for (int j = 1; ok && j < it.n1; ++j) ok = load_k_next(it.kvh, j) && load_v_next(it.kvh, j);
         // This item's loads are all issued: claim the next one.
@@ -709,7 +774,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (leader && *abort_flag) {
         // Let every copy this warp started land before the CTA exits.
-        for (int i = 0; i < QT; ++i) mbar_wait_drain(B_Q(i), (q_items[i] - 1) & 1, 100000000ull);
+        for (int x = gq - 1; x >= 0 && x >= gq - NQB; --x)   // the last load of each buffer
+          mbar_wait_drain(B_Q(qbuf(x / QT, x % QT)), quse(x / QT) & 1, 100000000ull);
         for (int s = 0; s < SK && s < gk; ++s)
           mbar_wait_drain(B_KF(s), ((gk - 1 - s) / SK) & 1, 100000000ull);
         for (int s = 0; s < SV && s < gv; ++s)
@@ -734,9 +800,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q_lo = static_cast<uint32_t>(dQ);
       const uint32_t k_lo = static_cast<uint32_t>(dK);
       const uint32_t v_lo = static_cast<uint32_t>(dV);
-      // S_i = Q_i K^T: both operands K-major (head dim contiguous), 128-B swizzle.
-      auto issue_qk = [&](int i, int sk) {
-        const uint32_t a0 = q_lo + ((i * C::Q_BYTES) >> 4);
+      // S_i = Q K^T from Q buffer qb and K stage sk: both operands K-major
+      // (head dim contiguous), 128-B swizzle.
+      auto issue_qk = [&](int i, int qb, int sk) {
+        const uint32_t a0 = q_lo + ((qb * C::Q_BYTES) >> 4);
         const uint32_t b0 = k_lo + ((sk * C::KV_BYTES) >> 4);
 #pragma unroll
         for (int kk = 0; kk < C::KSTEPS; ++kk) {   // 32-byte k-steps, 4 per 128-byte box
@@ -788,74 +855,82 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return true;
       };
+      // S_i of the first K/V tile of the t-th item (its K_0 at ring position
+      // kg); the caller has seen its operands arrive.  Tile 1 is K_0's last
+      // reader; a tile with a single K/V tile releases its Q buffer at once.
+      auto first_qk = [&](int i, int t, int kg, const Item &x) {
+        issue_qk(i, qbuf(t, i), kg % SK);
+        mma_commit(B_S(i));
+        if (i == QT - 1) mma_commit(B_KE(kg % SK));
+        if ((i == 0 ? x.n0 : x.n1) == 1) mma_commit(B_QE(qbuf(t, i)));
+      };
       bool ok = true;
-      int gk = 0, gv = 0;                    // K / V tiles consumed so far
+      int gk = 0, gv = 0;                    // ring positions of the current item's K_0 / V_0
       int base0 = 0, base1 = 0;              // steps of tiles 0 / 1 in earlier items
       for (int t = 0; ok; ++t) {
         Item it;
         if (!take_item(t, it, ok)) break;
         const int n0 = it.n0, n1 = it.n1;
-        // S_0 = Q_0 K_0^T, S_1 = Q_1 K_0^T.  Q_i of this item arrives only
-        // after the previous item's epilogue of tile i has read O_i, so the
-        // first P_i V_0 below may overwrite O_i.
-        {
-          const int sk = gk % SK;
-          ok = wait_all(B_Q(0), t & 1) && wait_all(B_KF(sk), (gk / SK) & 1);
-          if (ok) {
-            tc_fence_after();
-            if (leader) {
-              issue_qk(0, sk);
-              mma_commit(B_S(0));
-              if (C::kOwnStage && n0 == 1) mma_commit(B_QE(0));
-            }
-            __syncwarp();
-          }
-          ok = ok && wait_all(B_Q(1), t & 1);
-          if (ok) {
-            tc_fence_after();
-            if (leader) {
-              issue_qk(1, sk);
-              mma_commit(B_S(1));
-              mma_commit(B_KE(sk));
-              if (C::kOwnStage && n1 == 1) mma_commit(B_QE(1));
-            }
-            __syncwarp();
-          }
-        }
-        // Per K/V tile j: the V_j and K_{j+1} stages are checked first (they are
-        // normally resident long before), so that each softmax hand-off is
-        // followed by one wait and an uninterrupted run of MMAs:
-        // P_0 V_j, Q_0 K_{j+1}^T, then P_1 V_j, Q_1 K_{j+1}^T.
-        for (int j = 0; ok && j < n1; ++j) {
+        // S_0 = Q_0 K_0^T, then S_1 = Q_1 K_0^T.  The first P_i V_0 below
+        // overwrites O_i only after tile i's softmax warps have written P_i,
+        // which they do after reading O_i in the previous item's epilogue.
+        ok = wait_all(B_Q(qbuf(t, 0)), quse(t) & 1) && wait_all(B_KF(gk % SK), (gk / SK) & 1);
+        if (!ok) break;
+        tc_fence_after();
+        if (leader) first_qk(0, t, gk, it);
+        __syncwarp();
+        if (!(ok = wait_all(B_Q(qbuf(t, 1)), quse(t) & 1))) break;
+        tc_fence_after();
+        if (leader) first_qk(1, t, gk, it);
+        __syncwarp();
+        // Per K/V tile j but the last: the V_j and K_{j+1} stages are checked
+        // first (they are normally resident long before), so that each
+        // softmax hand-off is followed by one wait and an uninterrupted run of
+        // MMAs: P_0 V_j, Q_0 K_{j+1}^T, then P_1 V_j, Q_1 K_{j+1}^T.
+        for (int j = 0; ok && j + 1 < n1; ++j) {
           const int vp = gv + j, sv = vp % SV;
-          const bool more = j + 1 < n1;
           const int kp = gk + j + 1, sk1 = kp % SK;
-          if (!(ok = wait_all(B_VF(sv), (vp / SV) & 1))) break;
-          if (more && !(ok = wait_all(B_KF(sk1), (kp / SK) & 1))) break;
+          if (!(ok = wait_all(B_VF(sv), (vp / SV) & 1) && wait_all(B_KF(sk1), (kp / SK) & 1))) break;
           if (j < n0) {
             if (!(ok = pv(0, sv, j, (base0 + j) & 1))) break;
             if (leader) {
               if (j + 1 == n0) mma_commit(B_O(0));
               if (j + 1 < n0) {
-                issue_qk(0, sk1);   // overwrites S_0/P_0 after the P_0 V_j MMAs above read it
+                issue_qk(0, qbuf(t, 0), sk1);   // overwrites S_0/P_0 after the P_0 V_j MMAs above read it
                 mma_commit(B_S(0));
-                if (C::kOwnStage && j + 2 == n0) mma_commit(B_QE(0));
+                if (j + 2 == n0) mma_commit(B_QE(qbuf(t, 0)));
               }
             }
             __syncwarp();
           }
           if (!(ok = pv(1, sv, j, (base1 + j) & 1))) break;
           if (leader) {
-            if (j + 1 == n1) mma_commit(B_O(1));
             mma_commit(B_VE(sv));
-            if (more) {
-              issue_qk(1, sk1);
-              mma_commit(B_S(1));
-              mma_commit(B_KE(sk1));
-              if (C::kOwnStage && j + 2 == n1) mma_commit(B_QE(1));
-            }
+            issue_qk(1, qbuf(t, 1), sk1);
+            mma_commit(B_S(1));
+            mma_commit(B_KE(sk1));
+            if (j + 2 == n1) mma_commit(B_QE(qbuf(t, 1)));
           }
           __syncwarp();
+        }
+        // The last K/V tile, kept out of the loop above so that the loop body
+        // stays the short steady-state schedule (measured: a loop that also
+        // handles the item's end ran every K/V step slower).
+        if (ok) {
+          const int j = n1 - 1;
+          const int vp = gv + j, sv = vp % SV;
+          ok = wait_all(B_VF(sv), (vp / SV) & 1);
+          if (ok && j < n0 && (ok = pv(0, sv, j, (base0 + j) & 1))) {
+            if (leader) mma_commit(B_O(0));
+            __syncwarp();
+          }
+          if (ok && (ok = pv(1, sv, j, (base1 + j) & 1))) {
+            if (leader) {
+              mma_commit(B_O(1));
+              mma_commit(B_VE(sv));
+            }
+            __syncwarp();
+          }
         }
         gk += n1;
         gv += n1;

@@ -37,6 +37,7 @@ inline int sm_count() {
 // Bits of the device status word (see attn_get_device_status).
 constexpr unsigned kStatusTimeoutBit = 1u;
 constexpr unsigned kStatusBadInputBit = 2u;   // a kernel met an invalid index (a page id)
+constexpr unsigned kStatusSetupBit = 4u;      // a kernel could not set up (shared-memory alignment)
 
 // Forward: one launch of the fused tcgen05/TMA kernel; H query heads over
 // H_kv K/V heads per batch (H % H_kv == 0; H_kv == H is multi-head).  Arguments
@@ -77,6 +78,12 @@ cudaError_t sched_slot(unsigned **out);
 
 // Device address of the current device's status word (looked up once per device).
 cudaError_t device_status_word(unsigned **out);
+
+// attn_decode's host-side argument checks (null, shape, head dimension, scale,
+// 16-byte alignment), in that order; returns an attn_status code, 0 if valid.
+// Makes no CUDA call.
+int check_decode_args(const void *q, const void *K, const void *V, const void *O, int B, int H,
+                      int L, int d, float scale);
 
 // Decode: split kernel + combine kernel on `stream`, partials in `ws`.
 constexpr int kDecodeSplits = 32;

@@ -68,9 +68,13 @@ typedef enum {
  *   scale   : multiplies Q K^T before masking and softmax (finite, > 0).
  *   causal  : 0 = every key visible; 1 = key j visible to query i iff j <= i.
  *
- * One tcgen05/TMA kernel launch (one CTA per 256 query rows of one head); no
- * workspace; S and P stay on chip.
- * O and LSE are written exactly once per element.  O must not alias Q, K or V.
+ * One tcgen05/TMA kernel launch on a persistent grid of min(#SMs, work
+ * items) CTAs, one per SM.  A work item is 256 query rows (two 128-row tiles)
+ * of one head; each CTA starts with one item and claims the next from a
+ * per-launch counter in a library-owned device array once it has issued the
+ * current item's loads (causal: longest items first).  No workspace; S and P
+ * stay on chip.  O and LSE are written exactly once per element.  O must not
+ * alias Q, K or V.
  */
 attn_status attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
                      int B, int H, int N, int d, float scale, int causal,
@@ -85,10 +89,14 @@ attn_status attn_fwd(const void *Q, const void *K, const void *V, void *O, float
  *   L       : cache length, 1 <= L <= 2^24.  The new token follows the cache,
  *             so all L keys are visible (no mask).
  *
- * Split-KV: each head's keys are cut into 32 chunks of ceil(L/32) keys; one
- * launch computes every chunk's normalised partial output and log-sum-exp
- * into a workspace, a second launch combines them with weights
- * exp(lse_s - max_s lse_s).  The workspace is owned by the library: it is
+ * Split-KV: each head's keys are cut into s chunks of ceil(L/s) keys, s a
+ * power of two chosen from the shape: the one nearest (in ratio) to 108 split
+ * CTAs per SM over the call, i.e. 108 * SMs / (B*H) per head, raised to at
+ * least 4 and capped at 32, then halved while a chunk would hold fewer than 64
+ * keys (B=16, H=32, L=8192 on 152 SMs: s = 32; B=64, H=32, L=2048: s = 8).
+ * One launch computes every chunk's normalised partial output and log-sum-exp
+ * into a workspace (sized for 32 chunks whatever s is), a second launch
+ * combines them with weights exp(lse_s - max_s lse_s).  The workspace is owned by the library: it is
  * allocated on first use per device, grows when a larger call needs it and
  * lives until process exit.  Growing it synchronises the device, so warm it up
  * with the largest shape before capturing a CUDA graph.  Calls that share a
@@ -193,8 +201,8 @@ attn_status attn_decode_paged(const void *q, const void *K_pages, const void *V_
  *   scale      : multiplies the dequantised Q K^T, as in attn_fwd.
  *
  * Two launches on `stream`: a pass that writes V^T (d x N bytes per head)
- * into the workspace, and the forward kernel (one CTA per head and 128-row
- * query tile).  attn_fwd_fp8 uses a library-owned grow-only workspace (its
+ * into the workspace, and the persistent forward kernel of attn_fwd (items of
+ * 256 query rows of one head, one CTA per SM).  attn_fwd_fp8 uses a library-owned grow-only workspace (its
  * own, same caveats as attn_decode); attn_fwd_fp8_ws takes a caller-owned one
  * of at least attn_fwd_fp8_workspace_bytes(B, H, N, d) bytes (ATTN_ERR_NOMEM
  * if smaller; 0 bytes is returned for an invalid shape).
@@ -226,7 +234,9 @@ size_t attn_fwd_fp8_workspace_bytes(int B, int H, int N, int d);
  * dQ, dK and dV are overwritten (never accumulated into) and must not overlap
  * any input.  Three launches on `stream`: a row pass (rowsum(dO * O) and LSE
  * in base 2 into the workspace), a dK/dV kernel (one CTA per K/V head and
- * 128-key tile) and a dQ kernel (one CTA per query head and 128-query tile).
+ * 128-key tile; a persistent grid of one CTA per SM that claims those items
+ * from a per-launch counter) and a dQ kernel (one CTA per query head and
+ * 128-query tile).
  * No atomics: results are identical from run to run.  The workspace
  * (attn_bwd_workspace_bytes) is library-owned and grow-only as for
  * attn_decode, with the same synchronisation and stream caveats; it is not
@@ -283,7 +293,10 @@ size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
  *          call's contents (no part of it needs to start at zero).  Calls that
  *          overlap on the GPU -- on different streams, or from different host
  *          threads -- race on it and must be serialised by the caller.
- * Other arguments, validation and errors are those of attn_decode.
+ * Other arguments, validation and errors are those of attn_decode, checked in
+ * this order: attn_decode's argument checks (ATTN_ERR_NULL, _SHAPE, _HEADDIM,
+ * _ARG, _ALIGN, with no CUDA call), then the size limit (ATTN_ERR_NOMEM), then
+ * the one-time set-up (ATTN_ERR_CUDA if the address lookup fails).
  */
 attn_status attn_decode_noalloc(const void *q, const void *Kcache, const void *Vcache, void *O,
                                 int B, int H, int L, int d, float scale, cudaStream_t stream);
@@ -292,7 +305,10 @@ attn_status attn_decode_noalloc(const void *q, const void *Kcache, const void *V
  * attn_get_device_status — synchronises `stream`, then reads and clears the
  * library's device status word on the current device.  Returns ATTN_OK, or
  * ATTN_ERR_TIMEOUT if any kernel since the last call gave up on a bounded
- * wait, or ATTN_ERR_CUDA if synchronisation itself failed.
+ * wait, ATTN_ERR_CUDA if synchronisation itself failed or a kernel could not
+ * set up (the forward checks that its dynamic shared memory is 1024-byte
+ * aligned and otherwise returns without computing), or ATTN_ERR_ARG if a
+ * kernel met an invalid index (a page id).
  */
 attn_status attn_get_device_status(cudaStream_t stream);
 

@@ -101,6 +101,26 @@ def test_fwd_rejects_bad_arguments_before_launch(lib, kw, code):
 ])
 def test_decode_rejects_bad_arguments_before_launch(lib, kw, code):
     assert _dec(lib, **kw) == code
+    # The allocation-free decode runs the same checks first (before its size
+    # limit and its symbol lookup, so no CUDA call is made on this GPU-less host).
+    assert _dec_noalloc(lib, **kw) == code
+
+
+def _dec_noalloc(lib, q=P, K=P, V=P, O=P, B=1, H=1, L=128, d=64, scale=0.125):
+    vp = ctypes.c_void_p
+    return lib.attn_decode_noalloc(vp(q), vp(K), vp(V), vp(O), B, H, L, d, scale, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    # Too large for the 16 MiB scratch, with another error that must win.
+    (dict(B=64, H=32, d=128, q=0), NULL), (dict(B=64, H=32, d=128, scale=float("nan")), ARG),
+    (dict(B=64, H=32, d=128, O=P + 2), ALIGN), (dict(B=64, H=32, d=96), HEADDIM),
+    # Valid but too large: refused before any CUDA call.
+    (dict(B=64, H=32, d=128), NOMEM), (dict(B=1, H=1017, d=128), NOMEM),
+    (dict(B=1, H=2017, d=64), NOMEM), (dict(B=7, H=289, d=64), NOMEM),
+])
+def test_decode_noalloc_checks_arguments_before_its_size_limit(lib, kw, code):
+    assert _dec_noalloc(lib, **kw) == code
 
 
 def test_decode_ws_checks_workspace(lib):

@@ -19,7 +19,8 @@ import torch
 
 import exact_attention_tma_gb300 as ea
 from exact_attention_tma_gb300.inputs import decode_inputs
-from parity import O_MAX, O_MEAN
+import oracle
+from parity import O_MAX, O_MEAN, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -48,6 +49,14 @@ def _close(a, b):
     assert err.max().item() <= O_MAX and err.mean().item() <= O_MEAN, (err.max(), err.mean())
 
 
+def _matches_oracle(out, q, K, V, scale):
+    """Element by element against the fp64 oracle (independent of both decode paths)."""
+    O_ref, _ = oracle.decode(to_f64(q), to_f64(K), to_f64(V), scale)
+    err = np.abs(to_f64(out) - O_ref)
+    assert np.isfinite(to_f64(out)).all()
+    assert err.max() <= O_MAX and err.mean() <= O_MEAN, (err.max(), err.mean())
+
+
 @pytest.mark.parametrize("shape", [(4, 8, 1500, 128), (2, 5, 333, 64)])
 def test_noalloc_matches_allocating_decode_on_two_calls(lib, shape):
     B, H, L, d = shape
@@ -59,6 +68,7 @@ def test_noalloc_matches_allocating_decode_on_two_calls(lib, shape):
         assert _call_noalloc(lib, q, K, V, out, scale) == 0, f"call {call}"
         torch.cuda.synchronize()
         _close(out, ref)
+        _matches_oracle(out, q, K, V, scale)
     assert ea.attn_get_device_status() == 0
 
 
@@ -77,3 +87,20 @@ def test_noalloc_refuses_shapes_beyond_its_scratch(lib):
     torch.cuda.synchronize()
     _close(out, ea.decode(q, K, V, scale=128 ** -0.5))
     assert np.isfinite(out.float().cpu().numpy()).all()
+
+
+def test_noalloc_head_limit_at_d64(lib):
+    # At d = 64 the 16 MiB scratch holds 2016 heads (2016 * 32 * 65 * 4 B); 2017 are refused.
+    assert ea.attn_decode_workspace_bytes(1, 2016, 64, 64) <= 16 << 20
+    assert ea.attn_decode_workspace_bytes(1, 2017, 64, 64) > 16 << 20
+    q, K, V = decode_inputs(1, 2016, 64, 64, seed=5, device="cuda")
+    out = torch.full_like(q, float("nan"))
+    assert _call_noalloc(lib, q, K, V, out, 0.125) == 0
+    torch.cuda.synchronize()
+    _matches_oracle(out, q, K, V, 0.125)
+    q1, K1, V1 = decode_inputs(1, 2017, 64, 64, seed=5, device="cuda")
+    untouched = torch.full_like(q1, 7.0)
+    assert _call_noalloc(lib, q1, K1, V1, untouched, 0.125) == NOMEM
+    torch.cuda.synchronize()
+    assert (untouched == 7.0).all()   # nothing was launched
+    assert ea.attn_get_device_status() == 0
