@@ -89,6 +89,11 @@ constexpr float kRescaleSum = 32768.0f;
 // Running maximum of a key half that has seen no visible key yet: any visible
 // score then overflows the half's P sum to +inf, which takes the rescale path.
 constexpr float kMInit = -1.0e30f;
+// First tile started from m = 0 (bf16, d = 128): a half row whose P sum is
+// below 2^-50 has every score below about -44 (base 2); the tile is then
+// redone against its true maximum, so that no P falls near fp32's normal
+// range.
+constexpr float kTinySum = 8.8817841970012523e-16f;   // 2^-50
 
 // K/V ring depths per head dimension (shared memory: 2 query tiles + SK + SV
 // tiles of 128 x d bf16 must fit in 227 KB).
@@ -500,7 +505,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (okw) tc_fence_after();
         const int k0 = j * BN + h * 64;
-        if (j == 0) {
+        // bf16 at d = 128 starts the item's first tile from m = 0 instead of
+        // a separate maximum pass (redone below against the true maximum if a
+        // half's P sum is then too large or too small).
+        if (j == 0 && (kIndep || F8)) {
           // First tile: the maximum first (of the half, or of the whole row,
           // which always contains key 0).
           if (kIndep) {
@@ -524,7 +532,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kIndep) {
           redo = __any_sync(0xffffffffu, !(rs <= kRedo));
         } else {
-          redo = named_bar_any(pair_bar, 64, !okw || !(rs <= kRedo));
+          redo = named_bar_any(pair_bar, 64,
+                               !okw || !(rs <= kRedo) || (!F8 && j == 0 && !(rs >= kTinySum)));
           if (redo && pair_abort[pa]) {
             ok = false;
             break;
@@ -540,8 +549,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_bar_sync(pair_bar, 64);
             tmax = fmaxf(xi[r], xi[BM + r]);
           }
-          const float m_new = fmaxf(m_i, tmax * scale_log2);
-          alpha = ex2_approx(m_i - m_new);
+          float m_new;
+          if constexpr (kIndep || F8) {
+            m_new = fmaxf(m_i, tmax * scale_log2);
+            alpha = ex2_approx(m_i - m_new);
+          } else {
+            // (On the first tile nothing has accumulated yet: the factor is
+            // 1, and m is the tile's maximum whatever it started from.)
+            m_new = fmaxf(j == 0 ? -INFINITY : m_i, tmax * scale_log2);
+            alpha = j == 0 ? 1.f : ex2_approx(m_i - m_new);
+          }
           m_i = m_new;
           pass(k0, lim, m_i, pk, rs);
           if (j > 0) {

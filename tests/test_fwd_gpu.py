@@ -88,6 +88,26 @@ def test_growing_scores_force_rescales(d, causal):
     assert_within(compare_fwd(o, lse, O_ref, L_ref, range(B * H), None))
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_far_negative_scores(d, causal):
+    # Every score lies far below zero (about -170 in natural-log units, with
+    # unit spread): softmax is shift-invariant, so O and LSE - (common shift)
+    # behave as for centred scores, but a kernel that starts its running
+    # maximum at 0 sees every P underflow and must fall back to the true maximum.
+    B, H, N = 1, 2, 700
+    q, k, v = fwd_inputs(B, H, N, d, 91, v_dist="uniform", device="cpu")
+    base = torch.full((d,), 4.0 * (128.0 / d) ** 0.5)
+    q = (q.float() * 0.5 + base).to(torch.bfloat16).cuda()
+    k = (k.float() * 0.5 - base).to(torch.bfloat16).cuda()
+    v = v.cuda()
+    scale = d ** -0.5
+    o, lse = _run(q, k, v, causal, scale)
+    O_ref, L_ref = oracle_fwd(q, k, v, scale, causal)
+    assert L_ref.max() < -100
+    assert_within(compare_fwd(o, lse, O_ref, L_ref, range(B * H), None))
+
+
 def _sampled(name, heads, rows, full_heads=()):
     w = WORKLOADS[name]
     q, k, v = workload_inputs(w, device="cuda")
@@ -123,8 +143,9 @@ def test_long_causal_workload_sampled():
     _sampled("long_causal_fwd", heads=[0, 7, 19, 31], rows=_rows(w.N, 40, 3))
 
 
-def test_deterministic_and_no_out_of_bounds_writes():
-    B, H, N, d = 2, 2, 333, 128
+@pytest.mark.parametrize("d", [64, 128])
+def test_deterministic_and_no_out_of_bounds_writes(d):
+    B, H, N = 2, 2, 333
     q, k, v = fwd_inputs(B, H, N, d, 21, device="cuda")
     pad = 4096
     o_buf = torch.full((B * H * N * d + pad,), 7.0, dtype=torch.bfloat16, device="cuda")
@@ -155,12 +176,13 @@ def test_runs_on_a_side_stream():
     assert_within(compare_fwd(o, lse, O_ref, L_ref, range(B * H), None))
 
 
-def test_concurrent_launches_on_several_streams():
+@pytest.mark.parametrize("d", [64, 128])
+def test_concurrent_launches_on_several_streams(d):
     """The persistent forward hands out work items from a counter that each
     launch takes for itself: launches running at the same time on different
     streams (and more launches than there are counters) each compute their own
     result, equal to the same call made alone."""
-    B, H, N, d = 2, 8, 1024, 128
+    B, H, N = 2, 8, 1024
     streams = [torch.cuda.Stream() for _ in range(4)]
     ins = [fwd_inputs(B, H, N, d, 40 + n, device="cuda") for n in range(4)]
     refs = []
@@ -180,6 +202,24 @@ def test_concurrent_launches_on_several_streams():
     for (o, lse), (o_ref, l_ref) in zip(outs, refs):
         assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
     assert ea.attn_get_device_status() == 0
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_partial_items_among_full_items(d, causal):
+    """N = 640 leaves each head one work item whose last query tile lies past
+    N (at d = 64 an item is three 128-row tiles, at d = 128 two) next to full
+    items, and 256 heads give every persistent CTA several of both kinds in
+    turn, so the per-buffer barrier phases must stay in step across items
+    that skip a tile."""
+    B, H, N = 4, 64, 640
+    q, k, v = fwd_inputs(B, H, N, d, 71 + d + causal, device="cuda")
+    scale = d ** -0.5
+    o, lse = _run(q, k, v, causal, scale)
+    assert ea.attn_get_device_status() == 0
+    heads = [0, 1, 2, 75, 151, 152, 153, 200, 254, 255]
+    O_ref, L_ref = oracle_fwd(q, k, v, scale, causal, heads=heads)
+    assert_within(compare_fwd(o, lse, O_ref, L_ref, heads, None))
 
 
 @pytest.mark.parametrize("d", [64, 128])
