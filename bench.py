@@ -399,6 +399,7 @@ def run_ours(args, rank, world, local_rank):
     fwd_tflops = ff / fwd_avg / 1e12
     dec_gbs = db / dec_avg / 1e9
     traffic = recorded_traffic("decode_sm103a.cu")
+    traffic_fwd = recorded_traffic("fwd_sm103a.cu")
     record = {
         "metric": METRIC,
         "value": pct_of_roofline(roof_s, ms_step / 1e3),
@@ -439,6 +440,11 @@ def run_ours(args, rank, world, local_rank):
             "frac": fwd_tflops / peaks["bf16_tflops"],
             "frac_of_sustained": fwd_tflops / peaks["bf16_tflops_sustained"],
             "peak_source": f"{peaks['source']} bf16_tflops (burst)",
+            # DRAM bytes of one launch from an ncu capture of the current source
+            # (None once the kernel source changed), against the compulsory
+            # bytes (Q, K, V read, O, LSE written).
+            "traffic": traffic_fwd,
+            "traffic_algorithmic": fb,
             "avg_us": fwd_avg * 1e6,
         },
         "decode_avg_us": dec_avg * 1e6,

@@ -34,6 +34,31 @@ def oracle_fwd(q, k, v, scale, causal, heads=None, rows=None, threads=None):
     return O, LSE
 
 
+def oracle_fwd_head_rows(q, k, v, scale, causal, head, rows, threads=None):
+    """Oracle O, LSE of one flat head at the given query rows, the rows split
+    over host threads (rows are independent; each chunk is one oracle call).
+    Returns arrays shaped (1, len(rows), d) / (1, len(rows))."""
+    from concurrent.futures import ThreadPoolExecutor
+    import os
+
+    rows = list(rows)
+    threads = threads or min(len(rows), os.cpu_count() or 1)
+    chunks = [rows[i::threads] for i in range(threads)]
+    B, H, N, d = q.shape
+    Q = to_f64(q.reshape(B * H, N, d)[head:head + 1])
+    K = to_f64(k.reshape(-1, N, d)[head:head + 1])
+    V = to_f64(v.reshape(-1, N, d)[head:head + 1])
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        parts = list(ex.map(lambda c: oracle.attention(Q, K, V, scale, causal, rows=c, threads=1),
+                            chunks))
+    O = np.empty((1, len(rows), d))
+    L = np.empty((1, len(rows)))
+    for i, (o, l) in enumerate(parts):
+        O[0, i::threads] = o[0]
+        L[0, i::threads] = l[0]
+    return O, L
+
+
 def compare_fwd(o_gpu, lse_gpu, O_ref, LSE_ref, heads, rows):
     B, H, N, d = o_gpu.shape
     of = o_gpu.reshape(B * H, N, d)

@@ -11,7 +11,7 @@ import torch
 
 import exact_attention_tma_gb300 as ea
 from exact_attention_tma_gb300.inputs import WORKLOADS, fwd_inputs, workload_inputs
-from parity import assert_within, compare_fwd, oracle_fwd
+from parity import assert_within, compare_fwd, oracle_fwd, oracle_fwd_head_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -135,12 +135,32 @@ def test_causal_workload_sampled():
 def test_noncausal_workload_sampled():
     w = WORKLOADS["noncausal_fwd"]
     heads = np.random.default_rng(2).choice(w.B * w.H, 24, replace=False).tolist()
-    _sampled("noncausal_fwd", heads=sorted(heads), rows=_rows(w.N, 40, 2), full_heads=[5])
+    _sampled("noncausal_fwd", heads=sorted(heads), rows=_rows(w.N, 40, 2),
+             full_heads=[5, w.B * w.H - 1])
+
+
+def _one_row_per_tile(N, seed):
+    """One row in every 128-row query tile (at a varying offset), plus tile edges."""
+    rng = np.random.default_rng(seed)
+    rows = {t * 128 + int(rng.integers(128)) for t in range(N // 128)}
+    return sorted(rows | {0, 127, 128, 255, N - 129, N - 128, N - 1})
 
 
 def test_long_causal_workload_sampled():
+    # Every head, one row in each 128-row query tile: every persistent work
+    # item of the launch (the short causal blocks of the last heads included)
+    # contributes compared rows.
     w = WORKLOADS["long_causal_fwd"]
-    _sampled("long_causal_fwd", heads=[0, 7, 19, 31], rows=_rows(w.N, 40, 3))
+    _sampled("long_causal_fwd", heads=range(w.B * w.H), rows=_one_row_per_tile(w.N, 3))
+
+
+def test_long_causal_workload_one_full_head():
+    # Head 17 in full (all 16384 rows), the oracle's rows split over the host cores.
+    w = WORKLOADS["long_causal_fwd"]
+    q, k, v = workload_inputs(w, device="cuda")
+    o, lse = _run(q, k, v, w.causal, w.scale)
+    O_ref, L_ref = oracle_fwd_head_rows(q, k, v, w.scale, w.causal, 17, range(w.N))
+    assert_within(compare_fwd(o, lse, O_ref, L_ref, [17], None))
 
 
 @pytest.mark.parametrize("d", [64, 128])
