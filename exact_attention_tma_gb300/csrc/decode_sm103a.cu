@@ -242,14 +242,20 @@ struct Paging {
   unsigned *status;
 };
 
+// Paged, one query head per K/V head (GQ = 1): 4 keys per lane group per
+// batch and at most 72 registers, so that 7 CTAs fit on an SM; with 8 keys
+// (94 registers, 5 CTAs) the paged cache streamed 15 % slower than the
+// contiguous one although both read the same bytes (fewer warps, fewer bytes
+// in flight).
 template <int D, int GQ, bool PAGED>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, (PAGED && GQ == 1) ? 7 : 1)
     attn_decode_gqa_split_kernel(const __nv_bfloat16 *__restrict__ q,
                                  const __nv_bfloat16 *__restrict__ Kc,
                                  const __nv_bfloat16 *__restrict__ Vc, float *__restrict__ ws_o,
                                  float *__restrict__ ws_lse, int H, int H_kv, int L, int chunk,
                                  int nsplit, float scale_log2, Paging pg) {
-  constexpr int U = (GQ >= 8) ? 4 : 8;   // keys per lane group per batch (register budget)
+  // Keys per lane group per batch (register budget, and occupancy when paged).
+  constexpr int U = (GQ >= 8) ? 4 : (PAGED && GQ == 1) ? 4 : 8;
   constexpr int LPK = D / 8;             // lanes per key row
   constexpr int KPI = 32 / LPK;          // keys per warp-wide load
   constexpr int NG = kWarps * KPI;       // lane groups per CTA
@@ -420,7 +426,9 @@ __global__ void __launch_bounds__(kWarps * 32)
 // ~108 CTAs per SM in flight over the call (B16 H32 L8192: 32 splits; B64
 // H32 L2048: 8 splits, 7.09 against 6.64 TB/s with 32), the paged kernel with
 // ~13 (B16 H32 L8192, 64-token pages: 4 splits, 5.99 against 5.79 TB/s; B64
-// L2048: 5.97 against 4.70; B4: 16 splits, 5.35 against 5.04).
+// L2048: 5.97 against 4.70; B4: 16 splits, 5.35 against 5.04; measured before
+// the paged kernel's occupancy change, after which targets of 26 and 54 gave
+// the same or slower times).
 static int pow2_splits(long long units, long long target, int L) {
   int s = 1;
   while (s < kDecodeSplits && 1.41421356 * static_cast<double>(units) * s < static_cast<double>(target))
