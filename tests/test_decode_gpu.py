@@ -81,3 +81,25 @@ def test_peaky_scores():
     torch.cuda.synchronize()
     O_ref, hs = _ref(q, K, V, 0.125)
     _check(o, O_ref, hs)
+
+
+def test_concurrent_calls_on_several_streams():
+    """Calls running at the same time on different streams, each with a
+    workspace of its own (160 calls in flight in groups of four), each give
+    exactly the result of the same call made alone."""
+    B, H, L, d = 2, 16, 3000, 128
+    ins = [decode_inputs(B, H, L, d, seed=50 + n, device="cuda") for n in range(4)]
+    refs = [ea.decode(q, K, V, scale=d ** -0.5) for q, K, V in ins]
+    torch.cuda.synchronize()
+    nbytes = ea.attn_decode_workspace_bytes(B, H, L, d)
+    wss = [torch.empty(nbytes, dtype=torch.uint8, device="cuda") for _ in range(4)]
+    outs = [torch.empty_like(q) for q, _, _ in ins]
+    streams = [torch.cuda.Stream() for _ in range(4)]
+    for rep in range(40):   # 160 calls in flight in groups of four
+        for s, (q, K, V), o, ws in zip(streams, ins, outs, wss):
+            with torch.cuda.stream(s):
+                ea.attn_decode_ws(q, K, V, o, d ** -0.5, ws, stream=s)
+    torch.cuda.synchronize()
+    for o, ref in zip(outs, refs):
+        assert torch.equal(o, ref)
+    assert ea.attn_get_device_status() == 0
