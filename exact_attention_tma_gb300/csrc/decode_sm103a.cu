@@ -48,6 +48,9 @@ __global__ void __launch_bounds__(kWarps * 32)
   // The combine kernel is a programmatic dependent of this grid: it may
   // launch once every CTA has started, and waits for this grid's partials.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // This grid is itself a programmatic dependent of the previous kernel in
+  // the stream: wait for it before reading q and the caches.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // 1-D grid: consecutive CTAs read consecutive chunks of one head.
   const int split = blockIdx.x % nsplit;
   const int bh = blockIdx.x / nsplit;
@@ -176,6 +179,9 @@ __global__ void __launch_bounds__(128)
                                __nv_bfloat16 *__restrict__ O, int BH, int nsplit) {
   const int head = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+  // The next kernel in the stream may launch now (it waits for this grid
+  // before reading anything this grid writes).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // Launched as a programmatic dependent of the split kernel: wait for its
   // partials (a no-op when the previous launch did not allow it to start early).
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -459,10 +465,22 @@ static cudaError_t launch_t(const void *q, const void *Kc, const void *Vc, void 
   const int chunk = (L + nsplit - 1) / nsplit;
   float *ws_o = static_cast<float *>(ws);
   float *ws_lse = ws_o + static_cast<size_t>(BH) * nsplit * D;
-  attn_decode_split_kernel<D><<<static_cast<unsigned>(BH) * nsplit, kWarps * 32, 0, stream>>>(
-      static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(Kc),
-      static_cast<const __nv_bfloat16 *>(Vc), ws_o, ws_lse, L, chunk, nsplit, scale_log2);
-  cudaError_t e = cudaGetLastError();
+  // A programmatic dependent of the previous kernel in the stream (it waits
+  // for that kernel before its first read): the launch overlaps its end.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(BH) * nsplit);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_decode_split_kernel<D>,
+                                     static_cast<const __nv_bfloat16 *>(q),
+                                     static_cast<const __nv_bfloat16 *>(Kc),
+                                     static_cast<const __nv_bfloat16 *>(Vc), ws_o, ws_lse, L, chunk,
+                                     nsplit, scale_log2);
   if (e != cudaSuccess) return e;
   return launch_decode_combine(ws_o, ws_lse, O, BH, D, nsplit, stream);
 }

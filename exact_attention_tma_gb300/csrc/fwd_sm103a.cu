@@ -358,6 +358,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // One thread of the TMA warp sets up the barriers and at once starts the
   // first item's loads, in the order the first MMAs need them (Q_0 and K_0,
   // then Q_1 and V_0), while the MMA warp allocates TMEM.
+  // The next kernel in the stream may launch now (it cannot share an SM with
+  // this one's shared memory, and it waits for this grid before reading).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == kWarpTMA * 32) {
     for (int qb = 0; qb < NQB; ++qb) {
       mbar_init(B_Q(qb), 1);
@@ -391,6 +394,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmO);
     Item it0;
     if (item_at(static_cast<int>(blockIdx.x), it0)) {   // (always true: the grid is no larger than the item count)
+      // Launched as a programmatic dependent of the previous kernel in the
+      // stream: its inputs may come from that kernel, so wait for it before
+      // the first load (bf16; the FP8 instance's Q and K come from before the
+      // V^T pass, so it waits just before its first V^T load).
+      if constexpr (!F8) asm volatile("griddepcontrol.wait;" ::: "memory");
       load_q(it0, 0, 0);
       mbar_arrive_expect_tx(B_KF(0), C::KV_BYTES);
       load_k(it0.kvh, 0, 0);
@@ -723,7 +731,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     if (warp == kWarpTMA) {
       // ------------------------------------------------------ TMA producer
-      if constexpr (F8) asm volatile("griddepcontrol.wait;" ::: "memory");
+      // (Every lane: the loads below follow the previous kernel in the stream.)
+      asm volatile("griddepcontrol.wait;" ::: "memory");
       // (The first item's Q tiles and first K/V tile were issued before the
       // CTA-wide barrier.)  A Q buffer is refilled once the MMA warp has
       // released it after its previous item's last Q K^T.
@@ -1034,26 +1043,22 @@ static cudaError_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const 
   unsigned *sched = nullptr;
   e = sched_slot(&sched);
   if (e != cudaSuccess) return e;
-  if constexpr (F8) {
-    // Launched while the V^T pass before it is still running (it signals
-    // once all of its blocks have started): the set-up and the Q and K loads
-    // overlap the pass's end, and the first V^T load waits for its results.
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = C::SMEM_ALLOC;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, LSE, N, BH, n_blk, H, group, scale_log2,
-                              out_mul, status, sched);
-  }
-  kern<<<static_cast<unsigned>(grid), kThreads, C::SMEM_ALLOC, stream>>>(
-      mq, mk, mv, mo, LSE, N, BH, n_blk, H, group, scale_log2, out_mul, status, sched);
-  return cudaGetLastError();
+  // Launched as a programmatic dependent of the previous kernel in the stream
+  // (FP8: the V^T pass, which signals once all of its blocks have started):
+  // the set-up (barriers, TMEM, descriptor prefetch) overlaps that kernel's
+  // end, and the loads wait for it (griddepcontrol.wait above).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, LSE, N, BH, n_blk, H, group, scale_log2,
+                            out_mul, status, sched);
 }
 
 }  // namespace fwd
