@@ -477,44 +477,47 @@ def _pct(xs, q):
     return ys[lo] + (ys[hi] - ys[lo]) * (pos - lo)
 
 
-def per_config(ea, peaks, dev, stream, reps=20, warmup=20):
+def per_config(ea, peaks, dev, stream, reps=20, warmup=20, b2b_launches=30):
     """Each performance workload on its own: `warmup` untimed launches, then
     `reps` timed launches (CUDA events on the launching stream) with an L2
     flush before each: a 256 MB write, then a read of the same buffer, so that
     the dirty lines the write leaves in L2 are written back before the timed
     call rather than during it.  Reports the median, p10 and p90 of the
-    launch times, and the roofline fraction of the median."""
+    launch times, and the roofline fraction of the median.
+
+    Also `b2b_us`: `b2b_launches` calls back to back between one pair of
+    events, cycling over copies of the inputs whose total exceeds four times
+    L2 (so no call finds its inputs there), as calls follow one another in a
+    stream; the per-call mean of three such runs, median taken."""
     import torch
 
     from exact_attention_tma_gb300.inputs import WORKLOADS, workload_inputs
 
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     flush_words = flush.view(torch.int32)
-    out = {}
-    for name in ("causal_fwd", "noncausal_fwd", "long_causal_fwd", "decode", "gqa_fwd",
-                 "gqa_decode", "paged_decode", "paged_gqa_decode", "causal_bwd", "fp8_causal_fwd",
-                 "fp8_long_causal_fwd"):
-        w = WORKLOADS[name]
+    l2_bytes = 129 * 1024 * 1024
+
+    def make_call(w):
+        """One call of workload w on buffers of its own: (call, bytes of the buffers)."""
         ins = workload_inputs(w, dev)
         gqa = w.H_kv != w.H
         if w.kind == "fwd":
             o = torch.empty_like(ins[0])
             lse = torch.empty(ins[0].shape[:3], dtype=torch.float32, device=dev)
             fn = ea.attn_fwd_gqa if gqa else ea.attn_fwd
+            bufs = (*ins, o, lse)
             call = lambda: fn(*ins, o, lse, w.causal, w.scale, stream)  # noqa: E731
-            flops, nbytes = fwd_work(w)
         elif w.kind == "paged":
             o = torch.empty_like(ins[0])
+            bufs = (*ins, o)
             call = lambda: ea.attn_decode_paged(*ins, o, w.scale, stream)  # noqa: E731
-            flops, nbytes = dec_work(w)
         elif w.kind == "fp8":
             (q8, k8, v8), ds = ins
             o = torch.empty(q8.shape, dtype=torch.bfloat16, device=dev)
             lse = torch.empty(q8.shape[:3], dtype=torch.float32, device=dev)
+            bufs = (q8, k8, v8, o, lse)
             call = lambda: ea.attn_fwd_fp8(q8, k8, v8, o, lse, w.causal, w.scale,  # noqa: E731
                                            *ds, stream)
-            flops, nbytes = fwd_work(w)
-            nbytes = nbytes - 3 * w.B * w.H * w.N * w.d   # 1-byte Q, K, V
         elif w.kind == "bwd":
             # O and LSE of the forward are inputs; only the backward is timed.
             q, k, v, do = ins
@@ -522,13 +525,29 @@ def per_config(ea, peaks, dev, stream, reps=20, warmup=20):
             lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
             ea.attn_fwd_gqa(q, k, v, o, lse, w.causal, w.scale, stream)
             grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+            bufs = (q, k, v, do, o, lse, *grads)
             call = lambda: ea.attn_bwd(q, k, v, o, do, lse, *grads, w.causal, w.scale,  # noqa: E731
                                        stream)
-            flops, nbytes = bwd_work(w)
         else:
             o = torch.empty_like(ins[0])
             fn = ea.attn_decode_gqa if gqa else ea.attn_decode
+            bufs = (*ins, o)
             call = lambda: fn(*ins, o, w.scale, stream)  # noqa: E731
+        return call, sum(t.numel() * t.element_size() for t in bufs if torch.is_tensor(t))
+
+    out = {}
+    for name in ("causal_fwd", "noncausal_fwd", "long_causal_fwd", "decode", "gqa_fwd",
+                 "gqa_decode", "paged_decode", "paged_gqa_decode", "causal_bwd", "fp8_causal_fwd",
+                 "fp8_long_causal_fwd"):
+        w = WORKLOADS[name]
+        call, set_bytes = make_call(w)
+        if w.kind in ("fwd", "fp8"):
+            flops, nbytes = fwd_work(w)
+            if w.kind == "fp8":
+                nbytes = nbytes - 3 * w.B * w.H * w.N * w.d   # 1-byte Q, K, V
+        elif w.kind == "bwd":
+            flops, nbytes = bwd_work(w)
+        else:
             flops, nbytes = dec_work(w)
         for _ in range(warmup):
             call()
@@ -543,6 +562,20 @@ def per_config(ea, peaks, dev, stream, reps=20, warmup=20):
             b.synchronize()
             times.append(a.elapsed_time(b) / 1e3)
         t = statistics.median(times)
+        # Back to back over input copies totalling more than 4 x L2.
+        calls = [call] + [make_call(w)[0] for _ in range(max(1, -(-4 * l2_bytes // set_bytes)) - 1)]
+        for c in calls:
+            c()
+        b2b = []
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for n in range(b2b_launches):
+                calls[n % len(calls)]()
+            b.record(stream)
+            b.synchronize()
+            b2b.append(a.elapsed_time(b) / 1e3 / b2b_launches)
+        tb = statistics.median(b2b)
         if w.kind == "fp8":
             # FP8 tensor peak: the measured bf16 peak x 2 (the nominal ratio).
             roof = max(flops / (2 * peaks["bf16_tflops"] * 1e12), nbytes / (peaks["hbm_gbs"] * 1e9))
@@ -550,13 +583,14 @@ def per_config(ea, peaks, dev, stream, reps=20, warmup=20):
             roof = roof_time(flops, nbytes, peaks)
         rec = {"median_us": t * 1e6, "p10_us": _pct(times, 10) * 1e6,
                "p90_us": _pct(times, 90) * 1e6, "samples": len(times), "warmup": warmup,
-               "roofline_us": roof * 1e6, "frac_of_roofline": roof / t}
+               "roofline_us": roof * 1e6, "frac_of_roofline": roof / t,
+               "b2b_us": tb * 1e6, "b2b_copies": len(calls), "b2b_frac_of_roofline": roof / tb}
         if w.kind in ("fwd", "bwd", "fp8"):
             rec["tflops"] = flops / t / 1e12
         else:
             rec["gbs"] = nbytes / t / 1e9
         out[name] = rec
-        del ins, o
+        del call, calls
     return out
 
 
