@@ -12,9 +12,11 @@
 //     dQ = scale dS K,   dK = scale dS^T Q.
 //
 // Three launches:
-//   1. prep:  delta_i and L_i log2(e) per query row, into a workspace padded
-//             to whole 128-row tiles (padding: delta = 0, L = +inf, so padded
-//             query rows get P = 0 in every tile that reads them);
+//   1. prep:  -delta_i and -L_i log2(e) per query row (negated, so that the
+//             tiles' exponent and dP - delta are single packed fp32x2 FMAs /
+//             adds), into a workspace padded to whole 128-row tiles (padding:
+//             delta = 0, L = +inf, so padded query rows get P = 0 in every
+//             tile that reads them);
 //   2. dK/dV: one CTA per (K/V head, 128-key tile).  K and V stay in shared
 //             memory; the query tiles of every query head of the group stream
 //             through a two-stage TMA ring (Q, dO, L, delta).  Per query tile
@@ -26,7 +28,7 @@
 //             without atomics.
 //   3. dQ:    one CTA per (query head, 128-query tile); K/V tiles stream
 //             through the ring; S = Q K^T and dP = dO V^T into TMEM, dS back
-//             over S, dQ += dS K in TMEM.
+//             over dP, dQ += dS K in TMEM.
 // dQ is computed by its own kernel (recomputing S and dP once more) rather
 // than accumulated with atomics across the dK/dV CTAs: the gradient
 // reduction stays deterministic and free of the atomic contention that the
@@ -93,10 +95,12 @@ struct CfgKV {
   static_assert(TM_DPT + BT <= kTmemCols, "tensor memory budget");
 };
 
-// dQ kernel: shared memory = a ring of (K, V) tiles; TMEM S (dS) | dP | dQ |
+// dQ kernel: shared memory = a ring of (K, V) tiles; TMEM S | dP (dS) | dQ |
 // Q | dO.  The query tile's Q and dO sit in TMEM as the A operands of
 // S = Q K^T and dP = dO V^T, so those products read only K / V from shared
-// memory (half the shared-memory operand traffic of two SS products).
+// memory (half the shared-memory operand traffic of two SS products).  Q and
+// dO arrive by TMA in the ring's last stage, which holds K / V only from the
+// third key tile on, after they have been copied into TMEM.
 template <int D>
 struct CfgQ {
   static_assert(D == 64 || D == 128, "head dimension");
@@ -108,8 +112,10 @@ struct CfgQ {
   static constexpr uint32_t STAGE_BYTES = 2 * TILE;
   static constexpr int NST = (D == 64) ? 4 : 3;          // K/V ring depth
   static constexpr uint32_t OFF_BAR = OFF_STAGE + NST * STAGE_BYTES;
-  // q (Q, dO in TMEM), full[NST], empty[NST], s[2], dp[2], p[2], done, drain
-  static constexpr int NBAR = 1 + 2 * NST + 8;
+  // q (Q, dO in TMEM), full[NST], empty[NST], s[2], dp[2], p[2], done, drain,
+  // s read[2], Q / dO landed
+  static constexpr int NBAR = 1 + 2 * NST + 8 + 3;
+  static constexpr int ST_QDO = NST - 1;                 // stage that first holds Q, dO
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;
   static constexpr uint32_t SMEM_ALLOC =
@@ -124,15 +130,15 @@ struct CfgQ {
 };
 
 // ------------------------------------------------------------------ prep
-// delta = sum_k dO O (fp32) and L log2(e) per (head, padded row).  D / 8
+// -delta = -sum_k dO O (fp32) and -L log2(e) per (head, padded row).  D / 8
 // threads per row, 16-byte loads, two rows per thread (both loads issued
 // before either is used).
 constexpr int kPrepThreads = 256;
 template <int D>
 __global__ void __launch_bounds__(kPrepThreads)
     attn_bwd_prep_kernel(const __nv_bfloat16 *__restrict__ O, const __nv_bfloat16 *__restrict__ dO,
-                         const float *__restrict__ LSE, float *__restrict__ lse2,
-                         float *__restrict__ delta, int N, int N_pad) {
+                         const float *__restrict__ LSE, float *__restrict__ nl2,
+                         float *__restrict__ ndl, int N, int N_pad) {
   constexpr int TPR = D / 8;                          // threads per row
   constexpr int RPB = kPrepThreads / TPR;             // rows per block and pass
   const int sub = threadIdx.x % TPR;
@@ -171,11 +177,11 @@ __global__ void __launch_bounds__(kPrepThreads)
       if (sub == 0 && ii[u] < N_pad) {
         const size_t r = bh * N_pad + ii[u];
         if (ii[u] < N) {
-          delta[r] = acc;
-          lse2[r] = LSE[bh * N + ii[u]] * kLog2e;
+          ndl[r] = -acc;
+          nl2[r] = -LSE[bh * N + ii[u]] * kLog2e;
         } else {   // padding row: P = 0 wherever it is read
-          delta[r] = 0.f;
-          lse2[r] = INFINITY;
+          ndl[r] = 0.f;
+          nl2[r] = -INFINITY;
         }
       }
     }
@@ -203,6 +209,15 @@ __device__ __forceinline__ void stage_row32(uint32_t stage, int row, int col0,
 }
 constexpr uint32_t kEpiBar = 1;   // named barrier of the compute warps (epilogue)
 
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
 // Both kernels run two independent pipelines, one per half of the 128-wide
 // score tile (query columns 0-63 / 64-127 in the dK/dV kernel, key columns
 // in the dQ kernel).  Compute warps 4h..4h+3 own half h; the MMA warp issues
@@ -218,8 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tmV,
                          const __grid_constant__ CUtensorMap tmdO,
                          const __grid_constant__ CUtensorMap tmdK,
-                         const __grid_constant__ CUtensorMap tmdV, const float *__restrict__ lse2,
-                         const float *__restrict__ delta, int N, int N_pad, int H, int H_kv,
+                         const __grid_constant__ CUtensorMap tmdV, const float *__restrict__ nl2,
+                         const float *__restrict__ ndl, int N, int N_pad, int H, int H_kv,
                          int BHkv, int n_blk, float scale_log2, float scale, unsigned *status,
                          unsigned *sched) {
   using C = CfgKV<D>;
@@ -366,8 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(st + C::ST_DO + kb * kBoxBytes, &tmdO, kb * 64, qt * BT, bh, B_FULL(s));
         }
         const size_t row0 = static_cast<size_t>(bh) * N_pad + static_cast<size_t>(qt) * BT;
-        bulk_load_1d(st + C::ST_LSE, lse2 + row0, BT * 4, B_FULL(s));
-        bulk_load_1d(st + C::ST_DELTA, delta + row0, BT * 4, B_FULL(s));
+        bulk_load_1d(st + C::ST_LSE, nl2 + row0, BT * 4, B_FULL(s));
+        bulk_load_1d(st + C::ST_DELTA, ndl + row0, BT * 4, B_FULL(s));
       }
       ++g;
       return true;
@@ -539,12 +554,14 @@ __global__ void __launch_bounds__(kThreads, 1)
              __all_sync(0xffffffffu, mbar_wait(B_S(h), gs & 1, status, abort_flag));
         if (!ok) break;
         tc_fence_after();
-        const float *lse_s =
+        // The stage's -L log2(e) and -delta, one per query column.
+        const float *nl_s =
             reinterpret_cast<const float *>(smem + C::OFF_STAGE + s * C::STAGE_BYTES + C::ST_LSE);
-        const float *del_s =
+        const float *nd_s =
             reinterpret_cast<const float *>(smem + C::OFF_STAGE + s * C::STAGE_BYTES + C::ST_DELTA);
         const bool diag = CAUSAL && it == itm.jt;
         // P^T for the half's 64 queries while the dP^T product is still running.
+        const float2 sc2 = make_float2(scale_log2, scale_log2);
         float p[64];
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -554,15 +571,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait_regs(sr);
 #pragma unroll
           for (int k = 0; k < 32; k += 4) {
-            const float4 lv = *reinterpret_cast<const float4 *>(lse_s + col0 + k);
-            const float lsev[4] = {lv.x, lv.y, lv.z, lv.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              float pe = ex2_approx(fmaf(__uint_as_float(sr[k + e]), scale_log2, -lsev[e]));
-              if (diag && col0 + k + e < row) pe = 0.f;   // query before key: masked
-              p[32 * c + k + e] = pe;
-            }
+            const float4 lv = *reinterpret_cast<const float4 *>(nl_s + col0 + k);
+            const float2 x0 = ffma2(
+                make_float2(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), sc2,
+                make_float2(lv.x, lv.y));
+            const float2 x1 = ffma2(
+                make_float2(__uint_as_float(sr[k + 2]), __uint_as_float(sr[k + 3])), sc2,
+                make_float2(lv.z, lv.w));
+            p[32 * c + k] = ex2_approx(x0.x);
+            p[32 * c + k + 1] = ex2_approx(x0.y);
+            p[32 * c + k + 2] = ex2_approx(x1.x);
+            p[32 * c + k + 3] = ex2_approx(x1.y);
           }
+        }
+        if (diag) {   // (warp-uniform) query before key: masked
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (64 * h + e < row) p[e] = 0.f;
         }
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(B_DP(h), gs & 1, status, abort_flag)))) break;
         tc_fence_after();
@@ -575,16 +600,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t pk[16], dk[16];
 #pragma unroll
           for (int k = 0; k < 32; k += 4) {
-            const float4 dv = *reinterpret_cast<const float4 *>(del_s + col0 + k);
-            const float delv[4] = {dv.x, dv.y, dv.z, dv.w};
-            float ds[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              ds[e] = p[32 * c + k + e] * (__uint_as_float(dp[k + e]) - delv[e]);
+            const float4 dv = *reinterpret_cast<const float4 *>(nd_s + col0 + k);
+            const float2 d0 = fadd2(make_float2(__uint_as_float(dp[k]), __uint_as_float(dp[k + 1])),
+                                    make_float2(dv.x, dv.y));
+            const float2 d1 = fadd2(
+                make_float2(__uint_as_float(dp[k + 2]), __uint_as_float(dp[k + 3])),
+                make_float2(dv.z, dv.w));
+            const float2 s0 = fmul2(make_float2(p[32 * c + k], p[32 * c + k + 1]), d0);
+            const float2 s1 = fmul2(make_float2(p[32 * c + k + 2], p[32 * c + k + 3]), d1);
             pk[k / 2] = pack_bf16x2(p[32 * c + k], p[32 * c + k + 1]);
             pk[k / 2 + 1] = pack_bf16x2(p[32 * c + k + 2], p[32 * c + k + 3]);
-            dk[k / 2] = pack_bf16x2(ds[0], ds[1]);
-            dk[k / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+            dk[k / 2] = pack_bf16x2(s0.x, s0.y);
+            dk[k / 2 + 1] = pack_bf16x2(s1.x, s1.y);
           }
           tmem_st_16cols(tmem + lane_base + C::TM_ST + 64 * h + 16 * c, pk);
           tmem_st_16cols(tmem + lane_base + C::TM_DPT + 64 * h + 16 * c, dk);
@@ -656,11 +683,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------ dQ
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK,
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
+                       const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ CUtensorMap tmdO,
                        const __grid_constant__ CUtensorMap tmdQ,
-                       const __nv_bfloat16 *__restrict__ Q, const __nv_bfloat16 *__restrict__ dO,
-                       const float *__restrict__ lse2, const float *__restrict__ delta,
+                       const float *__restrict__ nl2, const float *__restrict__ ndl,
                        int N, int N_pad, int H, int H_kv,
                        int n_blk, float scale_log2, float scale, unsigned *status) {
   using C = CfgQ<D>;
@@ -689,14 +717,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar1 = bar0 + 8u * (1 + 2 * NST);
   auto B_S = [&](int h) { return bar1 + 8u * h; };          // S half h in TMEM
   auto B_DP = [&](int h) { return bar1 + 8u * (2 + h); };   // dP half h in TMEM
-  auto B_P = [&](int h) { return bar1 + 8u * (4 + h); };    // dS half h written
+  auto B_P = [&](int h) { return bar1 + 8u * (4 + h); };    // dS half h written (over dP)
   const uint32_t B_DONE = bar1 + 48;
   const uint32_t B_DRAIN = bar1 + 56;
+  auto B_SF = [&](int h) { return bar1 + 64 + 8u * h; };    // S half h read: region free
+  const uint32_t B_QL = bar1 + 80;                             // Q, dO landed in shared memory
+  static_assert(1 + 2 * NST + 8 + 3 == C::NBAR, "barrier count");
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+  const uint32_t st_qdo = sb + C::OFF_STAGE + C::ST_QDO * C::STAGE_BYTES;
 
   if (threadIdx.x == kWarpTMA * 32) {
     mbar_init(B_Q, kComputeWarps);
+    mbar_init(B_QL, 1);
     for (int s = 0; s < NST; ++s) {
       mbar_init(B_FULL(s), 1);
       mbar_init(B_EMPTY(s), 1);
@@ -705,11 +738,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(B_S(h), 1);
       mbar_init(B_DP(h), 1);
       mbar_init(B_P(h), kComputeWarps / 2);
+      mbar_init(B_SF(h), kComputeWarps / 2);
     }
     mbar_init(B_DONE, 1);
     mbar_init(B_DRAIN, 1);
     *abort_flag = 0;
     fence_mbar_init();
+    // The query tile's Q and dO first (inputs of the whole call: no wait for
+    // the kernels before this one).
+    mbar_arrive_expect_tx(B_QL, 2 * C::TILE);
+    for (int kb = 0; kb < C::KB; ++kb) {
+      tma_load_3d(st_qdo + C::ST_K + kb * kBoxBytes, &tmQ, kb * 64, it * BT, bh, B_QL);
+      tma_load_3d(st_qdo + C::ST_V + kb * kBoxBytes, &tmdO, kb * 64, it * BT, bh, B_QL);
+    }
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
@@ -728,6 +769,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int issued = 0;
     for (int j = 0; j < n_j; ++j) {
       const int s = j % NST;
+      // The stage that held Q and dO is refilled once they are in TMEM.
+      if (j == C::ST_QDO && !__all_sync(0xffffffffu, mbar_wait(B_Q, 0, status, abort_flag)))
+        break;
       if (!__all_sync(0xffffffffu,
                       mbar_wait(B_EMPTY(s), ((j / NST) & 1) ^ 1u, status, abort_flag)))
         break;
@@ -742,6 +786,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       issued = j + 1;
     }
     if (leader && *abort_flag) {
+      mbar_wait_drain(B_QL, 0, 100000000ull);
       for (int u = 0; u < NST && u < issued; ++u) {
         const int jj = issued - 1 - u;
         mbar_wait_drain(B_FULL(jj % NST), (jj / NST) & 1, 100000000ull);
@@ -763,7 +808,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // Half h of S = Q K^T and of dP = dO V^T: keys 64h..64h+63 of the tile;
     // Q / dO from TMEM (8 columns per 16-element step of the head dim).
-    auto issue_scores = [&](int s, int h) {
+    auto issue_s = [&](int s, int h) {
       const uint32_t so = (s * C::STAGE_BYTES + h * 64 * 128) >> 4;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
@@ -772,6 +817,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                        stk_lo + so + (C::ST_K >> 4) + koff, hi, kIdescS, kk > 0 ? 1u : 0u);
       }
       mma_commit(B_S(h));
+    };
+    auto issue_dp = [&](int s, int h) {
+      const uint32_t so = (s * C::STAGE_BYTES + h * 64 * 128) >> 4;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t koff = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
@@ -781,14 +829,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(B_DP(h));
     };
     // Half h of dQ += dS K: key steps 4h..4h+3, dS from TMEM (columns
-    // 64h..64h+31 of the S region), K MN-major (16-key steps).
+    // 64h..64h+31 of the dP region), K MN-major (16-key steps).
     auto issue_dq = [&](int s, int h, bool acc) {
       const uint32_t so = (s * C::STAGE_BYTES) >> 4;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int kk = 4 * h + u;
         const uint32_t boff = (kk * 16 * 128) >> 4;
-        mma_bf16_ts_lo(tmem + C::TM_DQ, tmem + C::TM_S + 64 * h + 8 * u,
+        mma_bf16_ts_lo(tmem + C::TM_DQ, tmem + C::TM_DP + 64 * h + 8 * u,
                        stm_lo + so + (C::ST_K >> 4) + boff, hi, kIdescG, (acc || u > 0) ? 1u : 0u);
       }
     };
@@ -796,28 +844,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       tc_fence_after();
       if (leader) {
-        issue_scores(0, 0);
-        issue_scores(0, 1);
+        issue_s(0, 0);
+        issue_s(0, 1);
+        issue_dp(0, 0);
+        issue_dp(0, 1);
       }
       __syncwarp();
     }
+    // Per key tile j: S of tile j + 1 goes out as soon as the compute warps
+    // have read S of tile j (dS is written over dP, not over S), so the next
+    // tile's exponentials overlap this tile's dQ and dP products; dP of tile
+    // j + 1 follows dQ of tile j, which reads the dS it overwrites (MMAs from
+    // one thread run in issue order).
     for (int j = 0; ok && j < n_j; ++j) {
-      const int s = j % NST;
+      const int s = j % NST, s1 = (j + 1) % NST;
+      const bool more = j + 1 < n_j;
+      if (more) {
+        if (!(ok = wait_all(B_FULL(s1), ((j + 1) / NST) & 1))) break;
+        for (int h = 0; h < 2; ++h) {
+          if (!(ok = wait_all(B_SF(h), j & 1))) break;
+          tc_fence_after();
+          if (leader) issue_s(s1, h);
+          __syncwarp();
+        }
+        if (!ok) break;
+      }
       for (int h = 0; h < 2; ++h) {
         if (!(ok = wait_all(B_P(h), j & 1))) break;
         tc_fence_after();
         if (leader) {
           issue_dq(s, h, j > 0 || h > 0);
-          if (h == 1) mma_commit(j + 1 < n_j ? B_EMPTY(s) : B_DONE);
+          if (h == 1) mma_commit(more ? B_EMPTY(s) : B_DONE);
+          if (more) issue_dp(s1, h);
         }
         __syncwarp();
-        if (j + 1 < n_j) {
-          if (h == 0 && !(ok = wait_all(B_FULL((j + 1) % NST), ((j + 1) / NST) & 1)))
-            break;
-          tc_fence_after();
-          if (leader) issue_scores((j + 1) % NST, h);
-          __syncwarp();
-        }
       }
     }
     if (leader) {
@@ -833,25 +893,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
     const size_t prow = static_cast<size_t>(bh) * N_pad + static_cast<size_t>(it) * BT + row;
     // This kernel is a programmatic dependent of the dK/dV kernel, which
-    // itself waited for the row pass: once that grid has finished, the
-    // row pass's L and delta are complete too.  Q, dO, K and V are inputs,
-    // so the loads and the first products need not wait.
+    // itself waited for the row pass: once that grid has finished, the row
+    // pass's -L log2(e) and -delta are complete too.  (Q, dO, K and V are
+    // inputs: their loads and the first products do not wait.)  The row's
+    // two values load while Q and dO arrive.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const float l2 = lse2[prow];
-    const float dl = delta[prow];
-    {
+    const float nl = nl2[prow];
+    const float nd = ndl[prow];
+    bool ok = __all_sync(0xffffffffu, mbar_wait(B_QL, 0, status, abort_flag));
+    if (ok) {
       // Warps of half 0 put this tile's Q rows into TMEM, warps of half 1
-      // its dO rows (row = lane, bf16 pairs along the columns; rows past N
-      // are zero).
-      const int qi = it * BT + row;
-      const __nv_bfloat16 *src = (h == 0 ? Q : dO) + (static_cast<size_t>(bh) * N + qi) * D;
+      // its dO rows (row = lane, bf16 pairs along the columns; the TMA load
+      // left rows past N zero).  A 128-byte row of a box holds its 16-byte
+      // chunk v at position v ^ (row % 8) (128-byte swizzle), so the 32
+      // lanes' loads of one chunk fall in distinct banks.
+      const uint32_t src = st_qdo + (h == 0 ? C::ST_K : C::ST_V) + row * 128;
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         uint32_t w[32];
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
-          uint4 x = make_uint4(0, 0, 0, 0);
-          if (qi < N) x = *reinterpret_cast<const uint4 *>(src + 64 * c + 8 * v);
+          const uint4 x = ld_shared_v4(src + c * kBoxBytes + ((v ^ (row & 7)) << 4));
           w[4 * v] = x.x;
           w[4 * v + 1] = x.y;
           w[4 * v + 2] = x.z;
@@ -860,12 +922,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_32cols(tmem + lane_base + (h == 0 ? C::TM_Q : C::TM_DO) + 32 * c, w);
       }
       tmem_st_wait();
+      // The TMA warp refills this stage (async proxy) after the reads above.
+      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(B_Q);
     }
-    bool ok = true;
-    for (int j = 0; j < n_j; ++j) {
+    const float2 sc2 = make_float2(scale_log2, scale_log2);
+    const float2 nl2v = make_float2(nl, nl);
+    const float2 nd2 = make_float2(nd, nd);
+    for (int j = 0; ok && j < n_j; ++j) {
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(B_S(h), j & 1, status, abort_flag)))) break;
       tc_fence_after();
       const bool diag = CAUSAL && j == it;
@@ -877,16 +943,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t sr[32];
         tmem_ld_32cols(tmem + lane_base + C::TM_S + col0, sr);
         tmem_ld_wait_regs(sr);
+        if (c == 1) {
+          // The half's S is in registers: its region may take the next tile's S.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(B_SF(h));
+        }
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int col = col0 + k;
-          float pe = ex2_approx(fmaf(__uint_as_float(sr[k]), scale_log2, -l2));
-          if ((diag && col > row) || col >= kmax) pe = 0.f;
-          p[32 * c + k] = pe;
+        for (int k = 0; k < 32; k += 2) {
+          const float2 x =
+              ffma2(make_float2(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), sc2, nl2v);
+          p[32 * c + k] = ex2_approx(x.x);
+          p[32 * c + k + 1] = ex2_approx(x.y);
+        }
+      }
+      if (diag || kmax < BT) {   // (warp-uniform) key after query, or past N: masked
+#pragma unroll
+        for (int e = 0; e < 64; ++e) {
+          const int col = 64 * h + e;
+          if ((diag && col > row) || col >= kmax) p[e] = 0.f;
         }
       }
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(B_DP(h), j & 1, status, abort_flag)))) break;
       tc_fence_after();
+      // dS as bf16 pairs over the first 32 columns of the half's dP region
+      // (chunk c's 16 columns over dP columns already read).
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const int col0 = 64 * h + 32 * c;
@@ -895,10 +976,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait_regs(dp);
         uint32_t dk[16];
 #pragma unroll
-        for (int k = 0; k < 32; k += 2)
-          dk[k / 2] = pack_bf16x2(p[32 * c + k] * (__uint_as_float(dp[k]) - dl),
-                                  p[32 * c + k + 1] * (__uint_as_float(dp[k + 1]) - dl));
-        tmem_st_16cols(tmem + lane_base + C::TM_S + 64 * h + 16 * c, dk);
+        for (int k = 0; k < 32; k += 2) {
+          const float2 d =
+              fadd2(make_float2(__uint_as_float(dp[k]), __uint_as_float(dp[k + 1])), nd2);
+          const float2 ds = fmul2(make_float2(p[32 * c + k], p[32 * c + k + 1]), d);
+          dk[k / 2] = pack_bf16x2(ds.x, ds.y);
+        }
+        tmem_st_16cols(tmem + lane_base + C::TM_DP + 64 * h + 16 * c, dk);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -941,8 +1025,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, bool CAUSAL>
 static cudaError_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                             const CUtensorMap &mdo, const CUtensorMap &mdq, const CUtensorMap &mdk,
-                            const CUtensorMap &mdv, const void *Q, const void *dO,
-                            const float *lse2, const float *delta, int B, int H, int H_kv, int N,
+                            const CUtensorMap &mdv, const float *nl2, const float *ndl, int B, int H, int H_kv, int N,
                             int N_pad, int n_blk, float scale, unsigned *status,
                             cudaStream_t stream) {
   const float scale_log2 = scale * kLog2e;
@@ -972,14 +1055,13 @@ static cudaError_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const 
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(kv_grid));
   cfg.dynamicSmemBytes = CfgKV<D>::SMEM_ALLOC;
-  e = cudaLaunchKernelEx(&cfg, kkv, mq, mk, mv, mdo, mdk, mdv, lse2, delta, N, N_pad, H, H_kv,
+  e = cudaLaunchKernelEx(&cfg, kkv, mq, mk, mv, mdo, mdk, mdv, nl2, ndl, N, N_pad, H, H_kv,
                          B * H_kv, n_blk, scale_log2, scale, status, sched);
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3(static_cast<unsigned>(B * H * n_blk));
   cfg.dynamicSmemBytes = CfgQ<D>::SMEM_ALLOC;
-  return cudaLaunchKernelEx(&cfg, kq, mk, mv, mdq, static_cast<const __nv_bfloat16 *>(Q),
-                            static_cast<const __nv_bfloat16 *>(dO), lse2, delta, N, N_pad, H,
-                            H_kv, n_blk, scale_log2, scale, status);
+  return cudaLaunchKernelEx(&cfg, kq, mq, mk, mv, mdo, mdq, nl2, ndl, N, N_pad, H, H_kv,
+                            n_blk, scale_log2, scale, status);
 }
 
 }  // namespace bwd
@@ -997,8 +1079,8 @@ cudaError_t launch_bwd(const void *Q, const void *K, const void *V, const void *
   const int n_blk = (N + BT - 1) / BT;
   const int N_pad = n_blk * BT;
   const long long rows = static_cast<long long>(B) * H * N_pad;
-  float *lse2 = static_cast<float *>(ws);
-  float *delta = lse2 + rows;
+  float *nl2 = static_cast<float *>(ws);    // -L log2(e) per padded row
+  float *ndl = nl2 + rows;                  // -delta per padded row
   // Grid: one row of blocks per head, up to 1024 blocks of 2 * 256 / (d / 8)
   // rows each along a head (a block loops when the head is longer).
   const int rows_per_block = 2 * kPrepThreads / (d / 8);
@@ -1006,12 +1088,12 @@ cudaError_t launch_bwd(const void *Q, const void *K, const void *V, const void *
                        static_cast<unsigned>(std::min(1024, (N_pad + rows_per_block - 1) / rows_per_block)));
   if (d == 128)
     attn_bwd_prep_kernel<128><<<prep_grid, kPrepThreads, 0, stream>>>(
-        static_cast<const __nv_bfloat16 *>(O), static_cast<const __nv_bfloat16 *>(dO), LSE, lse2,
-        delta, N, N_pad);
+        static_cast<const __nv_bfloat16 *>(O), static_cast<const __nv_bfloat16 *>(dO), LSE, nl2,
+        ndl, N, N_pad);
   else
     attn_bwd_prep_kernel<64><<<prep_grid, kPrepThreads, 0, stream>>>(
-        static_cast<const __nv_bfloat16 *>(O), static_cast<const __nv_bfloat16 *>(dO), LSE, lse2,
-        delta, N, N_pad);
+        static_cast<const __nv_bfloat16 *>(O), static_cast<const __nv_bfloat16 *>(dO), LSE, nl2,
+        ndl, N, N_pad);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
@@ -1021,13 +1103,13 @@ cudaError_t launch_bwd(const void *Q, const void *K, const void *V, const void *
       !make_bhnd_map(&mdv, dV, B * H_kv, N, d, BT))
     return cudaErrorInvalidValue;
   if (d == 128)
-    return causal ? launch_t<128, true>(mq, mk, mv, mdo, mdq, mdk, mdv, Q, dO, lse2, delta, B, H, H_kv, N,
+    return causal ? launch_t<128, true>(mq, mk, mv, mdo, mdq, mdk, mdv, nl2, ndl, B, H, H_kv, N,
                                         N_pad, n_blk, scale, status, stream)
-                  : launch_t<128, false>(mq, mk, mv, mdo, mdq, mdk, mdv, Q, dO, lse2, delta, B, H, H_kv, N,
+                  : launch_t<128, false>(mq, mk, mv, mdo, mdq, mdk, mdv, nl2, ndl, B, H, H_kv, N,
                                          N_pad, n_blk, scale, status, stream);
-  return causal ? launch_t<64, true>(mq, mk, mv, mdo, mdq, mdk, mdv, Q, dO, lse2, delta, B, H, H_kv, N, N_pad,
+  return causal ? launch_t<64, true>(mq, mk, mv, mdo, mdq, mdk, mdv, nl2, ndl, B, H, H_kv, N, N_pad,
                                      n_blk, scale, status, stream)
-                : launch_t<64, false>(mq, mk, mv, mdo, mdq, mdk, mdv, Q, dO, lse2, delta, B, H, H_kv, N,
+                : launch_t<64, false>(mq, mk, mv, mdo, mdq, mdk, mdv, nl2, ndl, B, H, H_kv, N,
                                       N_pad, n_blk, scale, status, stream);
 }
 
