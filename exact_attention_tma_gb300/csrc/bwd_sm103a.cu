@@ -60,8 +60,10 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kBoxBytes = 64 * BT * 2;    // one TMA box: 64 columns x 128 rows bf16
 constexpr float kLog2e = 1.44269504088896340736f;
 
-// dK/dV kernel: shared memory K | V | stages (Q, dO, L, delta); TMEM
-// dV | dK | S^T (P^T) | dP^T (dS^T).
+// dK/dV kernel: shared memory K | V | Q ring (Q tile + its rows' -L log2 e)
+// | dO ring (dO tile + its rows' -delta); TMEM dV | dK | S^T | dP^T (then
+// P^T and dS^T as bf16).  Q and dO have rings of their own so that each slot
+// frees as soon as its last product (dK for Q, dV for dO) has read it.
 template <int D>
 struct CfgKV {
   static_assert(D == 64 || D == 128, "head dimension");
@@ -69,18 +71,16 @@ struct CfgKV {
   static constexpr uint32_t TILE = BT * D * 2;
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = TILE;
-  static constexpr uint32_t OFF_STAGE = 2 * TILE;
-  static constexpr uint32_t ST_Q = 0;
-  static constexpr uint32_t ST_DO = TILE;
-  static constexpr uint32_t ST_LSE = 2 * TILE;          // 128 fp32
-  static constexpr uint32_t ST_DELTA = 2 * TILE + 512;  // 128 fp32
-  static constexpr uint32_t STAGE_BYTES = 2 * TILE + 1024;
-  static constexpr uint32_t STAGE_TX = 2 * TILE + 1024;
+  static constexpr uint32_t SLOT = TILE + 1024;          // tile + 128 fp32 (padded)
+  static constexpr uint32_t SLOT_ROWS = TILE;            // offset of the row values
+  static constexpr uint32_t SLOT_TX = TILE + 512;
   static constexpr int NST = (D == 64) ? 4 : 2;          // query-tile ring depth
-  static constexpr uint32_t OFF_BAR = OFF_STAGE + NST * STAGE_BYTES;
-  // kv, kv free, full[NST], empty[NST], s[2], dp[2], p[2], done, drain,
-  // item ring full[kRing], empty[kRing]
-  static constexpr int NBAR = 2 + 2 * NST + 8 + 2 * kRing;
+  static constexpr uint32_t OFF_QS = 2 * TILE;
+  static constexpr uint32_t OFF_DS = OFF_QS + NST * SLOT;
+  static constexpr uint32_t OFF_BAR = OFF_DS + NST * SLOT;
+  // kv, kv free, q full[NST], q empty[NST], do full[NST], do empty[NST], s,
+  // s read, dp, p[2], done, drain, item ring full[kRing], empty[kRing]
+  static constexpr int NBAR = 2 + 4 * NST + 7 + 2 * kRing;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 4 * kRing;   // tmem slot, abort flag, item ring
   // At least 116 KB so that one CTA runs per SM: each allocates all 512 TMEM
@@ -112,9 +112,9 @@ struct CfgQ {
   static constexpr uint32_t STAGE_BYTES = 2 * TILE;
   static constexpr int NST = (D == 64) ? 4 : 3;          // K/V ring depth
   static constexpr uint32_t OFF_BAR = OFF_STAGE + NST * STAGE_BYTES;
-  // q (Q, dO in TMEM), full[NST], empty[NST], s[2], dp[2], p[2], done, drain,
-  // s read[2], Q / dO landed
-  static constexpr int NBAR = 1 + 2 * NST + 8 + 3;
+  // q (Q, dO in TMEM), full[NST], empty[NST], s, s read, dp[2], p[2], done,
+  // drain, Q / dO landed
+  static constexpr int NBAR = 1 + 2 * NST + 9;
   static constexpr int ST_QDO = NST - 1;                 // stage that first holds Q, dO
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;
@@ -280,17 +280,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar0 = sb + C::OFF_BAR;
   const uint32_t B_KV = bar0;                                  // K, V of the item loaded
   const uint32_t B_KVE = bar0 + 8u;                            // K, V slots free (epilogue stored)
-  auto B_FULL = [&](int s) { return bar0 + 8u * (2 + s); };
-  auto B_EMPTY = [&](int s) { return bar0 + 8u * (2 + NST + s); };
-  const uint32_t bar1 = bar0 + 8u * (2 + 2 * NST);
-  auto B_S = [&](int h) { return bar1 + 8u * h; };          // S^T half h in TMEM
-  auto B_DP = [&](int h) { return bar1 + 8u * (2 + h); };   // dP^T half h in TMEM
-  auto B_P = [&](int h) { return bar1 + 8u * (4 + h); };    // P^T, dS^T half h written
-  const uint32_t B_DONE = bar1 + 48;                           // item's last products done
-  const uint32_t B_DRAIN = bar1 + 56;
-  auto B_IF = [&](int s) { return bar1 + 64 + 8u * s; };       // item slot s written
-  auto B_IE = [&](int s) { return bar1 + 64 + 8u * (kRing + s); };   // item slot s read by all
-  static_assert(2 + 2 * NST + 8 + 2 * kRing == C::NBAR, "barrier count");
+  auto B_QF = [&](int s) { return bar0 + 8u * (2 + s); };           // Q slot s loaded
+  auto B_QE = [&](int s) { return bar0 + 8u * (2 + NST + s); };     // Q slot s free
+  auto B_DF = [&](int s) { return bar0 + 8u * (2 + 2 * NST + s); };  // dO slot s loaded
+  auto B_DE = [&](int s) { return bar0 + 8u * (2 + 3 * NST + s); };  // dO slot s free
+  const uint32_t bar1 = bar0 + 8u * (2 + 4 * NST);
+  const uint32_t B_S = bar1;                                   // S^T in TMEM
+  const uint32_t B_SF = bar1 + 8;                              // S^T read: region free
+  const uint32_t B_DP = bar1 + 16;                             // dP^T in TMEM
+  auto B_P = [&](int h) { return bar1 + 24 + 8u * h; };     // P^T, dS^T half h written
+  const uint32_t B_DONE = bar1 + 40;                           // item's last products done
+  const uint32_t B_DRAIN = bar1 + 48;
+  auto B_IF = [&](int s) { return bar1 + 56 + 8u * s; };       // item slot s written
+  auto B_IE = [&](int s) { return bar1 + 56 + 8u * (kRing + s); };   // item slot s read by all
+  static_assert(2 + 4 * NST + 7 + 2 * kRing == C::NBAR, "barrier count");
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
   volatile int *item_ring = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 16);
@@ -318,14 +321,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(B_KV, 1);
     mbar_init(B_KVE, 1);
     for (int s = 0; s < NST; ++s) {
-      mbar_init(B_FULL(s), 1);
-      mbar_init(B_EMPTY(s), 1);
+      mbar_init(B_QF(s), 1);
+      mbar_init(B_QE(s), 1);
+      mbar_init(B_DF(s), 1);
+      mbar_init(B_DE(s), 1);
     }
-    for (int h = 0; h < 2; ++h) {
-      mbar_init(B_S(h), 1);
-      mbar_init(B_DP(h), 1);
-      mbar_init(B_P(h), kComputeWarps / 2);
-    }
+    mbar_init(B_S, 1);
+    mbar_init(B_SF, kComputeWarps);
+    mbar_init(B_DP, 1);
+    for (int h = 0; h < 2; ++h) mbar_init(B_P(h), kComputeWarps / 2);
     mbar_init(B_DONE, 1);
     mbar_init(B_DRAIN, 1);
     for (int s = 0; s < kRing; ++s) {
@@ -363,28 +367,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const bool leader = elect_one();
     int g = 0;                               // stages issued so far
+    int gd = 0;                              // dO loads issued so far
     int kv_items = 1;                        // items whose K/V load was issued
     bool ok = true;
     int k = static_cast<int>(blockIdx.x);
+    // Query tile t of the item into slot g % NST of each ring: Q with its
+    // rows' -L log2(e), then dO with their -delta, each once its slot is free.
     auto load_stage = [&](const Item &it, int t) {
       const int s = g % NST;
-      if (!__all_sync(0xffffffffu,
-                      mbar_wait(B_EMPTY(s), ((g / NST) & 1) ^ 1u, status, abort_flag)))
-        return false;
+      const uint32_t par = ((g / NST) & 1) ^ 1u;
+      const int bh = q_head(it, t);
+      const int qt = q_tile(it, t);
+      const size_t row0 = static_cast<size_t>(bh) * N_pad + static_cast<size_t>(qt) * BT;
+      if (!__all_sync(0xffffffffu, mbar_wait(B_QE(s), par, status, abort_flag))) return false;
       if (leader) {
-        const int bh = q_head(it, t);
-        const int qt = q_tile(it, t);
-        const uint32_t st = sb + C::OFF_STAGE + s * C::STAGE_BYTES;
-        mbar_arrive_expect_tx(B_FULL(s), C::STAGE_TX);
-        for (int kb = 0; kb < C::KB; ++kb) {
-          tma_load_3d(st + C::ST_Q + kb * kBoxBytes, &tmQ, kb * 64, qt * BT, bh, B_FULL(s));
-          tma_load_3d(st + C::ST_DO + kb * kBoxBytes, &tmdO, kb * 64, qt * BT, bh, B_FULL(s));
-        }
-        const size_t row0 = static_cast<size_t>(bh) * N_pad + static_cast<size_t>(qt) * BT;
-        bulk_load_1d(st + C::ST_LSE, nl2 + row0, BT * 4, B_FULL(s));
-        bulk_load_1d(st + C::ST_DELTA, ndl + row0, BT * 4, B_FULL(s));
+        const uint32_t st = sb + C::OFF_QS + s * C::SLOT;
+        mbar_arrive_expect_tx(B_QF(s), C::SLOT_TX);
+        for (int kb = 0; kb < C::KB; ++kb)
+          tma_load_3d(st + kb * kBoxBytes, &tmQ, kb * 64, qt * BT, bh, B_QF(s));
+        bulk_load_1d(st + C::SLOT_ROWS, nl2 + row0, BT * 4, B_QF(s));
       }
       ++g;
+      if (!__all_sync(0xffffffffu, mbar_wait(B_DE(s), par, status, abort_flag))) return false;
+      if (leader) {
+        const uint32_t st = sb + C::OFF_DS + s * C::SLOT;
+        mbar_arrive_expect_tx(B_DF(s), C::SLOT_TX);
+        for (int kb = 0; kb < C::KB; ++kb)
+          tma_load_3d(st + kb * kBoxBytes, &tmdO, kb * 64, qt * BT, bh, B_DF(s));
+        bulk_load_1d(st + C::SLOT_ROWS, ndl + row0, BT * 4, B_DF(s));
+      }
+      ++gd;
       return true;
     };
     for (int t = 0; ok; ++t) {
@@ -422,14 +434,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_drain(B_KV, (kv_items - 1) & 1, 100000000ull);
       for (int j = 0; j < NST && j < g; ++j) {
         const int tt = g - 1 - j;
-        mbar_wait_drain(B_FULL(tt % NST), (tt / NST) & 1, 100000000ull);
+        mbar_wait_drain(B_QF(tt % NST), (tt / NST) & 1, 100000000ull);
+      }
+      for (int j = 0; j < NST && j < gd; ++j) {
+        const int tt = gd - 1 - j;
+        mbar_wait_drain(B_DF(tt % NST), (tt / NST) & 1, 100000000ull);
       }
     }
     __syncwarp();
   } else if (warp == kWarpMMA) {
     // ------------------------------------------------------------ MMA
     const bool leader = elect_one();
-    constexpr uint32_t kIdescS = make_idesc_bf16(BT, BT / 2, 0, 0);
+    constexpr uint32_t kIdescS = make_idesc_bf16(BT, BT, 0, 0);
     constexpr uint32_t kIdescG = make_idesc_bf16(BT, D, 0, 1);
     // Low words of the shared-memory descriptors (one common high word):
     // K-major (head dim contiguous, 16-element k-steps inside a 64-column
@@ -440,50 +456,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t hi = static_cast<uint32_t>(dK0 >> 32);
     const uint32_t k_lo = static_cast<uint32_t>(dK0);
     const uint32_t v_lo = static_cast<uint32_t>(make_sdesc_sw128(sb + C::OFF_V, 16, 1024));
-    const uint32_t stk_lo = static_cast<uint32_t>(make_sdesc_sw128(sb + C::OFF_STAGE, 16, 1024));
-    const uint32_t stm_lo =
-        static_cast<uint32_t>(make_sdesc_sw128(sb + C::OFF_STAGE, kBoxBytes, 1024));
+    const uint32_t qk_lo = static_cast<uint32_t>(make_sdesc_sw128(sb + C::OFF_QS, 16, 1024));
+    const uint32_t dk_lo = static_cast<uint32_t>(make_sdesc_sw128(sb + C::OFF_DS, 16, 1024));
+    const uint32_t qm_lo =
+        static_cast<uint32_t>(make_sdesc_sw128(sb + C::OFF_QS, kBoxBytes, 1024));
+    const uint32_t dm_lo =
+        static_cast<uint32_t>(make_sdesc_sw128(sb + C::OFF_DS, kBoxBytes, 1024));
     auto wait_all = [&](uint32_t bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, abort_flag));
     };
-    // Half h of S^T = K Q^T and of dP^T = V dO^T: queries 64h..64h+63 (rows
-    // 64h.. of the stage's tiles, 64 rows x 128 B = 8 KB into each box).
-    auto issue_scores = [&](int s, int h) {
-      const uint32_t so = (s * C::STAGE_BYTES + h * 64 * 128) >> 4;
+    // S^T = K Q^T and dP^T = V dO^T over the whole query tile (N = 128:
+    // SS products at N = 64 are bound by shared-memory reads).
+    auto issue_st = [&](int s) {
+      const uint32_t so = (s * C::SLOT) >> 4;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t koff = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-        mma_bf16_ss_lo(tmem + C::TM_ST + 64 * h, k_lo + koff, stk_lo + so + (C::ST_Q >> 4) + koff,
-                       hi, kIdescS, kk > 0 ? 1u : 0u);
+        mma_bf16_ss_lo(tmem + C::TM_ST, k_lo + koff, qk_lo + so + koff, hi, kIdescS,
+                       kk > 0 ? 1u : 0u);
       }
-      mma_commit(B_S(h));
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t koff = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-        mma_bf16_ss_lo(tmem + C::TM_DPT + 64 * h, v_lo + koff, stk_lo + so + (C::ST_DO >> 4) + koff,
-                       hi, kIdescS, kk > 0 ? 1u : 0u);
-      }
-      mma_commit(B_DP(h));
+      mma_commit(B_S);
     };
-    // Half h of dV += P^T dO and dK += dS^T Q: the 16-query steps 4h..4h+3,
-    // A from TMEM (8 columns per step; half h's P^T / dS^T sit in columns
-    // 64h..64h+31 of their regions), B = the stage's dO / Q, MN-major.
-    auto issue_grads = [&](int s, int h, bool acc) {
-      const uint32_t so = (s * C::STAGE_BYTES) >> 4;
+    auto issue_dpt = [&](int s) {
+      const uint32_t so = (s * C::SLOT) >> 4;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t koff = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+        mma_bf16_ss_lo(tmem + C::TM_DPT, v_lo + koff, dk_lo + so + koff, hi, kIdescS,
+                       kk > 0 ? 1u : 0u);
+      }
+      mma_commit(B_DP);
+    };
+    // Half h of dK += dS^T Q (dk) or dV += P^T dO (!dk): the 16-query steps
+    // 4h..4h+3, A from TMEM, B = the slot's Q / dO, MN-major.  The compute
+    // warps left query chunk c (32 columns) of half h as P^T in dP^T columns
+    // 64h + 32c .. +15 and dS^T in 64h + 32c + 16 .. +31 (8 columns per step).
+    auto issue_grad = [&](int s, int h, bool dk, bool acc) {
+      const uint32_t so = (s * C::SLOT) >> 4;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int kk = 4 * h + u;
         const uint32_t boff = (kk * 16 * 128) >> 4;
-        mma_bf16_ts_lo(tmem + C::TM_DV, tmem + C::TM_ST + 64 * h + 8 * u,
-                       stm_lo + so + (C::ST_DO >> 4) + boff, hi, kIdescG, (acc || u > 0) ? 1u : 0u);
+        const uint32_t col = C::TM_DPT + 64 * h + 32 * (u >> 1) + 8 * (u & 1) + (dk ? 16 : 0);
+        mma_bf16_ts_lo(tmem + (dk ? C::TM_DK : C::TM_DV), tmem + col,
+                       (dk ? qm_lo : dm_lo) + so + boff, hi, kIdescG, (acc || u > 0) ? 1u : 0u);
       }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int kk = 4 * h + u;
-        const uint32_t boff = (kk * 16 * 128) >> 4;
-        mma_bf16_ts_lo(tmem + C::TM_DK, tmem + C::TM_DPT + 64 * h + 8 * u,
-                       stm_lo + so + (C::ST_Q >> 4) + boff, hi, kIdescG, (acc || u > 0) ? 1u : 0u);
-      }
+    };
+    // Issuing an MMA waits while the tensor pipe's queue is full, so this
+    // warp is never far ahead of the pipe, and a barrier round trip between
+    // two batches would leave the pipe idle.  Each barrier is therefore
+    // tested (non-blocking, every lane) before the batch ahead of it and the
+    // result read after the batch; only a phase not yet complete then takes
+    // the bounded wait.
+    auto ready = [&](uint32_t tst, uint32_t bar, uint32_t parity) {
+      return vote_all_ordered(tst) || wait_all(bar, parity);
     };
     bool ok = true;
     int g = 0;                               // stages consumed so far (= steps before this item)
@@ -494,39 +520,66 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The item's K and V, and its first stage.  dV and dK of the previous
       // item were read out by its epilogue before the compute warps handed
       // over this item's first P^T / dS^T, so the first gradient products
-      // below may overwrite them.
-      ok = wait_all(B_KV, t & 1) && wait_all(B_FULL(g % NST), (g / NST) & 1);
+      // below may overwrite them; the epilogue also came after the last
+      // reads of S^T and dP^T.
+      const uint32_t par0 = (g / NST) & 1;
+      ok = wait_all(B_KV, t & 1) && wait_all(B_QF(g % NST), par0) &&
+           wait_all(B_DF(g % NST), par0);
       if (ok) {
         tc_fence_after();
         if (leader) {
-          issue_scores(g % NST, 0);
-          issue_scores(g % NST, 1);
+          issue_st(g % NST);
+          issue_dpt(g % NST);
         }
         __syncwarp();
       }
+      // Per query tile, in the tensor pipe: S^T of the next tile (once the
+      // compute warps have read this one's: P^T and dS^T go over dP^T), dK of
+      // this tile (each half once the compute warps hand it over; the Q slot
+      // is then free), dV of this tile (the dO slot is then free), dP^T of the
+      // next tile (after the products that read the P^T / dS^T it
+      // overwrites: MMAs from one thread run in issue order).  Freeing each
+      // slot after its last product lets the next loads start a quarter of a
+      // step earlier than a shared Q / dO stage would.
+      uint32_t t_qf = 0, t_sf = 0;
       for (int u = 0; ok && u < n_it; ++u) {
-        const int gs = g + u, s = gs % NST;
-        for (int h = 0; h < 2; ++h) {
-          // Half h's warps have read S^T / dP^T and written P^T / dS^T over
-          // them: accumulate, then reuse the half's regions for the next step
-          // (MMAs from one thread run in issue order).
-          if (!(ok = wait_all(B_P(h), gs & 1))) break;
+        const int gs = g + u, s = gs % NST, g1 = gs + 1, s1 = g1 % NST;
+        const uint32_t par1 = (g1 / NST) & 1;
+        const bool more = u + 1 < n_it;
+        uint32_t t_p = 0;
+        if (more) {
+          if (!(ok = ready(t_qf, B_QF(s1), par1) && ready(t_sf, B_SF, gs & 1))) break;
+          t_p = mbar_test(B_P(0), gs & 1);
           tc_fence_after();
-          if (leader) {
-            issue_grads(s, h, u > 0 || h > 0);
-            if (h == 1) {
-              mma_commit(B_EMPTY(s));
-              if (u + 1 == n_it) mma_commit(B_DONE);
-            }
-          }
+          if (leader) issue_st(s1);
           __syncwarp();
-          if (u + 1 < n_it) {
-            const int g1 = gs + 1;
-            if (h == 0 && !(ok = wait_all(B_FULL(g1 % NST), (g1 / NST) & 1))) break;
-            tc_fence_after();
-            if (leader) issue_scores(g1 % NST, h);
-            __syncwarp();
-          }
+        }
+        if (!(ok = ready(t_p, B_P(0), gs & 1))) break;
+        t_p = mbar_test(B_P(1), gs & 1);
+        tc_fence_after();
+        if (leader) issue_grad(s, 0, true, u > 0);
+        __syncwarp();
+        if (!(ok = ready(t_p, B_P(1), gs & 1))) break;
+        const uint32_t t_df = more ? mbar_test(B_DF(s1), par1) : 0u;
+        if (u + 2 < n_it) {
+          t_qf = mbar_test(B_QF((gs + 2) % NST), ((gs + 2) / NST) & 1);
+          t_sf = mbar_test(B_SF, g1 & 1);
+        }
+        tc_fence_after();
+        if (leader) {
+          issue_grad(s, 1, true, true);
+          mma_commit(B_QE(s));
+          issue_grad(s, 0, false, u > 0);
+          issue_grad(s, 1, false, true);
+          mma_commit(B_DE(s));
+          if (!more) mma_commit(B_DONE);
+        }
+        __syncwarp();
+        if (more) {
+          if (!(ok = ready(t_df, B_DF(s1), par1))) break;
+          tc_fence_after();
+          if (leader) issue_dpt(s1);
+          __syncwarp();
         }
       }
       g += n_it;
@@ -550,15 +603,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = 0; u < itm.n_it; ++u) {
         const int gs = g + u, s = gs % NST;
         const int it = q_tile(itm, u);
-        ok = __all_sync(0xffffffffu, mbar_wait(B_FULL(s), (gs / NST) & 1, status, abort_flag)) &&
-             __all_sync(0xffffffffu, mbar_wait(B_S(h), gs & 1, status, abort_flag));
+        ok = __all_sync(0xffffffffu, mbar_wait(B_QF(s), (gs / NST) & 1, status, abort_flag)) &&
+             __all_sync(0xffffffffu, mbar_wait(B_S, gs & 1, status, abort_flag));
         if (!ok) break;
         tc_fence_after();
         // The stage's -L log2(e) and -delta, one per query column.
         const float *nl_s =
-            reinterpret_cast<const float *>(smem + C::OFF_STAGE + s * C::STAGE_BYTES + C::ST_LSE);
+            reinterpret_cast<const float *>(smem + C::OFF_QS + s * C::SLOT + C::SLOT_ROWS);
         const float *nd_s =
-            reinterpret_cast<const float *>(smem + C::OFF_STAGE + s * C::STAGE_BYTES + C::ST_DELTA);
+            reinterpret_cast<const float *>(smem + C::OFF_DS + s * C::SLOT + C::SLOT_ROWS);
         const bool diag = CAUSAL && it == itm.jt;
         // P^T for the half's 64 queries while the dP^T product is still running.
         const float2 sc2 = make_float2(scale_log2, scale_log2);
@@ -569,6 +622,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t sr[32];
           tmem_ld_32cols(tmem + lane_base + C::TM_ST + col0, sr);
           tmem_ld_wait_regs(sr);
+          if (c == 1) {
+            // This warp's S^T is in registers: once every warp's is, the
+            // region may take the next tile's S^T.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(B_SF);
+          }
 #pragma unroll
           for (int k = 0; k < 32; k += 4) {
             const float4 lv = *reinterpret_cast<const float4 *>(nl_s + col0 + k);
@@ -589,7 +649,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 64; ++e)
             if (64 * h + e < row) p[e] = 0.f;
         }
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(B_DP(h), gs & 1, status, abort_flag)))) break;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(B_DF(s), (gs / NST) & 1, status, abort_flag)) &&
+                   __all_sync(0xffffffffu, mbar_wait(B_DP, gs & 1, status, abort_flag))))
+          break;
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -613,8 +675,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             dk[k / 2] = pack_bf16x2(s0.x, s0.y);
             dk[k / 2 + 1] = pack_bf16x2(s1.x, s1.y);
           }
-          tmem_st_16cols(tmem + lane_base + C::TM_ST + 64 * h + 16 * c, pk);
-          tmem_st_16cols(tmem + lane_base + C::TM_DPT + 64 * h + 16 * c, dk);
+          // Over the dP^T columns just read: P^T then dS^T.
+          tmem_st_16cols(tmem + lane_base + C::TM_DPT + col0, pk);
+          tmem_st_16cols(tmem + lane_base + C::TM_DPT + col0 + 16, dk);
         }
         tmem_st_wait();
         // The stage's L / delta were read through the generic proxy and the
@@ -715,14 +778,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto B_FULL = [&](int s) { return bar0 + 8u * (1 + s); };
   auto B_EMPTY = [&](int s) { return bar0 + 8u * (1 + NST + s); };
   const uint32_t bar1 = bar0 + 8u * (1 + 2 * NST);
-  auto B_S = [&](int h) { return bar1 + 8u * h; };          // S half h in TMEM
+  const uint32_t B_S = bar1;                                   // S in TMEM
+  const uint32_t B_SF = bar1 + 8;                              // S read: region free
   auto B_DP = [&](int h) { return bar1 + 8u * (2 + h); };   // dP half h in TMEM
   auto B_P = [&](int h) { return bar1 + 8u * (4 + h); };    // dS half h written (over dP)
   const uint32_t B_DONE = bar1 + 48;
   const uint32_t B_DRAIN = bar1 + 56;
-  auto B_SF = [&](int h) { return bar1 + 64 + 8u * h; };    // S half h read: region free
-  const uint32_t B_QL = bar1 + 80;                             // Q, dO landed in shared memory
-  static_assert(1 + 2 * NST + 8 + 3 == C::NBAR, "barrier count");
+  const uint32_t B_QL = bar1 + 64;                             // Q, dO landed in shared memory
+  static_assert(1 + 2 * NST + 9 == C::NBAR, "barrier count");
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
   const uint32_t st_qdo = sb + C::OFF_STAGE + C::ST_QDO * C::STAGE_BYTES;
@@ -734,11 +797,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(B_FULL(s), 1);
       mbar_init(B_EMPTY(s), 1);
     }
+    mbar_init(B_S, 1);
+    mbar_init(B_SF, kComputeWarps);
     for (int h = 0; h < 2; ++h) {
-      mbar_init(B_S(h), 1);
       mbar_init(B_DP(h), 1);
       mbar_init(B_P(h), kComputeWarps / 2);
-      mbar_init(B_SF(h), kComputeWarps / 2);
     }
     mbar_init(B_DONE, 1);
     mbar_init(B_DRAIN, 1);
@@ -806,18 +869,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto wait_all = [&](uint32_t bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, abort_flag));
     };
-    // Half h of S = Q K^T and of dP = dO V^T: keys 64h..64h+63 of the tile;
-    // Q / dO from TMEM (8 columns per 16-element step of the head dim).
-    auto issue_s = [&](int s, int h) {
-      const uint32_t so = (s * C::STAGE_BYTES + h * 64 * 128) >> 4;
+    constexpr uint32_t kIdescS2 = make_idesc_bf16(BT, BT, 0, 0);
+    // S = Q K^T over the whole key tile (N = 128), Q from TMEM (8 columns per
+    // 16-element step of the head dim).
+    auto issue_s = [&](int s) {
+      const uint32_t so = (s * C::STAGE_BYTES) >> 4;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t koff = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-        mma_bf16_ts_lo(tmem + C::TM_S + 64 * h, tmem + C::TM_Q + 8 * kk,
-                       stk_lo + so + (C::ST_K >> 4) + koff, hi, kIdescS, kk > 0 ? 1u : 0u);
+        mma_bf16_ts_lo(tmem + C::TM_S, tmem + C::TM_Q + 8 * kk,
+                       stk_lo + so + (C::ST_K >> 4) + koff, hi, kIdescS2, kk > 0 ? 1u : 0u);
       }
-      mma_commit(B_S(h));
+      mma_commit(B_S);
     };
+    // Half h of dP = dO V^T: keys 64h..64h+63 of the tile, dO from TMEM.
     auto issue_dp = [&](int s, int h) {
       const uint32_t so = (s * C::STAGE_BYTES + h * 64 * 128) >> 4;
 #pragma unroll
@@ -840,12 +905,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                        stm_lo + so + (C::ST_K >> 4) + boff, hi, kIdescG, (acc || u > 0) ? 1u : 0u);
       }
     };
+    // Issuing an MMA waits while the tensor pipe's queue is full, so this
+    // warp is never far ahead of the pipe, and a barrier round trip between
+    // two batches would leave the pipe idle.  Each barrier is therefore
+    // tested (non-blocking, every lane) before the batch ahead of it and the
+    // result read after the batch; only a phase not yet complete then takes
+    // the bounded wait.
+    auto ready = [&](uint32_t t, uint32_t bar, uint32_t parity) {
+      return vote_all_ordered(t) || wait_all(bar, parity);
+    };
     bool ok = wait_all(B_Q, 0) && wait_all(B_FULL(0), 0);
     if (ok) {
       tc_fence_after();
       if (leader) {
-        issue_s(0, 0);
-        issue_s(0, 1);
+        issue_s(0);
         issue_dp(0, 0);
         issue_dp(0, 1);
       }
@@ -853,32 +926,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // Per key tile j: S of tile j + 1 goes out as soon as the compute warps
     // have read S of tile j (dS is written over dP, not over S), so the next
-    // tile's exponentials overlap this tile's dQ and dP products; dP of tile
-    // j + 1 follows dQ of tile j, which reads the dS it overwrites (MMAs from
-    // one thread run in issue order).
+    // tile's exponentials overlap this tile's dQ and dP products; dP half h
+    // of tile j + 1 follows dQ half h of tile j, which reads the dS it
+    // overwrites (MMAs from one thread run in issue order).
+    uint32_t t_full = 0, t_sf = 0;           // tests of the next tile's K/V and S-read phases
     for (int j = 0; ok && j < n_j; ++j) {
       const int s = j % NST, s1 = (j + 1) % NST;
       const bool more = j + 1 < n_j;
+      uint32_t t_p = 0;
       if (more) {
-        if (!(ok = wait_all(B_FULL(s1), ((j + 1) / NST) & 1))) break;
-        for (int h = 0; h < 2; ++h) {
-          if (!(ok = wait_all(B_SF(h), j & 1))) break;
-          tc_fence_after();
-          if (leader) issue_s(s1, h);
-          __syncwarp();
-        }
-        if (!ok) break;
-      }
-      for (int h = 0; h < 2; ++h) {
-        if (!(ok = wait_all(B_P(h), j & 1))) break;
+        if (!(ok = ready(t_full, B_FULL(s1), ((j + 1) / NST) & 1) && ready(t_sf, B_SF, j & 1)))
+          break;
+        t_p = mbar_test(B_P(0), j & 1);
         tc_fence_after();
-        if (leader) {
-          issue_dq(s, h, j > 0 || h > 0);
-          if (h == 1) mma_commit(more ? B_EMPTY(s) : B_DONE);
-          if (more) issue_dp(s1, h);
-        }
+        if (leader) issue_s(s1);
         __syncwarp();
       }
+      if (!(ok = ready(t_p, B_P(0), j & 1))) break;
+      t_p = mbar_test(B_P(1), j & 1);
+      tc_fence_after();
+      if (leader) {
+        issue_dq(s, 0, j > 0);
+        if (more) issue_dp(s1, 0);
+      }
+      __syncwarp();
+      if (!(ok = ready(t_p, B_P(1), j & 1))) break;
+      if (j + 2 < n_j) {
+        t_full = mbar_test(B_FULL((j + 2) % NST), ((j + 2) / NST) & 1);
+        t_sf = mbar_test(B_SF, (j + 1) & 1);
+      }
+      tc_fence_after();
+      if (leader) {
+        issue_dq(s, 1, true);
+        mma_commit(more ? B_EMPTY(s) : B_DONE);
+        if (more) issue_dp(s1, 1);
+      }
+      __syncwarp();
     }
     if (leader) {
       mma_commit(B_DRAIN);
@@ -932,7 +1015,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float2 nl2v = make_float2(nl, nl);
     const float2 nd2 = make_float2(nd, nd);
     for (int j = 0; ok && j < n_j; ++j) {
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(B_S(h), j & 1, status, abort_flag)))) break;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(B_S, j & 1, status, abort_flag)))) break;
       tc_fence_after();
       const bool diag = CAUSAL && j == it;
       const int kmax = N - j * BT;            // keys past the sequence are masked
@@ -944,10 +1027,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_32cols(tmem + lane_base + C::TM_S + col0, sr);
         tmem_ld_wait_regs(sr);
         if (c == 1) {
-          // The half's S is in registers: its region may take the next tile's S.
+          // This warp's S is in registers: once every warp's is, the region
+          // may take the next tile's S.
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(B_SF(h));
+          if (lane == 0) mbar_arrive(B_SF);
         }
 #pragma unroll
         for (int k = 0; k < 32; k += 2) {
