@@ -95,29 +95,30 @@ struct CfgKV {
   static_assert(TM_DPT + BT <= kTmemCols, "tensor memory budget");
 };
 
-// dQ kernel: shared memory = a ring of (K, V) tiles; TMEM S | dP (dS) | dQ |
-// Q | dO.  The query tile's Q and dO sit in TMEM as the A operands of
-// S = Q K^T and dP = dO V^T, so those products read only K / V from shared
-// memory (half the shared-memory operand traffic of two SS products).  Q and
-// dO arrive by TMA in the ring's last stage, which holds K / V only from the
-// third key tile on, after they have been copied into TMEM.
+// dQ kernel: shared memory = a ring of two-tile entries | a dQ staging tile;
+// TMEM S | dP (dS) | dQ | Q | dO.  The query tile's Q and dO sit in TMEM as
+// the A operands of S = Q K^T and dP = dO V^T, so those products read only
+// K / V from shared memory (half the shared-memory operand traffic of two SS
+// products).  The CTA is persistent; each item (query head, 128-query tile)
+// sends one entry through the ring with its Q and dO, which the compute warps
+// copy into TMEM, then one entry (K, V) per key tile.
 template <int D>
 struct CfgQ {
   static_assert(D == 64 || D == 128, "head dimension");
   static constexpr int KB = D / 64;
   static constexpr uint32_t TILE = BT * D * 2;
   static constexpr uint32_t OFF_STAGE = 0;
-  static constexpr uint32_t ST_K = 0;
-  static constexpr uint32_t ST_V = TILE;
+  static constexpr uint32_t ST_K = 0;                    // (Q in a Q / dO entry)
+  static constexpr uint32_t ST_V = TILE;                 // (dO in a Q / dO entry)
   static constexpr uint32_t STAGE_BYTES = 2 * TILE;
-  static constexpr int NST = (D == 64) ? 4 : 3;          // K/V ring depth
-  static constexpr uint32_t OFF_BAR = OFF_STAGE + NST * STAGE_BYTES;
+  static constexpr int NST = (D == 64) ? 4 : 3;          // ring depth
+  static constexpr uint32_t OFF_DQ = OFF_STAGE + NST * STAGE_BYTES;   // dQ (bf16) for its store
+  static constexpr uint32_t OFF_BAR = OFF_DQ + TILE;
   // q (Q, dO in TMEM), full[NST], empty[NST], s, s read, dp[2], p[2], done,
-  // drain, Q / dO landed
-  static constexpr int NBAR = 1 + 2 * NST + 9;
-  static constexpr int ST_QDO = NST - 1;                 // stage that first holds Q, dO
+  // drain, item ring full[kRing], empty[kRing]
+  static constexpr int NBAR = 1 + 2 * NST + 8 + 2 * kRing;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 4 * kRing;   // tmem slot, abort flag, item ring
   static constexpr uint32_t SMEM_ALLOC =
       SMEM_BYTES + 1024 > 118784u ? SMEM_BYTES + 1024 : 118784u;   // one CTA per SM
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
@@ -752,8 +753,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tmdO,
                        const __grid_constant__ CUtensorMap tmdQ,
                        const float *__restrict__ nl2, const float *__restrict__ ndl,
-                       int N, int N_pad, int H, int H_kv,
-                       int n_blk, float scale_log2, float scale, unsigned *status) {
+                       int N, int N_pad, int H, int H_kv, int BH, int n_blk, float scale_log2,
+                       float scale, unsigned *status, unsigned *sched) {
   using C = CfgQ<D>;
   constexpr int NST = C::NST;
   extern __shared__ uint8_t smem_raw[];
@@ -763,18 +764,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Causal: heads fastest, query tiles in descending order (longest first).
-  // Non-causal: query tiles fastest (co-resident CTAs share K/V through L2).
-  const int BH = static_cast<int>(gridDim.x) / n_blk;
-  const int bh = CAUSAL ? static_cast<int>(blockIdx.x % BH) : static_cast<int>(blockIdx.x / n_blk);
-  const int it = CAUSAL ? n_blk - 1 - static_cast<int>(blockIdx.x / BH)
-                        : static_cast<int>(blockIdx.x % n_blk);
+  // Work items are (query head, 128-query tile) pairs.  Causal: heads vary
+  // fastest and query tiles go in descending order (longest first);
+  // non-causal: query tiles vary fastest, so the CTAs working at the same
+  // time share a few heads' K/V through L2.  The CTA is persistent: it
+  // starts with item blockIdx and claims each further item from a global
+  // counter (sched[0]) once it has issued the current one's loads; the TMA
+  // warp hands the item indices to the others through a small ring in shared
+  // memory, and the last CTA to finish resets the counter.
+  const int n_items = BH * n_blk;
+  const int G = static_cast<int>(gridDim.x);
   const int group = H / H_kv;
-  const int kvh = (bh / H) * H_kv + (bh % H) / group;
-  const int n_j = CAUSAL ? it + 1 : n_blk;
+  struct Item {
+    int bh, kvh, it, n_j;   // query head, K/V head, query tile, key tiles
+  };
+  auto item_at = [&](int k, Item &w) {
+    if (k >= n_items) return false;
+    w.bh = CAUSAL ? k % BH : k / n_blk;
+    w.it = CAUSAL ? n_blk - 1 - k / BH : k % n_blk;
+    w.kvh = (w.bh / H) * H_kv + (w.bh % H) / group;
+    w.n_j = CAUSAL ? w.it + 1 : n_blk;
+    return true;
+  };
 
+  // Ring entries run on across items: item t's Q / dO entry, then its n_j
+  // (K, V) entries, then item t + 1's.  Per-step barriers (S, S read, dP,
+  // P) count key tiles over the CTA's whole sequence; Q-in-TMEM and done
+  // complete once per item.
   const uint32_t bar0 = sb + C::OFF_BAR;
-  const uint32_t B_Q = bar0;   // the compute warps have put Q and dO into TMEM
+  const uint32_t B_Q = bar0;   // the compute warps have put the item's Q and dO into TMEM
   auto B_FULL = [&](int s) { return bar0 + 8u * (1 + s); };
   auto B_EMPTY = [&](int s) { return bar0 + 8u * (1 + NST + s); };
   const uint32_t bar1 = bar0 + 8u * (1 + 2 * NST);
@@ -782,17 +800,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t B_SF = bar1 + 8;                              // S read: region free
   auto B_DP = [&](int h) { return bar1 + 8u * (2 + h); };   // dP half h in TMEM
   auto B_P = [&](int h) { return bar1 + 8u * (4 + h); };    // dS half h written (over dP)
-  const uint32_t B_DONE = bar1 + 48;
+  const uint32_t B_DONE = bar1 + 48;                           // item's last products done
   const uint32_t B_DRAIN = bar1 + 56;
-  const uint32_t B_QL = bar1 + 64;                             // Q, dO landed in shared memory
-  static_assert(1 + 2 * NST + 9 == C::NBAR, "barrier count");
+  auto B_IF = [&](int s) { return bar1 + 64 + 8u * s; };       // item slot s written
+  auto B_IE = [&](int s) { return bar1 + 64 + 8u * (kRing + s); };   // item slot s read by all
+  static_assert(1 + 2 * NST + 8 + 2 * kRing == C::NBAR, "barrier count");
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
-  const uint32_t st_qdo = sb + C::OFF_STAGE + C::ST_QDO * C::STAGE_BYTES;
+  volatile int *item_ring = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 16);
+  // The t-th item of this CTA as the TMA warp published it (warp-uniform).
+  auto take_item = [&](int t, Item &w, bool &ok) {
+    const int s = t % kRing;
+    if (!__all_sync(0xffffffffu, mbar_wait(B_IF(s), (t / kRing) & 1, status, abort_flag))) {
+      ok = false;
+      return false;
+    }
+    const int k = item_ring[s];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(B_IE(s));
+    return item_at(k, w);
+  };
 
   if (threadIdx.x == kWarpTMA * 32) {
     mbar_init(B_Q, kComputeWarps);
-    mbar_init(B_QL, 1);
     for (int s = 0; s < NST; ++s) {
       mbar_init(B_FULL(s), 1);
       mbar_init(B_EMPTY(s), 1);
@@ -805,17 +835,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(B_DONE, 1);
     mbar_init(B_DRAIN, 1);
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(B_IF(s), 1);
+      mbar_init(B_IE(s), 1 + kComputeWarps);   // the MMA warp and every compute warp
+    }
     *abort_flag = 0;
     fence_mbar_init();
-    // The query tile's Q and dO first (inputs of the whole call: no wait for
-    // the kernels before this one).
-    mbar_arrive_expect_tx(B_QL, 2 * C::TILE);
-    for (int kb = 0; kb < C::KB; ++kb) {
-      tma_load_3d(st_qdo + C::ST_K + kb * kBoxBytes, &tmQ, kb * 64, it * BT, bh, B_QL);
-      tma_load_3d(st_qdo + C::ST_V + kb * kBoxBytes, &tmdO, kb * 64, it * BT, bh, B_QL);
-    }
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmdO);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmdQ);
   }
   if (warp == kWarpMMA) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -828,31 +858,62 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpTMA) {
     // ------------------------------------------------------------ TMA
+    // (Q, dO, K and V are inputs of the whole call: no wait for the kernels
+    // launched before this one.)
     const bool leader = elect_one();
-    int issued = 0;
-    for (int j = 0; j < n_j; ++j) {
-      const int s = j % NST;
-      // The stage that held Q and dO is refilled once they are in TMEM.
-      if (j == C::ST_QDO && !__all_sync(0xffffffffu, mbar_wait(B_Q, 0, status, abort_flag)))
-        break;
-      if (!__all_sync(0xffffffffu,
-                      mbar_wait(B_EMPTY(s), ((j / NST) & 1) ^ 1u, status, abort_flag)))
+    int e = 0;                               // ring entries issued
+    bool ok = true;
+    int k = static_cast<int>(blockIdx.x);
+    // The next entry's slot, once the consumers of its previous use freed it.
+    auto next_slot = [&](uint32_t &st) {
+      const int s = e % NST;
+      st = sb + C::OFF_STAGE + s * C::STAGE_BYTES;
+      return __all_sync(0xffffffffu,
+                        mbar_wait(B_EMPTY(s), ((e / NST) & 1) ^ 1u, status, abort_flag));
+    };
+    for (int t = 0; ok; ++t) {
+      const int r = t % kRing;
+      if (!(ok = __all_sync(0xffffffffu,
+                            mbar_wait(B_IE(r), ((t / kRing) & 1) ^ 1u, status, abort_flag))))
         break;
       if (leader) {
-        const uint32_t st = sb + C::OFF_STAGE + s * C::STAGE_BYTES;
-        mbar_arrive_expect_tx(B_FULL(s), 2 * C::TILE);
+        item_ring[r] = k;
+        mbar_arrive(B_IF(r));
+      }
+      __syncwarp();
+      Item w;
+      if (!item_at(k, w)) break;
+      uint32_t st;
+      if (!(ok = next_slot(st))) break;
+      if (leader) {
+        mbar_arrive_expect_tx(B_FULL(e % NST), 2 * C::TILE);
         for (int kb = 0; kb < C::KB; ++kb) {
-          tma_load_3d(st + C::ST_K + kb * kBoxBytes, &tmK, kb * 64, j * BT, kvh, B_FULL(s));
-          tma_load_3d(st + C::ST_V + kb * kBoxBytes, &tmV, kb * 64, j * BT, kvh, B_FULL(s));
+          tma_load_3d(st + C::ST_K + kb * kBoxBytes, &tmQ, kb * 64, w.it * BT, w.bh, B_FULL(e % NST));
+          tma_load_3d(st + C::ST_V + kb * kBoxBytes, &tmdO, kb * 64, w.it * BT, w.bh, B_FULL(e % NST));
         }
       }
-      issued = j + 1;
+      ++e;
+      for (int j = 0; ok && j < w.n_j; ++j) {
+        if (!(ok = next_slot(st))) break;
+        if (leader) {
+          mbar_arrive_expect_tx(B_FULL(e % NST), 2 * C::TILE);
+          for (int kb = 0; kb < C::KB; ++kb) {
+            tma_load_3d(st + C::ST_K + kb * kBoxBytes, &tmK, kb * 64, j * BT, w.kvh, B_FULL(e % NST));
+            tma_load_3d(st + C::ST_V + kb * kBoxBytes, &tmV, kb * 64, j * BT, w.kvh, B_FULL(e % NST));
+          }
+        }
+        ++e;
+      }
+      // This item's loads are all issued: claim the next one.
+      int kn = 0;
+      if (lane == 0) kn = G + static_cast<int>(atomicAdd(sched, 1u));
+      k = __shfl_sync(0xffffffffu, kn, 0);
     }
     if (leader && *abort_flag) {
-      mbar_wait_drain(B_QL, 0, 100000000ull);
-      for (int u = 0; u < NST && u < issued; ++u) {
-        const int jj = issued - 1 - u;
-        mbar_wait_drain(B_FULL(jj % NST), (jj / NST) & 1, 100000000ull);
+      // Let every copy this warp started land before the CTA exits.
+      for (int u = 0; u < NST && u < e; ++u) {
+        const int x = e - 1 - u;
+        mbar_wait_drain(B_FULL(x % NST), (x / NST) & 1, 100000000ull);
       }
     }
     __syncwarp();
@@ -860,6 +921,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA
     const bool leader = elect_one();
     constexpr uint32_t kIdescS = make_idesc_bf16(BT, BT / 2, 0, 0);
+    constexpr uint32_t kIdescS2 = make_idesc_bf16(BT, BT, 0, 0);
     constexpr uint32_t kIdescG = make_idesc_bf16(BT, D, 0, 1);
     const uint64_t dst0 = make_sdesc_sw128(sb + C::OFF_STAGE, 16, 1024);
     const uint32_t hi = static_cast<uint32_t>(dst0 >> 32);
@@ -869,7 +931,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto wait_all = [&](uint32_t bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, abort_flag));
     };
-    constexpr uint32_t kIdescS2 = make_idesc_bf16(BT, BT, 0, 0);
     // S = Q K^T over the whole key tile (N = 128), Q from TMEM (8 columns per
     // 16-element step of the head dim).
     auto issue_s = [&](int s) {
@@ -911,57 +972,79 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tested (non-blocking, every lane) before the batch ahead of it and the
     // result read after the batch; only a phase not yet complete then takes
     // the bounded wait.
-    auto ready = [&](uint32_t t, uint32_t bar, uint32_t parity) {
-      return vote_all_ordered(t) || wait_all(bar, parity);
+    auto ready = [&](uint32_t tst, uint32_t bar, uint32_t parity) {
+      return vote_all_ordered(tst) || wait_all(bar, parity);
     };
-    bool ok = wait_all(B_Q, 0) && wait_all(B_FULL(0), 0);
-    if (ok) {
-      tc_fence_after();
-      if (leader) {
-        issue_s(0);
-        issue_dp(0, 0);
-        issue_dp(0, 1);
-      }
-      __syncwarp();
-    }
-    // Per key tile j: S of tile j + 1 goes out as soon as the compute warps
-    // have read S of tile j (dS is written over dP, not over S), so the next
-    // tile's exponentials overlap this tile's dQ and dP products; dP half h
-    // of tile j + 1 follows dQ half h of tile j, which reads the dS it
-    // overwrites (MMAs from one thread run in issue order).
-    uint32_t t_full = 0, t_sf = 0;           // tests of the next tile's K/V and S-read phases
-    for (int j = 0; ok && j < n_j; ++j) {
-      const int s = j % NST, s1 = (j + 1) % NST;
-      const bool more = j + 1 < n_j;
-      uint32_t t_p = 0;
-      if (more) {
-        if (!(ok = ready(t_full, B_FULL(s1), ((j + 1) / NST) & 1) && ready(t_sf, B_SF, j & 1)))
-          break;
-        t_p = mbar_test(B_P(0), j & 1);
+    bool ok = true;
+    int e = 0;                               // ring entries consumed
+    int g = 0;                               // key tiles of earlier items
+    for (int t = 0; ok; ++t) {
+      Item w;
+      if (!take_item(t, w, ok)) break;
+      const int n_j = w.n_j;
+      // The item's Q and dO are in TMEM once the compute warps have copied
+      // them out of its first entry (after their last reads of the previous
+      // item's S and the completion of its last dP products, the only
+      // readers of the old Q and dO): that entry's slot is free.  Its S and
+      // dP then overwrite regions whose previous contents the compute warps
+      // have read (S) or the previous item's last dQ products, issued before
+      // them, read (dS over dP).
+      ok = wait_all(B_Q, t & 1);
+      if (ok && leader) mbar_arrive(B_EMPTY(e % NST));
+      ++e;
+      ok = ok && wait_all(B_FULL(e % NST), (e / NST) & 1);
+      if (ok) {
         tc_fence_after();
-        if (leader) issue_s(s1);
+        if (leader) {
+          issue_s(e % NST);
+          issue_dp(e % NST, 0);
+          issue_dp(e % NST, 1);
+        }
         __syncwarp();
       }
-      if (!(ok = ready(t_p, B_P(0), j & 1))) break;
-      t_p = mbar_test(B_P(1), j & 1);
-      tc_fence_after();
-      if (leader) {
-        issue_dq(s, 0, j > 0);
-        if (more) issue_dp(s1, 0);
+      // Per key tile j: S of tile j + 1 goes out as soon as the compute
+      // warps have read S of tile j (dS is written over dP, not over S), so
+      // the next tile's exponentials overlap this tile's dQ and dP products;
+      // dP half h of tile j + 1 follows dQ half h of tile j, which reads the
+      // dS it overwrites (MMAs from one thread run in issue order).
+      uint32_t t_full = 0, t_sf = 0;         // tests of the next tile's K/V and S-read phases
+      for (int j = 0; ok && j < n_j; ++j) {
+        const int gs = g + j, ej = e + j, s = ej % NST, s1 = (ej + 1) % NST;
+        const bool more = j + 1 < n_j;
+        uint32_t t_p = 0;
+        if (more) {
+          if (!(ok = ready(t_full, B_FULL(s1), ((ej + 1) / NST) & 1) &&
+                     ready(t_sf, B_SF, gs & 1)))
+            break;
+          t_p = mbar_test(B_P(0), gs & 1);
+          tc_fence_after();
+          if (leader) issue_s(s1);
+          __syncwarp();
+        }
+        if (!(ok = ready(t_p, B_P(0), gs & 1))) break;
+        t_p = mbar_test(B_P(1), gs & 1);
+        tc_fence_after();
+        if (leader) {
+          issue_dq(s, 0, j > 0);
+          if (more) issue_dp(s1, 0);
+        }
+        __syncwarp();
+        if (!(ok = ready(t_p, B_P(1), gs & 1))) break;
+        if (j + 2 < n_j) {
+          t_full = mbar_test(B_FULL((ej + 2) % NST), ((ej + 2) / NST) & 1);
+          t_sf = mbar_test(B_SF, (gs + 1) & 1);
+        }
+        tc_fence_after();
+        if (leader) {
+          issue_dq(s, 1, true);
+          mma_commit(B_EMPTY(s));
+          if (more) issue_dp(s1, 1);
+          else mma_commit(B_DONE);
+        }
+        __syncwarp();
       }
-      __syncwarp();
-      if (!(ok = ready(t_p, B_P(1), j & 1))) break;
-      if (j + 2 < n_j) {
-        t_full = mbar_test(B_FULL((j + 2) % NST), ((j + 2) / NST) & 1);
-        t_sf = mbar_test(B_SF, (j + 1) & 1);
-      }
-      tc_fence_after();
-      if (leader) {
-        issue_dq(s, 1, true);
-        mma_commit(more ? B_EMPTY(s) : B_DONE);
-        if (more) issue_dp(s1, 1);
-      }
-      __syncwarp();
+      e += n_j;
+      g += n_j;
     }
     if (leader) {
       mma_commit(B_DRAIN);
@@ -974,111 +1057,152 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = warp >> 2;                 // key columns 64h .. 64h + 63
     const int row = 32 * q + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-    const size_t prow = static_cast<size_t>(bh) * N_pad + static_cast<size_t>(it) * BT + row;
+    const uint32_t st_dq = sb + C::OFF_DQ;
     // This kernel is a programmatic dependent of the dK/dV kernel, which
     // itself waited for the row pass: once that grid has finished, the row
     // pass's -L log2(e) and -delta are complete too.  (Q, dO, K and V are
-    // inputs: their loads and the first products do not wait.)  The row's
-    // two values load while Q and dO arrive.
+    // inputs: their loads and the first products do not wait.)
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const float nl = nl2[prow];
-    const float nd = ndl[prow];
-    bool ok = __all_sync(0xffffffffu, mbar_wait(B_QL, 0, status, abort_flag));
-    if (ok) {
-      // Warps of half 0 put this tile's Q rows into TMEM, warps of half 1
-      // its dO rows (row = lane, bf16 pairs along the columns; the TMA load
-      // left rows past N zero).  A 128-byte row of a box holds its 16-byte
-      // chunk v at position v ^ (row % 8) (128-byte swizzle), so the 32
-      // lanes' loads of one chunk fall in distinct banks.
-      const uint32_t src = st_qdo + (h == 0 ? C::ST_K : C::ST_V) + row * 128;
+    auto row_of = [&](const Item &w) {
+      return static_cast<size_t>(w.bh) * N_pad + static_cast<size_t>(w.it) * BT + row;
+    };
+    // Ring entry eq (an item's Q and dO) into TMEM: warps of half 0 copy the
+    // Q rows, warps of half 1 the dO rows (row = lane, bf16 pairs along the
+    // columns; the TMA load left rows past N zero).  A 128-byte row of a box
+    // holds its 16-byte chunk v at position v ^ (row % 8) (128-byte swizzle),
+    // so the 32 lanes' loads of one chunk fall in distinct banks.  Called
+    // after this warp's last reads of the previous item's S (half 0) or dP
+    // (half 1), so the previous item's S / dP products, the only readers of
+    // the old Q / dO, have completed.
+    auto copy_qdo = [&](int eq) {
+      const int s = eq % NST;
+      if (!__all_sync(0xffffffffu, mbar_wait(B_FULL(s), (eq / NST) & 1, status, abort_flag)))
+        return false;
+      const uint32_t src =
+          sb + C::OFF_STAGE + s * C::STAGE_BYTES + (h == 0 ? C::ST_K : C::ST_V) + row * 128;
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
-        uint32_t w[32];
+        uint32_t v[32];
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const uint4 x = ld_shared_v4(src + c * kBoxBytes + ((v ^ (row & 7)) << 4));
-          w[4 * v] = x.x;
-          w[4 * v + 1] = x.y;
-          w[4 * v + 2] = x.z;
-          w[4 * v + 3] = x.w;
+        for (int x = 0; x < 8; ++x) {
+          const uint4 y = ld_shared_v4(src + c * kBoxBytes + ((x ^ (row & 7)) << 4));
+          v[4 * x] = y.x;
+          v[4 * x + 1] = y.y;
+          v[4 * x + 2] = y.z;
+          v[4 * x + 3] = y.w;
         }
-        tmem_st_32cols(tmem + lane_base + (h == 0 ? C::TM_Q : C::TM_DO) + 32 * c, w);
+        tmem_st_32cols(tmem + lane_base + (h == 0 ? C::TM_Q : C::TM_DO) + 32 * c, v);
       }
       tmem_st_wait();
-      // The TMA warp refills this stage (async proxy) after the reads above.
+      // The TMA warp refills this slot (async proxy) after the reads above.
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(B_Q);
+      return true;
+    };
+    bool ok = true;
+    int e = 0;                               // ring entry of the current item's Q / dO
+    int g = 0;                               // key tiles of earlier items
+    Item cur;
+    bool have = take_item(0, cur, ok);
+    float nl = 0.f, nd = 0.f;
+    if (have) {
+      nl = nl2[row_of(cur)];
+      nd = ndl[row_of(cur)];
+      ok = copy_qdo(e);
     }
     const float2 sc2 = make_float2(scale_log2, scale_log2);
-    const float2 nl2v = make_float2(nl, nl);
-    const float2 nd2 = make_float2(nd, nd);
-    for (int j = 0; ok && j < n_j; ++j) {
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(B_S, j & 1, status, abort_flag)))) break;
-      tc_fence_after();
-      const bool diag = CAUSAL && j == it;
-      const int kmax = N - j * BT;            // keys past the sequence are masked
-      float p[64];
+    for (int t = 0;; ++t) {
+      // The compute warps agree at each item (and at its epilogue below) on
+      // whether to go on, so that they all take part in every named barrier
+      // or all leave: every one has the item and no wait has given up.
+      if (named_bar_any(kEpiBar, 32 * kComputeWarps, !(have && ok))) break;
+      const int n_j = cur.n_j;
+      const float2 nl2v = make_float2(nl, nl);
+      const float2 nd2 = make_float2(nd, nd);
+      for (int j = 0; ok && j < n_j; ++j) {
+        const int gs = g + j;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(B_S, gs & 1, status, abort_flag)))) break;
+        tc_fence_after();
+        const bool diag = CAUSAL && j == cur.it;
+        const int kmax = N - j * BT;          // keys past the sequence are masked
+        float p[64];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int col0 = 64 * h + 32 * c;
-        uint32_t sr[32];
-        tmem_ld_32cols(tmem + lane_base + C::TM_S + col0, sr);
-        tmem_ld_wait_regs(sr);
-        if (c == 1) {
-          // This warp's S is in registers: once every warp's is, the region
-          // may take the next tile's S.
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(B_SF);
-        }
+        for (int c = 0; c < 2; ++c) {
+          const int col0 = 64 * h + 32 * c;
+          uint32_t sr[32];
+          tmem_ld_32cols(tmem + lane_base + C::TM_S + col0, sr);
+          tmem_ld_wait_regs(sr);
+          if (c == 1) {
+            // This warp's S is in registers: once every warp's is, the
+            // region may take the next tile's S.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(B_SF);
+          }
 #pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          const float2 x =
-              ffma2(make_float2(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), sc2, nl2v);
-          p[32 * c + k] = ex2_approx(x.x);
-          p[32 * c + k + 1] = ex2_approx(x.y);
+          for (int k = 0; k < 32; k += 2) {
+            const float2 x =
+                ffma2(make_float2(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), sc2, nl2v);
+            p[32 * c + k] = ex2_approx(x.x);
+            p[32 * c + k + 1] = ex2_approx(x.y);
+          }
         }
+        if (diag || kmax < BT) {   // (warp-uniform) key after query, or past N: masked
+#pragma unroll
+          for (int x = 0; x < 64; ++x) {
+            const int col = 64 * h + x;
+            if ((diag && col > row) || col >= kmax) p[x] = 0.f;
+          }
+        }
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(B_DP(h), gs & 1, status, abort_flag))))
+          break;
+        tc_fence_after();
+        // dS as bf16 pairs over the first 32 columns of the half's dP region
+        // (chunk c's 16 columns over dP columns already read).
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int col0 = 64 * h + 32 * c;
+          uint32_t dp[32];
+          tmem_ld_32cols(tmem + lane_base + C::TM_DP + col0, dp);
+          tmem_ld_wait_regs(dp);
+          uint32_t dk[16];
+#pragma unroll
+          for (int k = 0; k < 32; k += 2) {
+            const float2 d =
+                fadd2(make_float2(__uint_as_float(dp[k]), __uint_as_float(dp[k + 1])), nd2);
+            const float2 ds = fmul2(make_float2(p[32 * c + k], p[32 * c + k + 1]), d);
+            dk[k / 2] = pack_bf16x2(ds.x, ds.y);
+          }
+          tmem_st_16cols(tmem + lane_base + C::TM_DP + 64 * h + 16 * c, dk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(B_P(h));
       }
-      if (diag || kmax < BT) {   // (warp-uniform) key after query, or past N: masked
-#pragma unroll
-        for (int e = 0; e < 64; ++e) {
-          const int col = 64 * h + e;
-          if ((diag && col > row) || col >= kmax) p[e] = 0.f;
-        }
+      // The next item's Q and dO go into TMEM before this item's epilogue,
+      // so that its first products overlap the epilogue.
+      Item nxt;
+      const bool have_next = ok && take_item(t + 1, nxt, ok);
+      float nl_n = 0.f, nd_n = 0.f;
+      if (have_next) {
+        nl_n = nl2[row_of(nxt)];
+        nd_n = ndl[row_of(nxt)];
+        ok = copy_qdo(e + 1 + n_j);
       }
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(B_DP(h), j & 1, status, abort_flag)))) break;
-      tc_fence_after();
-      // dS as bf16 pairs over the first 32 columns of the half's dP region
-      // (chunk c's 16 columns over dP columns already read).
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int col0 = 64 * h + 32 * c;
-        uint32_t dp[32];
-        tmem_ld_32cols(tmem + lane_base + C::TM_DP + col0, dp);
-        tmem_ld_wait_regs(dp);
-        uint32_t dk[16];
-#pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          const float2 d =
-              fadd2(make_float2(__uint_as_float(dp[k]), __uint_as_float(dp[k + 1])), nd2);
-          const float2 ds = fmul2(make_float2(p[32 * c + k], p[32 * c + k + 1]), d);
-          dk[k / 2] = pack_bf16x2(ds.x, ds.y);
-        }
-        tmem_st_16cols(tmem + lane_base + C::TM_DP + 64 * h + 16 * c, dk);
+      // Epilogue: dQ staged as bf16 and stored by TMA.  The staging tile is
+      // rewritten once the previous item's store has read it; the next
+      // item's first dQ product overwrites the accumulator only after these
+      // warps hand over its first dS, after the reads below.
+      const bool okd = ok && __all_sync(0xffffffffu, mbar_wait(B_DONE, t & 1, status, abort_flag));
+      if (threadIdx.x == 0) bulk_wait_group_read0();
+      if (named_bar_any(kEpiBar, 32 * kComputeWarps, !okd)) {
+        ok = false;
+        break;
       }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(B_P(h));
-    }
-    // Epilogue: dQ staged as bf16 in stage 0's K slot (every K/V load has
-    // been consumed once the last products are done) and stored by TMA.
-    const bool okd = ok && __all_sync(0xffffffffu, mbar_wait(B_DONE, 0, status, abort_flag));
-    if (!named_bar_any(kEpiBar, 32 * kComputeWarps, !okd)) {
       tc_fence_after();
-      const uint32_t st_dq = sb + C::OFF_STAGE + C::ST_K;
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         uint32_t r[32];
@@ -1087,21 +1211,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         stage_row32(st_dq, row, h * (D / 2) + 32 * c, r, scale);
       }
       fence_proxy_async_smem();
+      tc_fence_before();
       named_bar_sync(kEpiBar, 32 * kComputeWarps);
       if (threadIdx.x == 0) {
 #pragma unroll
         for (int kb = 0; kb < C::KB; ++kb)
-          tma_store_3d(&tmdQ, kb * 64, it * BT, bh, st_dq + kb * kBoxBytes);
+          tma_store_3d(&tmdQ, kb * 64, cur.it * BT, cur.bh, st_dq + kb * kBoxBytes);
         bulk_commit_group();
-        bulk_wait_group_read0();
       }
+      e += 1 + n_j;
+      g += n_j;
+      cur = nxt;
+      have = have_next;
+      nl = nl_n;
+      nd = nd_n;
     }
+    // The last store must have read shared memory before the CTA exits.
+    if (threadIdx.x == 0) bulk_wait_group_read0();
   }
   tc_fence_before();
   __syncthreads();
   if (warp == kWarpMMA) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  }
+  // Every claim of this CTA is behind it: the last CTA to get here resets
+  // the item counter (sched[0]) and this count (sched[1]) for the next launch.
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(sched + 1, 1u) == gridDim.x - 1) {
+      atomicExch(sched, 0u);
+      atomicExch(sched + 1, 0u);
+    }
   }
 }
 
@@ -1142,10 +1283,15 @@ static cudaError_t launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const 
   e = cudaLaunchKernelEx(&cfg, kkv, mq, mk, mv, mdo, mdk, mdv, nl2, ndl, N, N_pad, H, H_kv,
                          B * H_kv, n_blk, scale_log2, scale, status, sched);
   if (e != cudaSuccess) return e;
-  cfg.gridDim = dim3(static_cast<unsigned>(B * H * n_blk));
+  // dQ: persistent as well, one CTA per SM (at most one per item).
+  unsigned *sched_q = nullptr;
+  e = sched_slot(&sched_q);
+  if (e != cudaSuccess) return e;
+  const long long q_items = static_cast<long long>(B) * H * n_blk;
+  cfg.gridDim = dim3(static_cast<unsigned>(q_items < sm_count() ? q_items : sm_count()));
   cfg.dynamicSmemBytes = CfgQ<D>::SMEM_ALLOC;
-  return cudaLaunchKernelEx(&cfg, kq, mq, mk, mv, mdo, mdq, nl2, ndl, N, N_pad, H, H_kv,
-                            n_blk, scale_log2, scale, status);
+  return cudaLaunchKernelEx(&cfg, kq, mq, mk, mv, mdo, mdq, nl2, ndl, N, N_pad, H, H_kv, B * H,
+                            n_blk, scale_log2, scale, status, sched_q);
 }
 
 }  // namespace bwd
