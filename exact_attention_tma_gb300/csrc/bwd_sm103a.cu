@@ -363,10 +363,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpTMA) {
     // ------------------------------------------------------------ TMA
-    // L and delta come from the row pass launched just before this kernel
-    // (programmatic dependent launch): wait for it before the first load.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     const bool leader = elect_one();
+    // -L log2(e) and -delta come from the row pass launched just before this
+    // kernel (programmatic dependent launch): the first load of them waits
+    // for it; Q, dO, K and V are inputs of the whole call and load at once.
+    bool rows_ready = false;
     int g = 0;                               // stages issued so far
     int gd = 0;                              // dO loads issued so far
     int kv_items = 1;                        // items whose K/V load was issued
@@ -386,6 +387,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(B_QF(s), C::SLOT_TX);
         for (int kb = 0; kb < C::KB; ++kb)
           tma_load_3d(st + kb * kBoxBytes, &tmQ, kb * 64, qt * BT, bh, B_QF(s));
+        if (!rows_ready) {
+          asm volatile("griddepcontrol.wait;" ::: "memory");
+          rows_ready = true;
+        }
         bulk_load_1d(st + C::SLOT_ROWS, nl2 + row0, BT * 4, B_QF(s));
       }
       ++g;
