@@ -232,11 +232,11 @@ size_t attn_fwd_fp8_workspace_bytes(int B, int H, int N, int d);
  *   scale, causal: those of the forward call.
  *
  * dQ, dK and dV are overwritten (never accumulated into) and must not overlap
- * any input.  Three launches on `stream`: a row pass (rowsum(dO * O) and LSE
- * in base 2 into the workspace), a dK/dV kernel (one CTA per K/V head and
- * 128-key tile; a persistent grid of one CTA per SM that claims those items
- * from a per-launch counter) and a dQ kernel (one CTA per query head and
- * 128-query tile).
+ * any input.  Three launches on `stream`: a row pass (-rowsum(dO * O) and -LSE
+ * in base 2 into the workspace), a dK/dV kernel (items: K/V head and 128-key
+ * tile) and a dQ kernel (items: query head and 128-query tile), each on a
+ * persistent grid of one CTA per SM that claims its items from a per-launch
+ * counter.
  * No atomics: results are identical from run to run.  The workspace
  * (attn_bwd_workspace_bytes) is library-owned and grow-only as for
  * attn_decode, with the same synchronisation and stream caveats; it is not
