@@ -131,14 +131,18 @@ def test_bwd_workload_sampled():
 
 
 @pytest.mark.parametrize("causal", [False, True])
-def test_bwd_many_short_items_per_persistent_cta(causal):
-    """The persistent dK/dV kernel over far more (K/V head, key tile) items
-    than SMs, two key tiles per head: each CTA runs many items in a row, with
-    dK/dV leaving through the K/V slots that the next item reloads.  Batches
-    at the start, middle and end of the item order are checked against the
-    oracle in full."""
-    B, H, H_kv, N, d = 96, 4, 2, 200, 128   # 192 K/V heads x 2 key tiles = 384 items
-    q, k, v, do = bwd_inputs(B, H, N, d, seed=77 + causal, device="cuda", H_kv=H_kv)
+@pytest.mark.parametrize("N,d", [(200, 128), (200, 64), (100, 128)])
+def test_bwd_many_short_items_per_persistent_cta(causal, N, d):
+    """Both persistent gradient kernels over far more items than SMs: (K/V
+    head, key tile) items for dK/dV, with dK/dV leaving through the K/V slots
+    that the next item reloads, and (query head, query tile) items for dQ,
+    whose Q and dO travel through the K/V ring and enter TMEM during the
+    previous item's epilogue (N = 100: one key tile per item, so Q / dO and
+    K / V entries alternate in the ring; N = 200: a ragged second tile).
+    Batches at the start, middle and end of the item order are checked
+    against the oracle in full."""
+    B, H, H_kv = 96, 4, 2   # N = 200: 192 K/V heads x 2 key tiles = 384 dK/dV items, 768 dQ items
+    q, k, v, do = bwd_inputs(B, H, N, d, seed=77 + causal + N + d, device="cuda", H_kv=H_kv)
     scale = d ** -0.5
     o, lse = _oracle_fwd(q, k, v, scale, causal)
     dq, dk, dv = _bwd(q, k, v, o, do, lse, causal, scale)
