@@ -42,6 +42,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <type_traits>
 #include <cmath>
 
 #include "internal.h"
@@ -495,15 +496,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // Half h of dK += dS^T Q (dk) or dV += P^T dO (!dk): the 16-query steps
     // 4h..4h+3, A from TMEM, B = the slot's Q / dO, MN-major.  The compute
-    // warps left query chunk c (32 columns) of half h as P^T in dP^T columns
-    // 64h + 32c .. +15 and dS^T in 64h + 32c + 16 .. +31 (8 columns per step).
+    // warps left query step u (16 queries) of half h as P^T in dP^T columns
+    // 64h + 16u .. +7 and dS^T in 64h + 16u + 8 .. +15.
     auto issue_grad = [&](int s, int h, bool dk, bool acc) {
       const uint32_t so = (s * C::SLOT) >> 4;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int kk = 4 * h + u;
         const uint32_t boff = (kk * 16 * 128) >> 4;
-        const uint32_t col = C::TM_DPT + 64 * h + 32 * (u >> 1) + 8 * (u & 1) + (dk ? 16 : 0);
+        const uint32_t col = C::TM_DPT + 64 * h + 16 * u + (dk ? 8 : 0);
         mma_bf16_ts_lo(tmem + (dk ? C::TM_DK : C::TM_DV), tmem + col,
                        (dk ? qm_lo : dm_lo) + so + boff, hi, kIdescG, (acc || u > 0) ? 1u : 0u);
       }
@@ -659,31 +660,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                    __all_sync(0xffffffffu, mbar_wait(B_DP, gs & 1, status, abort_flag))))
           break;
         tc_fence_after();
+        {
+          // dS^T = P^T (dP^T - delta) in four 16-query steps, each loading the
+          // next step's dP^T columns while it computes; P^T and dS^T of a step
+          // (bf16 pairs, 8 columns each) go over its 16 dP^T columns.
+          const uint32_t dbase = tmem + lane_base + C::TM_DPT + 64 * h;
+          uint32_t da[16], db[16];
+          auto dstep = [&](auto kc, const uint32_t (&dp)[16]) {
+            constexpr int k = decltype(kc)::value;
+            uint32_t w[16];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int col0 = 64 * h + 32 * c;
-          uint32_t dp[32];
-          tmem_ld_32cols(tmem + lane_base + C::TM_DPT + col0, dp);
-          tmem_ld_wait_regs(dp);
-          uint32_t pk[16], dk[16];
-#pragma unroll
-          for (int k = 0; k < 32; k += 4) {
-            const float4 dv = *reinterpret_cast<const float4 *>(nd_s + col0 + k);
-            const float2 d0 = fadd2(make_float2(__uint_as_float(dp[k]), __uint_as_float(dp[k + 1])),
-                                    make_float2(dv.x, dv.y));
-            const float2 d1 = fadd2(
-                make_float2(__uint_as_float(dp[k + 2]), __uint_as_float(dp[k + 3])),
-                make_float2(dv.z, dv.w));
-            const float2 s0 = fmul2(make_float2(p[32 * c + k], p[32 * c + k + 1]), d0);
-            const float2 s1 = fmul2(make_float2(p[32 * c + k + 2], p[32 * c + k + 3]), d1);
-            pk[k / 2] = pack_bf16x2(p[32 * c + k], p[32 * c + k + 1]);
-            pk[k / 2 + 1] = pack_bf16x2(p[32 * c + k + 2], p[32 * c + k + 3]);
-            dk[k / 2] = pack_bf16x2(s0.x, s0.y);
-            dk[k / 2 + 1] = pack_bf16x2(s1.x, s1.y);
-          }
-          // Over the dP^T columns just read: P^T then dS^T.
-          tmem_st_16cols(tmem + lane_base + C::TM_DPT + col0, pk);
-          tmem_st_16cols(tmem + lane_base + C::TM_DPT + col0 + 16, dk);
+            for (int i = 0; i < 16; i += 4) {
+              const float4 dv = *reinterpret_cast<const float4 *>(nd_s + 64 * h + 16 * k + i);
+              const float2 d0 = fadd2(make_float2(__uint_as_float(dp[i]), __uint_as_float(dp[i + 1])),
+                                      make_float2(dv.x, dv.y));
+              const float2 d1 = fadd2(
+                  make_float2(__uint_as_float(dp[i + 2]), __uint_as_float(dp[i + 3])),
+                  make_float2(dv.z, dv.w));
+              const float2 s0 = fmul2(make_float2(p[16 * k + i], p[16 * k + i + 1]), d0);
+              const float2 s1 = fmul2(make_float2(p[16 * k + i + 2], p[16 * k + i + 3]), d1);
+              w[i / 2] = pack_bf16x2(p[16 * k + i], p[16 * k + i + 1]);
+              w[i / 2 + 1] = pack_bf16x2(p[16 * k + i + 2], p[16 * k + i + 3]);
+              w[8 + i / 2] = pack_bf16x2(s0.x, s0.y);
+              w[8 + i / 2 + 1] = pack_bf16x2(s1.x, s1.y);
+            }
+            tmem_st_16cols(dbase + 16 * k, w);
+          };
+          tmem_ld_16cols(dbase, da);
+          tmem_ld_wait_regs16(da);
+          tmem_ld_16cols(dbase + 16, db);
+          dstep(std::integral_constant<int, 0>(), da);
+          tmem_ld_wait_regs16(db);
+          tmem_ld_16cols(dbase + 32, da);
+          dstep(std::integral_constant<int, 1>(), db);
+          tmem_ld_wait_regs16(da);
+          tmem_ld_16cols(dbase + 48, db);
+          dstep(std::integral_constant<int, 2>(), da);
+          tmem_ld_wait_regs16(db);
+          dstep(std::integral_constant<int, 3>(), db);
         }
         tmem_st_wait();
         // The stage's L / delta were read through the generic proxy and the
