@@ -652,7 +652,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t stage_base = sb + C::OFF_OST + (C::NSTG == 1 ? 0 : i) * C::O_TILE;
       const uint32_t stage = stage_base + static_cast<uint32_t>(r) * 128;
       const uint32_t o_addr = tmem + lane_addr + C::TMEM_O + (kIndep ? 2 * i * D : i * D) + h * (D / 2);
-#pragma unroll
       if constexpr (kIndep) {
         // 16 columns of each half's accumulator at a time (both are live).
 #pragma unroll
