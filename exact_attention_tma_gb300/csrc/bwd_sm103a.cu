@@ -17,17 +17,18 @@
 //             adds), into a workspace padded to whole 128-row tiles (padding:
 //             delta = 0, L = +inf, so padded query rows get P = 0 in every
 //             tile that reads them);
-//   2. dK/dV: one CTA per (K/V head, 128-key tile).  K and V stay in shared
-//             memory; the query tiles of every query head of the group stream
-//             through a two-stage TMA ring (Q, dO, L, delta).  Per query tile
-//             the MMA warp computes S^T = K Q^T and dP^T = V dO^T into TMEM,
-//             eight compute warps turn them into P^T and dS^T (bf16, written
-//             back over S^T and dP^T), and the MMA warp accumulates
-//             dV += P^T dO and dK += dS^T Q in TMEM.  Summing over the group's
-//             query heads in the loop gives grouped-query K/V gradients
-//             without atomics.
-//   3. dQ:    one CTA per (query head, 128-query tile); K/V tiles stream
-//             through the ring; S = Q K^T and dP = dO V^T into TMEM, dS back
+//   2. dK/dV: items (K/V head, 128-key tile) on a persistent grid.  K and V
+//             stay in shared memory; the query tiles of every query head of
+//             the group stream through two TMA rings ((Q, -L) and
+//             (dO, -delta)).  Per query tile the MMA warp computes
+//             S^T = K Q^T and dP^T = V dO^T into TMEM, eight compute warps turn
+//             them into P^T and dS^T (bf16, written over dP^T), and the MMA
+//             warp accumulates dK += dS^T Q and dV += P^T dO in TMEM.  Summing
+//             over the group's query heads in the loop gives grouped-query K/V
+//             gradients without atomics.
+//   3. dQ:    items (query head, 128-query tile) on a persistent grid; each
+//             item's Q and dO, then its K/V tiles, stream through one ring;
+//             Q and dO go into TMEM, S = Q K^T and dP = dO V^T into TMEM, dS
 //             over dP, dQ += dS K in TMEM.
 // dQ is computed by its own kernel (recomputing S and dP once more) rather
 // than accumulated with atomics across the dK/dV CTAs: the gradient
@@ -42,8 +43,8 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
-#include <type_traits>
 #include <cmath>
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -220,12 +221,13 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   return v;
 }
 
-// Both kernels run two independent pipelines, one per half of the 128-wide
-// score tile (query columns 0-63 / 64-127 in the dK/dV kernel, key columns
-// in the dQ kernel).  Compute warps 4h..4h+3 own half h; the MMA warp issues
-// each half's score products (N = 64) as soon as that half's region is free
-// and each half's gradient products as soon as that half's P / dS are in.
-// While one half's warps compute, the tensor pipe works on the other half.
+// In both kernels compute warps 4h..4h+3 own half h of the 128-wide score
+// tile (query columns 0-63 / 64-127 in the dK/dV kernel, key columns in the
+// dQ kernel) and hand it over on a barrier of its own; the MMA warp issues
+// each half's gradient products (and, in the dQ kernel, its dP product for
+// the next tile) as soon as that half is in, so one half's element work
+// overlaps the other half's products.  The score product S (S^T) of the
+// next tile goes out whole once every warp has read the current one.
 
 // ------------------------------------------------------------------ dK / dV
 template <int D, bool CAUSAL>
@@ -276,8 +278,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   auto q_tile = [&](const Item &it, int t) { return it.it0 + t % it.n_q; };
 
-  // Barrier phases run on across items: the stage ring counts stages over
-  // the CTA's whole sequence, S/dP/P count steps, K/V, K/V-free and done
+  // Barrier phases run on across items: the Q and dO rings count query tiles
+  // over the CTA's whole sequence, S/dP/P count steps, K/V, K/V-free and done
   // complete once per item.
   const uint32_t bar0 = sb + C::OFF_BAR;
   const uint32_t B_KV = bar0;                                  // K, V of the item loaded
@@ -456,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t kIdescG = make_idesc_bf16(BT, D, 0, 1);
     // Low words of the shared-memory descriptors (one common high word):
     // K-major (head dim contiguous, 16-element k-steps inside a 64-column
-    // box) and MN-major (the stage's Q / dO as B operands with the query
+    // box) and MN-major (a slot's Q / dO as B operands with the query
     // index as the reduction dimension: 16-row k-steps, 64-column boxes
     // kBoxBytes apart).
     const uint64_t dK0 = make_sdesc_sw128(sb + C::OFF_K, 16, 1024);
@@ -614,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
              __all_sync(0xffffffffu, mbar_wait(B_S, gs & 1, status, abort_flag));
         if (!ok) break;
         tc_fence_after();
-        // The stage's -L log2(e) and -delta, one per query column.
+        // The slots' -L log2(e) and -delta, one per query column.
         const float *nl_s =
             reinterpret_cast<const float *>(smem + C::OFF_QS + s * C::SLOT + C::SLOT_ROWS);
         const float *nd_s =
@@ -700,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           dstep(std::integral_constant<int, 3>(), db);
         }
         tmem_st_wait();
-        // The stage's L / delta were read through the generic proxy and the
+        // The slots' -L / -delta were read through the generic proxy and the
         // next TMA refill writes them through the async proxy.
         fence_proxy_async_smem();
         tc_fence_before();
