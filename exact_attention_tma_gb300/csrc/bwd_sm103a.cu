@@ -1079,11 +1079,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = 32 * q + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
     const uint32_t st_dq = sb + C::OFF_DQ;
-    // This kernel is a programmatic dependent of the dK/dV kernel, which
-    // itself waited for the row pass: once that grid has finished, the row
-    // pass's -L log2(e) and -delta are complete too.  (Q, dO, K and V are
-    // inputs: their loads and the first products do not wait.)
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     auto row_of = [&](const Item &w) {
       return static_cast<size_t>(w.bh) * N_pad + static_cast<size_t>(w.it) * BT + row;
     };
@@ -1127,11 +1122,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     int g = 0;                               // key tiles of earlier items
     Item cur;
     bool have = take_item(0, cur, ok);
+    if (have) ok = copy_qdo(e);
+    // This kernel is a programmatic dependent of the dK/dV kernel, which
+    // itself waited for the row pass: once that grid has finished, the row
+    // pass's -L log2(e) and -delta are complete too.  Q, dO, K and V are
+    // inputs: the first item's Q / dO copy above and its first products do
+    // not wait.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     float nl = 0.f, nd = 0.f;
     if (have) {
       nl = nl2[row_of(cur)];
       nd = ndl[row_of(cur)];
-      ok = copy_qdo(e);
     }
     const float2 sc2 = make_float2(scale_log2, scale_log2);
     for (int t = 0;; ++t) {
