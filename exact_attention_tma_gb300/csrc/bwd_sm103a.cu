@@ -613,8 +613,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = 0; u < itm.n_it; ++u) {
         const int gs = g + u, s = gs % NST;
         const int it = q_tile(itm, u);
-        ok = __all_sync(0xffffffffu, mbar_wait(B_QF(s), (gs / NST) & 1, status, abort_flag)) &&
-             __all_sync(0xffffffffu, mbar_wait(B_S, gs & 1, status, abort_flag));
+        // (Usually both complete already: tested together, they cost one
+        // shared-memory round trip instead of two on the warps' chain.)
+        ok = mbar_wait2_all(B_QF(s), (gs / NST) & 1, B_S, gs & 1, status, abort_flag);
         if (!ok) break;
         tc_fence_after();
         // The slots' -L log2(e) and -delta, one per query column.
@@ -659,8 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 64; ++e)
             if (64 * h + e < row) p[e] = 0.f;
         }
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(B_DF(s), (gs / NST) & 1, status, abort_flag)) &&
-                   __all_sync(0xffffffffu, mbar_wait(B_DP, gs & 1, status, abort_flag))))
+        if (!(ok = mbar_wait2_all(B_DF(s), (gs / NST) & 1, B_DP, gs & 1, status, abort_flag)))
           break;
         tc_fence_after();
         {

@@ -122,6 +122,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
   return mbar_wait_limit(bar, parity, status, abort_flag, kWaitLimitNs);
 }
 
+// Warp-wide wait for two phases.  Both are tested first, back to back, so
+// that their shared-memory round trips overlap (two waits one after the
+// other pay two); only a phase not complete yet then takes the bounded wait.
+__device__ __forceinline__ bool mbar_wait2_all(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1,
+                                               unsigned *status, volatile int *abort_flag) {
+  const uint32_t t0 = mbar_test(b0, p0);
+  const uint32_t t1 = mbar_test(b1, p1);
+  if (vote_all_ordered(t0 & t1)) return true;
+  return __all_sync(0xffffffffu, t0 != 0 || mbar_wait(b0, p0, status, abort_flag)) &&
+         __all_sync(0xffffffffu, t1 != 0 || mbar_wait(b1, p1, status, abort_flag));
+}
+
 // Same as mbar_wait but without the abort flag (used while draining).
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity,
                                                 unsigned long long limit_ns) {
